@@ -1,0 +1,143 @@
+"""CPU oracle for the decode-time MSA lightning indexer -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It wraps ``msa_oracle.c`` (plain C,
+fp64) through ctypes and shares no code with the CUDA library.  See the
+header of ``msa_oracle.c`` for what each function computes and the passages
+of the pages it follows.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Tuple
+
+import numpy as np
+
+HEADS = 4
+DIM = 128
+PAGE = 128
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "msa_oracle.c")
+BUILD_DIR = os.path.join(_HERE, "_build")
+LIBRARY = os.path.join(BUILD_DIR, "libmsa_oracle.so")
+
+_lock = threading.Lock()
+_default = None
+
+
+def build(src: str = SOURCE, out: str = LIBRARY, openmp: bool = True) -> str:
+    """Compile the oracle into a shared library with gcc (host only)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    cmd = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-Wall", "-Wextra"]
+    if openmp:
+        cmd.append("-fopenmp")
+    cmd += ["-o", out + ".tmp", src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(out + ".tmp", out)
+    return out
+
+
+def _needs_build(out: str, src: str) -> bool:
+    return not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src)
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library."""
+
+    def __init__(self, path: str):
+        self.path = path
+        lib = ctypes.CDLL(path)
+        c_i64, c_int = ctypes.c_int64, ctypes.c_int
+        P = ctypes.c_void_p
+        lib.msa_oracle_block_scores.argtypes = [P, P, c_i64, P, c_i64, P, c_int, P]
+        lib.msa_oracle_block_scores.restype = c_int
+        lib.msa_oracle_select.argtypes = [P, c_int, c_i64, P, c_int, c_int, c_int, P, P]
+        lib.msa_oracle_select.restype = c_int
+        lib.msa_oracle_select_split.argtypes = [P, c_int, c_i64, P, c_int, c_int, c_int, c_i64, P, P]
+        lib.msa_oracle_select_split.restype = c_int
+        lib.msa_oracle_num_threads.argtypes = []
+        lib.msa_oracle_num_threads.restype = c_int
+        self.lib = lib
+
+    @staticmethod
+    def _ptr(a: np.ndarray) -> int:
+        return a.ctypes.data
+
+    def num_threads(self) -> int:
+        return int(self.lib.msa_oracle_num_threads())
+
+    def block_scores(self, q: np.ndarray, pool: np.ndarray, block_table: np.ndarray,
+                     seq_lens: np.ndarray) -> np.ndarray:
+        """fp64 block scores [B, 4, bt_stride]; -inf past each row's last block."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        pool = np.ascontiguousarray(pool, dtype=np.uint16)
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        seq = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        B, stride = bt.shape
+        assert q.shape == (B, HEADS, DIM) and seq.shape == (B,)
+        assert pool.ndim == 3 and pool.shape[1:] == (PAGE, DIM)
+        out = np.empty((B, HEADS, stride), dtype=np.float64)
+        rc = self.lib.msa_oracle_block_scores(self._ptr(q), self._ptr(pool), pool.shape[0],
+                                              self._ptr(bt), stride, self._ptr(seq), B,
+                                              self._ptr(out))
+        if rc != 0:
+            raise ValueError(f"oracle refused the inputs (code {rc})")
+        return out
+
+    def select(self, scores: np.ndarray, seq_lens: np.ndarray, k: int, n_sink: int,
+               n_window: int) -> Tuple[np.ndarray, np.ndarray]:
+        """Per-head selection: (ids int32 [B,4,k], scores fp64 [B,4,k])."""
+        scores = np.ascontiguousarray(scores, dtype=np.float64)
+        seq = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        B, H, stride = scores.shape
+        assert H == HEADS and seq.shape == (B,)
+        ids = np.empty((B, HEADS, k), dtype=np.int32)
+        out = np.empty((B, HEADS, k), dtype=np.float64)
+        rc = self.lib.msa_oracle_select(self._ptr(scores), B, stride, self._ptr(seq), k, n_sink,
+                                        n_window, self._ptr(ids), self._ptr(out))
+        if rc != 0:
+            raise ValueError(f"oracle refused the selection arguments (code {rc})")
+        return ids, out
+
+    def select_split(self, scores: np.ndarray, seq_lens: np.ndarray, k: int, n_sink: int,
+                     n_window: int, split_blocks: int) -> Tuple[np.ndarray, np.ndarray]:
+        """The selection reached through contiguous splits of `split_blocks` blocks."""
+        scores = np.ascontiguousarray(scores, dtype=np.float64)
+        seq = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        B, H, stride = scores.shape
+        ids = np.empty((B, HEADS, k), dtype=np.int32)
+        out = np.empty((B, HEADS, k), dtype=np.float64)
+        rc = self.lib.msa_oracle_select_split(self._ptr(scores), B, stride, self._ptr(seq), k,
+                                              n_sink, n_window, split_blocks, self._ptr(ids),
+                                              self._ptr(out))
+        if rc != 0:
+            raise ValueError(f"oracle refused the selection arguments (code {rc})")
+        return ids, out
+
+    def run(self, w, k: Optional[int] = None, n_sink: Optional[int] = None,
+            n_window: Optional[int] = None):
+        """Block scores and selection for a `workloads.Workload`."""
+        k = w.k if k is None else k
+        n_sink = w.n_sink if n_sink is None else n_sink
+        n_window = w.n_window if n_window is None else n_window
+        s = self.block_scores(w.q, w.pool, w.block_table, w.seq_lens)
+        ids, sc = self.select(s, w.seq_lens, k, n_sink, n_window)
+        return s, ids, sc
+
+
+def load(path: Optional[str] = None) -> Oracle:
+    """The oracle library (built on first use when missing or stale)."""
+    global _default
+    if path is not None:
+        return Oracle(path)
+    with _lock:
+        if _default is None:
+            if _needs_build(LIBRARY, SOURCE):
+                build()
+            _default = Oracle(LIBRARY)
+        return _default

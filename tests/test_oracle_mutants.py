@@ -1,0 +1,51 @@
+"""Plant plausible mistakes in copies of the oracle and require the pins to catch each.
+
+Every mutant is built on the CPU from a modified copy of oracle/msa_oracle.c
+in a temporary directory; the real oracle is never touched.
+"""
+
+import os
+
+import pytest
+
+import oracle
+import oracle_pins as pins
+
+MUTANTS = [
+    ("drop the last dimension", "d < DIM; ++d", "d < DIM - 1; ++d"),
+    ("read the whole last page", "if (valid > PAGE)\n                    valid = PAGE;", "valid = PAGE;"),
+    ("skip the last valid token", "t < valid; ++t", "t < valid - 1; ++t"),
+    ("head 0's query for every head", "q + ((int64_t)b * HEADS + h) * DIM", "q + ((int64_t)b * HEADS) * DIM"),
+    ("min instead of max", "if (dot > best)", "if (best == -INFINITY || dot < best)"),
+    ("transposed key tile",
+     "bf16_to_double(krow[d])",
+     "bf16_to_double(pool[((int64_t)page * DIM + d) * PAGE + t])"),
+    ("scaled scores", "if (dot > best)", "dot *= 0.08838834764831845;\n                    if (dot > best)"),
+    ("tie-break toward the higher id",
+     "if (a->id < b->id)\n        return -1;\n    if (a->id > b->id)\n        return 1;",
+     "if (a->id < b->id)\n        return 1;\n    if (a->id > b->id)\n        return -1;"),
+    ("lower score first",
+     "if (a->score > b->score)\n        return -1;\n    if (a->score < b->score)\n        return 1;",
+     "if (a->score > b->score)\n        return 1;\n    if (a->score < b->score)\n        return -1;"),
+    ("window pin off by one", "|| j >= nb - n_window;", "|| j > nb - n_window;"),
+    ("sink pin off by one", "return j < n_sink ||", "return j <= n_sink ||"),
+    ("pad ids with 0", "out_ids[filled] = -1;", "out_ids[filled] = 0;"),
+    ("bf16 read as the low half", "((uint32_t)bits) << 16", "((uint32_t)bits) << 15"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new):
+    src = open(oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation anchor for {name!r} not found exactly once"
+    mutated = tmp_path / "msa_oracle_mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.build(src=str(mutated), out=str(tmp_path / "libmutant.so"))
+    mutant = oracle.load(lib)
+    caught = []
+    for check in pins.ALL_CHECKS:
+        try:
+            check(mutant)
+        except (AssertionError, ValueError):
+            caught.append(check.__name__)
+    assert caught, f"no pin caught the mutant {name!r}"
