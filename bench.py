@@ -1,0 +1,409 @@
+"""Benchmark of the decode-time MSA lightning indexer on GB300.
+
+One step = one decode call of the whole hot path (block scores, pins, per-head
+top-16: the score kernel then the merge kernel) over the long-context batch:
+32 requests x 131072 tokens, 4 index heads, d=128, 128-token pages, a 1 GiB
+shuffled index-K pool.  The metric is index-K GB/s (algorithmic bytes: every
+valid token's 128 bf16 values once) with us/call beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the batch on its
+own GPU; there is no data-path collective (weak scaling), only a barrier and
+a max over ranks of the timed interval.  `--impl reference` times the CPU
+oracle (the method's plain definition in fp64) on the host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "indexer decode µs/call and index-K HBM GB/s (B=32, 128K ctx) vs GB300 peak"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "score_kernel_long_context.md")
+CSRC = os.path.join(ROOT, "sparse_attention_decode_gb300", "csrc")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=32,
+                    help="requests per step (32 is the headline workload; smaller only for profiling)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------
+# ranks
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is None:
+        return
+    if device is not None and dist.get_backend() == "nccl":
+        dist.barrier(device_ids=[device.index])
+    else:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    """The largest per-rank value (the job's wall interval is the slowest rank's)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=device if (device is not None and dist.get_backend() == "nccl") else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(batch: int):
+    """DRAM bytes per score launch from the committed ncu summary, if it is current."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_bytes = re.search(r"dram_bytes_per_launch_full_batch:\s*([0-9]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1)) * batch // 32
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the GPU is busy."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu):
+        self.gpu = gpu  # nvidia-smi selector (UUID) or None for every GPU
+        self.proc = None
+
+    def start(self):
+        try:
+            sel = ["-i", str(self.gpu)] if self.gpu is not None else []
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 *sel, "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            text, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            text, _ = self.proc.communicate()
+        rows = []
+        for line in text.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[3], parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for _, _, _, flags in rows:
+            for n, v in zip(names[1:], flags[1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        sm = [r[0] for r in rows]
+        busy = sorted(sm)[len(sm) // 2:]  # the upper half: samples taken under load
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# our implementation
+# ----------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import sparse_attention_decode_gb300 as msa
+    import workloads as wl
+
+    world, rank, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = init_dist(world, "nccl")
+    msa.load()
+
+    w = wl.long_context(batch=args.batch)
+    B, k, L = w.batch, w.k, w.max_model_len
+    bytes_per_step = w.index_k_bytes
+    q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).to(device)
+    pool = torch.from_numpy(w.pool.view(np.int16)).view(torch.bfloat16).to(device)
+    bt = torch.from_numpy(w.block_table).to(device)
+    seq = torch.from_numpy(w.seq_lens).to(device)
+    ids = torch.empty((B, 4, k), dtype=torch.int32, device=device)
+    sc = torch.empty((B, 4, k), dtype=torch.float32, device=device)
+    ws = msa.new_workspace(B, L, k, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        msa.msa_indexer_score(q, pool, bt, seq, k, w.n_sink, w.n_window, ws, max_model_len=L,
+                              stream=stream)
+        msa.msa_indexer_merge(B, k, ids, sc, ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(device)
+    assert msa.msa_indexer_get_error(ws, stream=stream) == 0
+
+    uuid = getattr(torch.cuda.get_device_properties(device), "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else None)
+    sampler.start()
+    t_soak = time.time()
+    while time.time() - t_soak < 1.5:  # keep the GPU busy so the clock samples see load
+        for _ in range(50):
+            step()
+        torch.cuda.synchronize(device)
+
+    # --- timed region: exactly K steps --------------------------------------
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 * args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    start.record(stream)
+    for i in range(args.steps):
+        ev[3 * i].record(stream)
+        msa.msa_indexer_score(q, pool, bt, seq, k, w.n_sink, w.n_window, ws, max_model_len=L,
+                              stream=stream)
+        ev[3 * i + 1].record(stream)
+        msa.msa_indexer_merge(B, k, ids, sc, ws, stream=stream)
+        ev[3 * i + 2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    clocks = sampler.stop()
+    local_ms = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(dist, local_ms, device)
+    score_ms = statistics.mean(ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(args.steps))
+    merge_ms = statistics.mean(ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(args.steps))
+    gpu_launches = 2 * args.steps
+    assert msa.msa_indexer_get_error(ws, stream=stream) == 0
+
+    # --- end to end through the C ABI with host buffers ----------------------
+    e2e = None
+    if not args.no_e2e:
+        h_q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_bt = torch.from_numpy(w.block_table).pin_memory()
+        h_seq = torch.from_numpy(w.seq_lens).pin_memory()
+        h_ids = torch.empty((B, 4, k), dtype=torch.int32).pin_memory()
+        h_sc = torch.empty((B, 4, k), dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_bt, h_seq))
+        d2h = sum(t.numel() * t.element_size() for t in (h_ids, h_sc))
+
+        def e2e_step():
+            q.copy_(h_q, non_blocking=True)
+            bt.copy_(h_bt, non_blocking=True)
+            seq.copy_(h_seq, non_blocking=True)
+            msa.msa_indexer_decode(q, pool, bt, seq, k, w.n_sink, w.n_window, ids, sc, ws,
+                                   max_model_len=L, stream=stream)
+            h_ids.copy_(ids, non_blocking=True)
+            h_sc.copy_(sc, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(dist, device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(dist, device)
+        e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, device)
+        e2e = {"value": round(world * bytes_per_step / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+               "us_per_call": round(e2e_ms * 1e3, 2), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        return None
+
+    peak, peak_src = measured_hbm_peak()
+    achieved = bytes_per_step / (score_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(world * bytes_per_step / (ms * 1e-3) / 1e9, 2),
+        "unit": UNIT,
+        "us_per_call": round(ms * 1e3, 2),
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"long_context: B={B} x 131072 tokens, 4 index heads, d=128, 128-token "
+                        f"pages, k=16, n_sink=1, n_window=2, {w.num_pages}-page shuffled pool",
+            "batch": B, "seq_len": 131072, "index_k_bytes_per_step": bytes_per_step,
+            "split_blocks": "auto", "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (1 GiB index-K pool vs 129 MB L2); no flush",
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "score_kernel", "achieved": round(achieved, 1),
+            "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(B),
+            "score_us": round(score_ms * 1e3, 2), "merge_us": round(merge_ms * 1e3, 2),
+        },
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, bytes_per_step)
+    return line
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle (baseline leg and reference arm)
+# ----------------------------------------------------------------------------
+
+def _oracle_pass(orc, w, rows):
+    import numpy as np
+    sub_q, sub_bt, sub_seq = w.q[:rows], w.block_table[:rows], w.seq_lens[:rows]
+    t0 = time.perf_counter()
+    s = orc.block_scores(sub_q, w.pool, sub_bt, sub_seq)
+    orc.select(s, sub_seq, w.k, w.n_sink, w.n_window)
+    dt = time.perf_counter() - t0
+    return dt, int(np.asarray(sub_seq, dtype=np.int64).sum()) * 128 * 2
+
+
+def cpu_baseline(w, bytes_per_step, budget_s: float = 12.0):
+    """The oracle, as it stands, on the host cores over a bounded sample of the batch."""
+    import oracle
+    orc = oracle.load()
+    dt, nbytes = _oracle_pass(orc, w, 1)  # one request first, to size the sample
+    rows = max(1, min(w.batch, int(budget_s / 3 / max(dt, 1e-6))))
+    times = []
+    t_all = time.perf_counter()
+    while len(times) < 3 and time.perf_counter() - t_all < budget_s:
+        dt, nbytes = _oracle_pass(orc, w, rows)
+        times.append(dt)
+    med = statistics.median(times)
+    return {"value": round(nbytes / med / 1e9, 4), "unit": UNIT, "cores": orc.num_threads(),
+            "kind": "oracle",
+            "sample": f"first {rows} of {w.batch} requests of the same batch "
+                      f"({nbytes} index-K bytes), {len(times)} passes, median"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import workloads as wl
+    import oracle
+    w = wl.long_context(batch=args.batch)
+    orc = oracle.load()
+    dt1, _ = _oracle_pass(orc, w, 1)
+    # each step: as many requests as fit ~1.5 s, so K + W steps end within minutes
+    rows = max(1, min(w.batch, int(1.5 / max(dt1, 1e-6))))
+    for _ in range(args.warmup):
+        _oracle_pass(orc, w, rows)
+    times, nbytes = [], 0
+    for _ in range(args.steps):
+        dt, nbytes = _oracle_pass(orc, w, rows)
+        times.append(dt)
+    per_step = sum(times) / len(times)
+    value = round(nbytes / per_step / 1e9, 4)
+    sample = (f"first {rows} of {w.batch} requests of the long_context batch per step "
+              f"({nbytes} index-K bytes)")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": UNIT,
+        "us_per_call": round(per_step * 1e6, 1),
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per_step * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"long_context: B={w.batch} x 131072 tokens (CPU oracle sample)",
+                   "batch": w.batch, "seq_len": 131072, "sample_requests": rows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

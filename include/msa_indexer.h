@@ -1,0 +1,183 @@
+/*
+ * msa_indexer.h -- C ABI of the decode-time MSA lightning indexer on GB300.
+ *
+ * What the library computes.  For each decode request b and each of the four
+ * index-query heads h, every 128-token block j of the request's paged,
+ * single-head index-K cache gets the score
+ *
+ *     s[b,h,j] = max over valid tokens t of block j of  sum_d q[b,h,d] * K[page(b,j),t,d]
+ *
+ * with fp32 accumulation and no scale (TensorRT-LLM PR #17008, "Description":
+ * a full-kv_len MQA max-score pass that scores every KV block so top-k can
+ * pick 16; vLLM blog "Following the Bottleneck: Optimizing MiniMax M3 on AMD
+ * Instinct MI355X", section 2: the positive score scale was removed because
+ * only the top-k order matters).  Each head then keeps its own top-k blocks
+ * (vLLM PR #57832, "Solution", steps 3-4), with the first n_sink and the last
+ * n_window blocks pinned inside the k outputs (same page, "Solution": forced
+ * init/sink and sliding-window blocks are pinned; SGLang PR #41488,
+ * "Modifications": initial/recent block priorities are preserved).
+ *
+ * Fixed shapes: 4 index heads, head dim 128, 128-token pages, bf16 inputs
+ * (vLLM PR #57832, "Problem": index heads == KV heads == 4, one shared
+ * index-K head; SGLang PR #41488, "Modifications": dimension 128, 128-token
+ * blocks, top-k 16).
+ *
+ * Output order per (b, h): the pinned blocks in increasing block id, then the
+ * other selected blocks by higher score first and, on equal fp32 scores,
+ * lower block id first.  Ids are logical block indices within the request.
+ * Unused slots (fewer than k blocks, or an empty request) hold id -1 and
+ * score -inf.  The reported score of every selected block, pinned ones
+ * included, is its fp32 block score.
+ *
+ * Memory.  Every pointer is device memory owned by the caller; the library
+ * allocates, frees and synchronises nothing inside msa_indexer_decode /
+ * _score / _merge.  All work is enqueued on `stream` (a cudaStream_t passed
+ * as void*; NULL = the legacy default stream), so the calls can be recorded
+ * into a CUDA graph.  Kernel shapes depend only on the bounds (batch,
+ * max_model_len, split_blocks) and the SM count, never on the live seq_lens
+ * (vLLM PR #57832, "CUDA graph capture": kernel shapes must be
+ * capture-stable and come from max_model_len; block counts are runtime
+ * values).
+ *
+ * Errors.  Argument errors are returned synchronously before anything is
+ * enqueued.  Bad device data is not an error status (the host never reads
+ * it): a seq_len outside [0, min(max_model_len, 128*bt_stride)] makes that
+ * request empty (ids -1 / scores -inf); a block-table entry outside
+ * [0, num_pages) makes that block score -inf and excludes it from the
+ * selection.  Both set a bit in the workspace fault word, read (and cleared)
+ * by msa_indexer_get_error().  No kernel traps or waits without bound.
+ *
+ * Concurrency.  The library keeps no state between calls except in the
+ * caller's workspace.  Calls that may overlap on the GPU need separate
+ * workspaces.
+ */
+#ifndef MSA_INDEXER_H
+#define MSA_INDEXER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MSA_NUM_HEADS 4
+#define MSA_HEAD_DIM 128
+#define MSA_PAGE_TOKENS 128
+#define MSA_MAX_TOPK 32     /* largest k accepted */
+#define MSA_MAX_BATCH 4096  /* largest batch / max_batch accepted */
+#define MSA_MAX_GRID 1024   /* bound on score CTAs used to size auto-mode workspaces */
+
+typedef enum msa_status {
+    MSA_OK = 0,
+    MSA_ERR_INVALID_ARG = 1,         /* a null pointer, a bad size or an unaligned pointer */
+    MSA_ERR_UNSUPPORTED = 2,         /* a size the kernels do not handle (k > MSA_MAX_TOPK, ...) */
+    MSA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes below msa_indexer_workspace_bytes() */
+    MSA_ERR_CUDA = 4                 /* a CUDA runtime call or a launch failed */
+} msa_status;
+
+/* Bits of the workspace fault word (see msa_indexer_get_error). */
+#define MSA_FAULT_SEQ_LEN 0x1u /* a seq_len outside [0, min(max_model_len, 128*bt_stride)] */
+#define MSA_FAULT_PAGE_ID 0x2u /* a block-table entry outside [0, num_pages) */
+#define MSA_FAULT_TIMEOUT 0x4u /* a bounded wait inside a kernel ran out (work was skipped) */
+#define MSA_FAULT_SLOTS 0x8u   /* the workspace held fewer candidate slots than needed */
+
+/*
+ * Bytes of device workspace the calls below need for any batch <= max_batch
+ * and any seq_len <= max_model_len, with top-k `k` and split width
+ * `split_blocks` (0 = automatic).  Depends on the bounds only.  Returns 0
+ * for arguments the library rejects.
+ *
+ * The workspace must be zero-filled once before its first use (for example
+ * cudaMemset or torch.zeros); afterwards the library keeps it consistent.
+ * It is 256-byte aligned storage owned by the caller.
+ */
+size_t msa_indexer_workspace_bytes(int max_batch, int max_model_len, int k, int split_blocks);
+
+/*
+ * One decode step of the indexer: block scores, pins, per-head top-k.
+ * Enqueues two kernels on `stream`: msa_indexer_score() then
+ * msa_indexer_merge().
+ *
+ *   q             bf16 [batch, 4, 128], contiguous, 16-byte aligned; the
+ *                 post-RoPE index queries (SGLang PR #41488, "Modifications":
+ *                 the existing post-RoPE queries are used).
+ *   kcache_pool   bf16 [num_pages, 128, 128] (page, token, dim), contiguous,
+ *                 16-byte aligned; the paged single-head index-K cache.
+ *   num_pages     pages in the pool, 1 <= num_pages <= 2^24.
+ *   block_table   int32 [batch, bt_stride]; entry (b, j) is the physical
+ *                 page of logical block j of request b.  Only entries
+ *                 j < ceil(seq_lens[b] / 128) are read.
+ *   bt_stride     row stride of block_table in entries, >= 1.
+ *   seq_lens      int32 [batch]: tokens of request b, the current one included.
+ *   batch         requests, 0 <= batch <= max_batch (0 enqueues nothing).
+ *   max_batch     the bound the workspace was sized for, <= MSA_MAX_BATCH.
+ *   max_model_len the bound on seq_len the workspace was sized for, >= 1.
+ *   k             outputs per head, 1 <= k <= MSA_MAX_TOPK.
+ *   n_sink        leading blocks pinned, >= 0.
+ *   n_window      trailing blocks pinned, >= 0; n_sink + n_window <= k.
+ *   out_ids       int32 [batch, 4, k]: selected logical block ids.
+ *   out_scores    fp32  [batch, 4, k]: their fp32 block scores.
+ *   out_block_scores  optional fp32 [batch, 4, bt_stride]: every block's
+ *                 score (entries j >= ceil(seq_len/128) are left untouched);
+ *                 NULL to skip.
+ *   workspace     caller-owned device scratch of workspace_bytes bytes,
+ *                 >= msa_indexer_workspace_bytes(max_batch, max_model_len,
+ *                 k, split_blocks), 256-byte aligned, zero-filled before its
+ *                 first use.
+ *   split_blocks  pages each score work unit covers; 0 = automatic (the
+ *                 batch's pages spread evenly over one CTA per SM).  Any
+ *                 value gives bitwise-identical results.
+ *   stream        cudaStream_t as void*.
+ *
+ * Returns MSA_OK when both kernels were enqueued.
+ */
+msa_status msa_indexer_decode(const void *q, const void *kcache_pool, int64_t num_pages,
+                              const int32_t *block_table, int64_t bt_stride,
+                              const int32_t *seq_lens, int batch, int max_batch,
+                              int max_model_len, int k, int n_sink, int n_window,
+                              int32_t *out_ids, float *out_scores, float *out_block_scores,
+                              void *workspace, size_t workspace_bytes, int split_blocks,
+                              void *stream);
+
+/*
+ * The first stage of msa_indexer_decode alone: gathers every page of every
+ * request once (all four heads scored while the tile is resident), forms the
+ * block scores and the packed (score, block id) keys, and leaves each work
+ * unit's own top-k per head in the workspace.  Keeping the full top-k per
+ * unit makes the later merge exact (vLLM PR #57832, "Solution": a block in a
+ * head's global top-k is necessarily in its own shard's top-k).  Same
+ * arguments as msa_indexer_decode minus the outputs.
+ */
+msa_status msa_indexer_score(const void *q, const void *kcache_pool, int64_t num_pages,
+                             const int32_t *block_table, int64_t bt_stride,
+                             const int32_t *seq_lens, int batch, int max_batch,
+                             int max_model_len, int k, int n_sink, int n_window,
+                             float *out_block_scores, void *workspace, size_t workspace_bytes,
+                             int split_blocks, void *stream);
+
+/*
+ * The second stage alone: merges the per-unit top-k lists that the last
+ * msa_indexer_score() on this workspace left, per (request, head), into the
+ * exact top-k (vLLM PR #57832, "Solution", step 4: merge per head) and
+ * writes out_ids / out_scores.  `batch` and `k` must equal those of that
+ * msa_indexer_score() call.
+ */
+msa_status msa_indexer_merge(int batch, int k, int32_t *out_ids, float *out_scores,
+                             const void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Reads the workspace fault word (MSA_FAULT_* bits) into *flags and clears
+ * it.  Synchronises `stream`.  Returns MSA_ERR_INVALID_ARG for null
+ * pointers, MSA_ERR_CUDA if a CUDA call fails.
+ */
+msa_status msa_indexer_get_error(void *workspace, void *stream, uint32_t *flags);
+
+/* A static, human-readable name for a status code. */
+const char *msa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_INDEXER_H */

@@ -1,0 +1,175 @@
+"""Thin ctypes binding of libmsa_indexer.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and passes
+device pointers of torch tensors straight through; all compute runs in the
+CUDA kernels of the library.  If the library has not been built, importing
+the package still works but every call raises: there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import build as _build
+
+MSA_OK = 0
+MSA_ERR_INVALID_ARG = 1
+MSA_ERR_UNSUPPORTED = 2
+MSA_ERR_WORKSPACE_TOO_SMALL = 3
+MSA_ERR_CUDA = 4
+
+MSA_FAULT_SEQ_LEN = 0x1
+MSA_FAULT_PAGE_ID = 0x2
+MSA_FAULT_TIMEOUT = 0x4
+MSA_FAULT_SLOTS = 0x8
+
+MSA_NUM_HEADS = 4
+MSA_HEAD_DIM = 128
+MSA_PAGE_TOKENS = 128
+MSA_MAX_TOPK = 32
+MSA_MAX_BATCH = 4096
+
+EXPORTED = (
+    "msa_indexer_workspace_bytes",
+    "msa_indexer_decode",
+    "msa_indexer_score",
+    "msa_indexer_merge",
+    "msa_indexer_get_error",
+    "msa_status_string",
+)
+
+_lib = None
+
+
+class MsaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {msa_status_string(status)} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIBRARY
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """The compiled library; raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIBRARY
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"CUDA library {p} is missing; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(p)
+    c_i64, c_int, c_size, P = ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+    lib.msa_indexer_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int]
+    lib.msa_indexer_workspace_bytes.restype = c_size
+    common = [P, P, c_i64, P, c_i64, P, c_int, c_int, c_int, c_int, c_int, c_int]
+    lib.msa_indexer_decode.argtypes = common + [P, P, P, P, c_size, c_int, P]
+    lib.msa_indexer_decode.restype = c_int
+    lib.msa_indexer_score.argtypes = common + [P, P, c_size, c_int, P]
+    lib.msa_indexer_score.restype = c_int
+    lib.msa_indexer_merge.argtypes = [c_int, c_int, P, P, P, c_size, P]
+    lib.msa_indexer_merge.restype = c_int
+    lib.msa_indexer_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.msa_indexer_get_error.restype = c_int
+    lib.msa_status_string.argtypes = [c_int]
+    lib.msa_status_string.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return int(t.data_ptr())
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _check(status: int, what: str) -> None:
+    if status != MSA_OK:
+        raise MsaError(status, what)
+
+
+def msa_status_string(status: int) -> str:
+    return load().msa_status_string(int(status)).decode()
+
+
+def msa_indexer_workspace_bytes(max_batch: int, max_model_len: int, k: int,
+                                split_blocks: int = 0) -> int:
+    return int(load().msa_indexer_workspace_bytes(max_batch, max_model_len, k, split_blocks))
+
+
+def _shape_args(q, kcache_pool, block_table, seq_lens):
+    import torch
+    assert q.dtype == torch.bfloat16 and q.is_contiguous() and q.dim() == 3, "q: bf16 [B,4,128]"
+    assert tuple(q.shape[1:]) == (MSA_NUM_HEADS, MSA_HEAD_DIM), "q: bf16 [B,4,128]"
+    assert kcache_pool.dtype == torch.bfloat16 and kcache_pool.is_contiguous(), "kcache_pool: bf16"
+    assert tuple(kcache_pool.shape[1:]) == (MSA_PAGE_TOKENS, MSA_HEAD_DIM), "kcache_pool: [P,128,128]"
+    assert block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.stride(1) == 1
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+    B = int(q.shape[0])
+    assert block_table.shape[0] == B and seq_lens.shape[0] == B
+    return B, int(kcache_pool.shape[0]), int(block_table.stride(0))
+
+
+def msa_indexer_decode(q, kcache_pool, block_table, seq_lens, k: int, n_sink: int, n_window: int,
+                       out_ids, out_scores, workspace, *, max_batch: Optional[int] = None,
+                       max_model_len: int, out_block_scores=None, split_blocks: int = 0,
+                       stream=None) -> None:
+    """msa_indexer_decode() on torch CUDA tensors; raises MsaError on a bad status."""
+    B, num_pages, bt_stride = _shape_args(q, kcache_pool, block_table, seq_lens)
+    st = load().msa_indexer_decode(
+        _ptr(q), _ptr(kcache_pool), num_pages, _ptr(block_table), bt_stride, _ptr(seq_lens), B,
+        B if max_batch is None else max_batch, max_model_len, k, n_sink, n_window, _ptr(out_ids),
+        _ptr(out_scores), _ptr(out_block_scores), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), split_blocks, _stream_ptr(stream))
+    _check(st, "msa_indexer_decode")
+
+
+def msa_indexer_score(q, kcache_pool, block_table, seq_lens, k: int, n_sink: int, n_window: int,
+                      workspace, *, max_batch: Optional[int] = None, max_model_len: int,
+                      out_block_scores=None, split_blocks: int = 0, stream=None) -> None:
+    B, num_pages, bt_stride = _shape_args(q, kcache_pool, block_table, seq_lens)
+    st = load().msa_indexer_score(
+        _ptr(q), _ptr(kcache_pool), num_pages, _ptr(block_table), bt_stride, _ptr(seq_lens), B,
+        B if max_batch is None else max_batch, max_model_len, k, n_sink, n_window,
+        _ptr(out_block_scores), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), split_blocks, _stream_ptr(stream))
+    _check(st, "msa_indexer_score")
+
+
+def msa_indexer_merge(batch: int, k: int, out_ids, out_scores, workspace, *, stream=None) -> None:
+    st = load().msa_indexer_merge(batch, k, _ptr(out_ids), _ptr(out_scores), _ptr(workspace),
+                                  int(workspace.numel() * workspace.element_size()),
+                                  _stream_ptr(stream))
+    _check(st, "msa_indexer_merge")
+
+
+def msa_indexer_get_error(workspace, *, stream=None) -> int:
+    flags = ctypes.c_uint32(0)
+    st = load().msa_indexer_get_error(_ptr(workspace), _stream_ptr(stream), ctypes.byref(flags))
+    _check(st, "msa_indexer_get_error")
+    return int(flags.value)
+
+
+def new_workspace(max_batch: int, max_model_len: int, k: int, split_blocks: int = 0,
+                  device=None):
+    """A zero-filled uint8 CUDA tensor of msa_indexer_workspace_bytes() bytes."""
+    import torch
+    n = msa_indexer_workspace_bytes(max_batch, max_model_len, k, split_blocks)
+    if n == 0:
+        raise MsaError(MSA_ERR_UNSUPPORTED, "msa_indexer_workspace_bytes")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")

@@ -1,0 +1,842 @@
+// Decode-time MSA lightning indexer for GB300 (sm_103a): kernels and C ABI.
+//
+// Two kernels per decode step:
+//
+//  score_kernel  (persistent, one CTA per SM)
+//    a1  plan: page counts per request from the live seq_lens and their
+//        prefix sums; the batch's pages are cut into equal chunks, so a long
+//        request is spread over many CTAs and short ones share a CTA.
+//    a2  gather: a producer warp issues one 2-D TMA pair per 32 KiB page
+//        (page = block_table[b, j]) into a ring of shared-memory stages.
+//    a3  score: a consumer warp multiplies the resident 128x128 tile by the
+//        four query heads with mma.sync m16n8k16 (bf16 in, fp32 accumulate);
+//        the tile is read once for all four heads.
+//    a4  block max over the valid tokens (rows past seq_len are masked).
+//    a5  pin and pack into 64-bit keys (keys.cuh).
+//    a6  per-(chunk, request) top-kmax list per head in the workspace.
+//
+//  merge_kernel  (one CTA per (head, request))
+//    a7  exact top-k of that request's chunk lists, decoded to ids/scores.
+//
+// The exactness of the split is the context-parallel argument of vLLM
+// PR #57832 ("Solution"): a block in a head's global top-k is in the top-k of
+// its own shard, so keeping the full top-k per shard and merging is exact.
+// Splitting the KV axis across CTAs to shorten each CTA's serial chain is
+// TensorRT-LLM PR #17008 ("Changes": num_kv_splits); max is exact, so the
+// block scores do not depend on the split.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/msa_indexer.h"
+#include "keys.cuh"
+#include "layout.cuh"
+#include "ptx.cuh"
+
+namespace msa {
+
+// Pipeline shape.  Page number `it` (counted per CTA) is scored by consumer
+// warp it % kConsumerWarps in stage stage_of(it); every stage belongs to one
+// consumer warp, so each full/empty barrier has a single waiter that sees its
+// phases strictly in order (no warp can lap another warp's stage).
+constexpr int kConsumerWarps = 2;
+constexpr int kStagesPerConsumer = 3;
+constexpr int kStages = kConsumerWarps * kStagesPerConsumer;
+constexpr int kHeadsPerConsumer = kHeads / kConsumerWarps;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
+constexpr int kListBarrier = 1;  // named barrier id for the consumer warps
+
+__host__ __device__ constexpr int stage_of(uint32_t it)
+{
+    return static_cast<int>(it % kConsumerWarps) +
+           kConsumerWarps * static_cast<int>((it / kConsumerWarps) % kStagesPerConsumer);
+}
+
+// Use index of page `it` in its stage (its phase number on the barriers).
+__host__ __device__ constexpr uint32_t use_of(uint32_t it) { return it / kStages; }
+
+struct ScoreParams {
+    CUtensorMap tmap;  // pool viewed as [num_pages*128 rows][128 bf16]; 64x128 boxes, 128B swizzle
+    const uint16_t *q;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    float *out_block_scores;
+    uint8_t *ws;
+    int64_t bt_stride;
+    int64_t num_pages;
+    int batch;
+    int seq_limit;
+    int n_sink;
+    int n_window;
+    int split_blocks;
+    int slot_capacity;
+};
+
+struct SmemCtl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    int2 meta[kStages];  // (valid tokens, page ok)
+    int warp_sums[kConsumerWarps + 1];
+    volatile int abort_flag;
+};
+
+template <int KMAX>
+struct SmemLayout {
+    static constexpr size_t stages = 0;
+    static constexpr size_t ctl = stages + static_cast<size_t>(kStages) * kPageBytes;
+    static constexpr size_t lists = round_up(ctl + sizeof(SmemCtl), 16);
+    static constexpr size_t list_entries = 2 * kConsumerWarps * kHeads * KMAX;
+    static constexpr size_t prefix = lists + list_entries * sizeof(uint64_t);
+    static __host__ __device__ size_t bytes(int batch)
+    {
+        return 1024 /* alignment slack */ + prefix + sizeof(int32_t) * (batch + 1);
+    }
+};
+
+__device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+// The request that owns batch page p: the largest b with prefix[b] <= p.
+__device__ __forceinline__ int find_row(const int *prefix, int batch, int p)
+{
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= p)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int pages_of_request(const ScoreParams &p, int b)
+{
+    const int L = p.seq_lens[b];
+    if (L < 0 || L > p.seq_limit)
+        return 0;
+    return (L + kPage - 1) / kPage;
+}
+
+// a1: prefix[b] = pages of requests 0..b-1, computed by every CTA from the
+// live seq_lens (the grid itself never depends on them).
+__device__ void build_prefix(const ScoreParams &p, int *prefix, SmemCtl *ctl, WorkspaceHeader *hdr)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = p.batch;
+    const int per = (B + kThreads - 1) / kThreads;
+    const int r0 = min(B, tid * per), r1 = min(B, r0 + per);
+    int local = 0;
+    for (int b = r0; b < r1; ++b) {
+        const int L = p.seq_lens[b];
+        if ((L < 0 || L > p.seq_limit) && blockIdx.x == 0)
+            atomicOr(&hdr->fault, MSA_FAULT_SEQ_LEN);
+        local += pages_of_request(p, b);
+    }
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x += y;
+    }
+    if (lane == 31)
+        ctl->warp_sums[warp] = x;
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < warp; ++w)
+        before += ctl->warp_sums[w];
+    int run = before + x - local;
+    for (int b = r0; b < r1; ++b) {
+        prefix[b] = run;
+        run += pages_of_request(p, b);
+    }
+    if (tid == kThreads - 1)
+        prefix[B] = before + x;
+    __syncthreads();
+}
+
+// a3 + a4: the four heads' block scores of one resident page.  The page sits
+// in two 16 KiB halves (dims 0-63, 64-127), each 128 rows of 128 bytes with
+// the TMA 128-byte swizzle (16-byte chunk index XOR row % 8).  A = 16 tokens
+// x 16 dims via ldmatrix; B = q (16 dims x 8 columns: heads 0-3, 4-7 zero).
+// C row = token, column = head.  Returns m0/m1 = max over valid tokens of
+// heads 2t and 2t+1 (t = lane % 4), reduced over the warp.
+__device__ __forceinline__ void score_page(uint32_t stage, const uint32_t (&bq)[8][2], int valid,
+                                           uint32_t lane_off, const uint32_t (&xo)[4], int lane,
+                                           float &m0, float &m1)
+{
+    const float neg_inf = -__int_as_float(0x7f800000);
+    m0 = neg_inf;
+    m1 = neg_inf;
+#pragma unroll
+    for (int mt0 = 0; mt0 < 8; mt0 += 4) {
+        float acc[4][4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                acc[u][e] = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                uint32_t a[4];
+                ldsm_x4(a, stage + (ks >> 2) * kHalfPageBytes + (mt0 + u) * 16 * 128 + lane_off +
+                               xo[ks & 3]);
+                mma_bf16_16816(acc[u], a, bq[ks][0], bq[ks][1]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int row = (mt0 + u) * 16 + (lane >> 2);
+            const bool v0 = row < valid, v1 = row + 8 < valid;
+            m0 = fmaxf(m0, v0 ? acc[u][0] : neg_inf);
+            m1 = fmaxf(m1, v0 ? acc[u][1] : neg_inf);
+            m0 = fmaxf(m0, v1 ? acc[u][2] : neg_inf);
+            m1 = fmaxf(m1, v1 ? acc[u][3] : neg_inf);
+        }
+    }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    }
+}
+
+template <int KMAX>
+__device__ void run_consumer(const ScoreParams &p, uint8_t *smem, SmemCtl *ctl, const int *prefix,
+                             WorkspaceHeader *hdr, uint64_t *g_slots, int total, int split,
+                             int chunks)
+{
+    constexpr int NR = KMAX / 8;  // list registers per lane: 4 heads x KMAX / 32 lanes
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const float neg_inf = -__int_as_float(0x7f800000);
+    uint64_t *listbuf = reinterpret_cast<uint64_t *>(smem + SmemLayout<KMAX>::lists);
+
+    // ldmatrix lane geometry: matrix mi = lane / 8 (rows +8 for odd, dims +8
+    // for mi >= 2), row-in-matrix r = lane % 8.
+    const int mi = lane >> 3, rr = lane & 7;
+    const uint32_t lane_off = static_cast<uint32_t>(((mi & 1) * 8 + rr) * 128);
+    uint32_t xo[4];
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4)
+        xo[c4] = static_cast<uint32_t>((((c4 * 2 + (mi >> 1)) ^ rr) & 7) << 4);
+
+    const uint32_t stage0 = smem_addr(smem + SmemLayout<KMAX>::stages);
+    const int g = lane >> 2, t = lane & 3;
+    uint32_t bq[8][2];
+    int q_row = -1;
+    uint32_t it = 0;
+    int buf = 0;
+
+    for (int c = blockIdx.x; c < chunks; c += gridDim.x) {
+        const int p0 = c * split, p1 = min(total, p0 + split);
+        int pg = p0;
+        while (pg < p1) {
+            const int b = find_row(prefix, p.batch, pg);
+            const int row_first = prefix[b], row_end = prefix[b + 1];
+            const int nb = row_end - row_first;
+            const int seg_end = min(p1, row_end);
+            uint64_t lst[NR];
+#pragma unroll
+            for (int r = 0; r < NR; ++r)
+                lst[r] = 0;
+
+            const int skip = (w - static_cast<int>(it % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
+            for (int x = pg + skip; x < seg_end; x += kConsumerWarps) {
+                const uint32_t my = it + static_cast<uint32_t>(x - pg);
+                const int s = stage_of(my);
+                const uint32_t parity = use_of(my) & 1u;
+                const int j = x - row_first;
+
+                if (b != q_row) {  // issue the query loads before waiting on the page
+                    const uint32_t *qw = reinterpret_cast<const uint32_t *>(
+                        p.q + (static_cast<size_t>(b) * kHeads + (g & 3)) * kDim);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        bq[ks][0] = g < kHeads ? __ldg(qw + 8 * ks + t) : 0u;
+                        bq[ks][1] = g < kHeads ? __ldg(qw + 8 * ks + 4 + t) : 0u;
+                    }
+                    q_row = b;
+                }
+
+                bool ready = false;
+                if (!ctl->abort_flag) {
+                    ready = mbar_wait(smem_addr(&ctl->full[s]), parity);
+                    if (!ready) {
+                        atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
+                        ctl->abort_flag = 1;
+                    }
+                }
+                ready = __all_sync(0xffffffffu, ready);  // warp-uniform before any shuffle
+                const int2 meta = ctl->meta[s];
+                float sc[4] = {neg_inf, neg_inf, neg_inf, neg_inf};
+                const bool ok = ready && meta.y != 0;
+                if (ok) {
+                    float m0, m1;
+                    score_page(stage0 + s * kPageBytes, bq, meta.x, lane_off, xo, lane, m0, m1);
+                    sc[0] = __shfl_sync(0xffffffffu, m0, 0);
+                    sc[1] = __shfl_sync(0xffffffffu, m1, 0);
+                    sc[2] = __shfl_sync(0xffffffffu, m0, 1);
+                    sc[3] = __shfl_sync(0xffffffffu, m1, 1);
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(&ctl->empty[s]));
+
+                if (p.out_block_scores != nullptr && lane < kHeads) {
+                    float v = sc[0];
+                    v = lane == 1 ? sc[1] : v;
+                    v = lane == 2 ? sc[2] : v;
+                    v = lane == 3 ? sc[3] : v;
+                    p.out_block_scores[(static_cast<size_t>(b) * kHeads + lane) * p.bt_stride + j] = v;
+                }
+
+                const bool pinned = j < p.n_sink || j >= nb - p.n_window;
+                uint64_t key[4];
+#pragma unroll
+                for (int h = 0; h < kHeads; ++h)
+                    key[h] = ok ? pack_key(sc[h], j, pinned) : 0ull;
+                if constexpr (KMAX == 16) {
+                    lst[0] = insert_desc<16>(lst[0], lane < 16 ? key[0] : key[1], lane);
+                    lst[1] = insert_desc<16>(lst[1], lane < 16 ? key[2] : key[3], lane);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < kHeads; ++h)
+                        lst[h] = insert_desc<32>(lst[h], key[h], lane);
+                }
+            }
+            it += static_cast<uint32_t>(seg_end - pg);
+            pg = seg_end;
+
+            // a6: combine the consumer warps' lists of this (chunk, request);
+            // warp w merges heads 2w and 2w+1 and stores them in slot c + b.
+            uint64_t *lb = listbuf + static_cast<size_t>(buf) * kConsumerWarps * kHeads * KMAX;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const int head = r * (32 / KMAX) + lane / KMAX;
+                lb[(w * kHeads + head) * KMAX + lane % KMAX] = lst[r];
+            }
+            named_barrier_sync(kListBarrier, kConsumerThreads);
+            static_assert(kConsumerWarps == 2, "the list merge below combines two warps' lists");
+            const int slot = c + b;
+            if constexpr (KMAX == 16) {
+                // lanes 0-15: head 2w, lanes 16-31: head 2w+1; merge warp 0's and warp 1's list
+                const int h = kHeadsPerConsumer * w + (lane >> 4), r = lane & 15;
+                const uint64_t v = merge_top<16>(lb[(0 * kHeads + h) * KMAX + r],
+                                                 lb[(1 * kHeads + h) * KMAX + (15 - r)], lane);
+                if (slot < p.slot_capacity)
+                    g_slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + r] = v;
+            } else {
+#pragma unroll
+                for (int hh = 0; hh < kHeadsPerConsumer; ++hh) {
+                    const int h = kHeadsPerConsumer * w + hh;
+                    const uint64_t v = merge_top<32>(lb[(0 * kHeads + h) * KMAX + lane],
+                                                     lb[(1 * kHeads + h) * KMAX + (31 - lane)], lane);
+                    if (slot < p.slot_capacity)
+                        g_slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + lane] = v;
+                }
+            }
+            if (slot >= p.slot_capacity && lane == 0)
+                atomicOr(&hdr->fault, MSA_FAULT_SLOTS);
+            buf ^= 1;
+        }
+    }
+}
+
+template <int KMAX>
+__device__ void run_producer(const ScoreParams &p, uint8_t *smem, SmemCtl *ctl, const int *prefix,
+                             WorkspaceHeader *hdr, int total, int split, int chunks)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t stage0 = smem_addr(smem + SmemLayout<KMAX>::stages);
+    uint32_t it = 0;
+
+    for (int c = blockIdx.x; c < chunks; c += gridDim.x) {
+        const int p0 = c * split, p1 = min(total, p0 + split);
+        // lane-parallel lookup of 32 pages, one batch ahead of the issue loop
+        auto lookup = [&](int pb, int &page, int &valid, int &ok) {
+            const int pg = pb + lane;
+            page = 0;
+            valid = 0;
+            ok = 0;
+            if (pg < p1) {
+                const int b = find_row(prefix, p.batch, pg);
+                const int j = pg - prefix[b];
+                page = p.block_table[static_cast<int64_t>(b) * p.bt_stride + j];
+                valid = min(kPage, p.seq_lens[b] - j * kPage);
+                ok = (page >= 0 && page < p.num_pages) ? 1 : 0;
+                if (!ok)
+                    atomicOr(&hdr->fault, MSA_FAULT_PAGE_ID);
+            }
+        };
+        int n_page, n_valid, n_ok;
+        lookup(p0, n_page, n_valid, n_ok);
+        for (int pb = p0; pb < p1; pb += 32) {
+            const int c_page = n_page, c_valid = n_valid, c_ok = n_ok;
+            if (pb + 32 < p1)
+                lookup(pb + 32, n_page, n_valid, n_ok);
+            const int n = min(32, p1 - pb);
+            for (int i = 0; i < n; ++i, ++it) {
+                const int page = __shfl_sync(0xffffffffu, c_page, i);
+                const int valid = __shfl_sync(0xffffffffu, c_valid, i);
+                const int ok = __shfl_sync(0xffffffffu, c_ok, i);
+                if (lane == 0) {
+                    const int s = stage_of(it);
+                    const uint32_t full = smem_addr(&ctl->full[s]);
+                    if (it >= kStages && !ctl->abort_flag) {
+                        if (!mbar_wait(smem_addr(&ctl->empty[s]), (use_of(it) - 1) & 1u)) {
+                            atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
+                            ctl->abort_flag = 1;
+                        }
+                    }
+                    const bool issue = ok && !ctl->abort_flag;
+                    ctl->meta[s] = make_int2(valid, issue ? 1 : 0);
+                    if (issue) {
+                        const uint32_t dst = stage0 + s * kPageBytes;
+                        mbar_arrive_expect_tx(full, kPageBytes);
+                        tma_load_2d(dst, &p.tmap, 0, page * kPage, full);
+                        tma_load_2d(dst + kHalfPageBytes, &p.tmap, 64, page * kPage, full);
+                    } else {
+                        mbar_arrive(full);
+                    }
+                }
+                __syncwarp();
+            }
+        }
+    }
+    // Drain: no copy may still be landing in shared memory when the CTA exits.
+    if (lane == 0) {
+        const uint32_t n = it < kStages ? it : kStages;
+        for (uint32_t i = 0; i < n; ++i) {
+            const uint32_t q = it - 1 - i;
+            if (!mbar_wait(smem_addr(&ctl->full[stage_of(q)]), use_of(q) & 1u))
+                atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
+        }
+    }
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ ScoreParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + SmemLayout<KMAX>::ctl);
+    int *prefix = reinterpret_cast<int *>(smem + SmemLayout<KMAX>::prefix);
+    WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(p.ws);
+    uint64_t *g_slots = reinterpret_cast<uint64_t *>(p.ws + slots_offset(p.batch));
+    const int warp = threadIdx.x >> 5;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_addr(&ctl->full[s]), 1);
+            mbar_init(smem_addr(&ctl->empty[s]), 1);
+        }
+        ctl->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kProducerWarp && (threadIdx.x & 31) == 0)
+        prefetch_tensormap(&p.tmap);
+
+    build_prefix(p, prefix, ctl, hdr);  // ends with __syncthreads
+
+    const int total = prefix[p.batch];
+    const int split = p.split_blocks > 0 ? p.split_blocks : max(1, ceil_div_i(total, gridDim.x));
+    const int chunks = total > 0 ? ceil_div_i(total, split) : 0;
+
+    if (blockIdx.x == 0) {
+        int *g_prefix = reinterpret_cast<int *>(p.ws + prefix_offset());
+        for (int b = threadIdx.x; b <= p.batch; b += kThreads)
+            g_prefix[b] = prefix[b];
+        if (threadIdx.x == 0) {
+            hdr->split = split;
+            hdr->total = total;
+            hdr->chunks = chunks;
+            hdr->batch = p.batch;
+            hdr->kmax = KMAX;
+        }
+    }
+
+    if (warp == kProducerWarp)
+        run_producer<KMAX>(p, smem, ctl, prefix, hdr, total, split, chunks);
+    else
+        run_consumer<KMAX>(p, smem, ctl, prefix, hdr, g_slots, total, split, chunks);
+}
+
+// a7: one CTA per (head, request).  Groups of KMAX lanes each fold a share of
+// the request's chunk lists into a running top-KMAX, then a tree in shared
+// memory merges the groups.
+template <int KMAX>
+__global__ void __launch_bounds__(128) merge_kernel(const uint8_t *ws, int batch, int k,
+                                                    int slot_capacity, int32_t *out_ids,
+                                                    float *out_scores)
+{
+    constexpr int kGroups = 128 / KMAX;
+    __shared__ uint64_t part[128];
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int lane = threadIdx.x & 31, grp = threadIdx.x / KMAX, rank = threadIdx.x % KMAX;
+    const WorkspaceHeader *hdr = reinterpret_cast<const WorkspaceHeader *>(ws);
+    const int *prefix = reinterpret_cast<const int *>(ws + prefix_offset());
+    const uint64_t *slots = reinterpret_cast<const uint64_t *>(ws + slots_offset(batch));
+
+    const int split = hdr->split;
+    const int p0 = prefix[b], p1 = prefix[b + 1];
+    int c_first = 0, n_lists = 0;
+    if (p1 > p0 && split > 0) {
+        c_first = p0 / split;
+        n_lists = min((p1 - 1) / split - c_first + 1, slot_capacity);
+    }
+
+    uint64_t run = 0;
+    for (int base = 0; base < n_lists; base += kGroups) {
+        const int i = base + grp;
+        const int slot = c_first + i + b;
+        uint64_t other = 0;
+        if (i < n_lists && slot < slot_capacity)
+            other = slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + (KMAX - 1 - rank)];
+        run = merge_top<KMAX>(run, other, lane);
+    }
+    part[threadIdx.x] = run;
+    __syncthreads();
+#pragma unroll
+    for (int step = 1; step < kGroups; step <<= 1) {
+        const bool active = (grp % (2 * step)) == 0 && grp + step < kGroups;
+        const uint64_t other = active ? part[(grp + step) * KMAX + (KMAX - 1 - rank)] : 0ull;
+        run = merge_top<KMAX>(run, other, lane);
+        __syncthreads();
+        part[threadIdx.x] = run;
+        __syncthreads();
+    }
+    if (grp == 0 && rank < k) {
+        int id;
+        float score;
+        unpack_key(run, id, score);
+        const size_t o = (static_cast<size_t>(b) * kHeads + h) * k + rank;
+        out_ids[o] = id;
+        out_scores[o] = score;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+constexpr int kMaxDevices = 64;
+
+static int device_sms(int dev)
+{
+    static std::atomic<int> cache[kMaxDevices];
+    int v = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (v > 0)
+        return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+        return 0;
+    if (dev >= 0 && dev < kMaxDevices)
+        cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+template <int KMAX>
+static bool ensure_smem_attr(int dev)
+{
+    static std::atomic<bool> done[kMaxDevices];
+    if (dev >= 0 && dev < kMaxDevices && done[dev].load(std::memory_order_acquire))
+        return true;
+    const size_t bytes = SmemLayout<KMAX>::bytes(MSA_MAX_BATCH);
+    if (cudaFuncSetAttribute(score_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(bytes)) != cudaSuccess)
+        return false;
+    if (dev >= 0 && dev < kMaxDevices)
+        done[dev].store(true, std::memory_order_release);
+    return true;
+}
+
+struct Geometry {
+    int grid;
+    int64_t chunks_bound;
+    int64_t max_blocks;
+};
+
+static int64_t blocks_for(int max_model_len) { return (static_cast<int64_t>(max_model_len) + kPage - 1) / kPage; }
+
+static bool bounds_ok(int max_batch, int max_model_len, int k, int split_blocks)
+{
+    if (max_batch < 1 || max_batch > MSA_MAX_BATCH || max_model_len < 1)
+        return false;
+    if (k < 1 || k > MSA_MAX_TOPK || split_blocks < 0)
+        return false;
+    return static_cast<int64_t>(max_batch) * blocks_for(max_model_len) < (int64_t{1} << 30);
+}
+
+static int64_t chunk_bound(int batch, int64_t max_blocks, int split_blocks, int grid)
+{
+    if (split_blocks == 0)
+        return grid;
+    return (static_cast<int64_t>(batch) * max_blocks + split_blocks - 1) / split_blocks;
+}
+
+static msa_status validate(const void *q, const void *kcache_pool, int64_t num_pages,
+                           const int32_t *block_table, int64_t bt_stride, const int32_t *seq_lens,
+                           int batch, int max_batch, int max_model_len, int k, int n_sink,
+                           int n_window, const void *workspace, int split_blocks)
+{
+    if (!q || !kcache_pool || !block_table || !seq_lens || !workspace)
+        return MSA_ERR_INVALID_ARG;
+    if (batch < 0 || batch > max_batch || max_batch < 1 || max_model_len < 1)
+        return MSA_ERR_INVALID_ARG;
+    if (max_batch > MSA_MAX_BATCH)
+        return MSA_ERR_UNSUPPORTED;
+    if (k < 1 || n_sink < 0 || n_window < 0 || split_blocks < 0)
+        return MSA_ERR_INVALID_ARG;
+    if (k > MSA_MAX_TOPK)
+        return MSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(n_sink) + n_window > k)
+        return MSA_ERR_INVALID_ARG;
+    if (num_pages < 1 || bt_stride < 1)
+        return MSA_ERR_INVALID_ARG;
+    if (num_pages > (int64_t{1} << 24))  // TMA row coordinate page*128 must fit in int32
+        return MSA_ERR_UNSUPPORTED;
+    if (!bounds_ok(max_batch, max_model_len, k, split_blocks))
+        return MSA_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(kcache_pool) & 15) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255) ||
+        (reinterpret_cast<uintptr_t>(block_table) & 3) || (reinterpret_cast<uintptr_t>(seq_lens) & 3))
+        return MSA_ERR_INVALID_ARG;
+    return MSA_OK;
+}
+
+static int score_grid(int sms, int batch, int64_t max_blocks, int split_blocks)
+{
+    const int64_t work = static_cast<int64_t>(batch) * max_blocks;
+    int64_t units = split_blocks > 0 ? (work + split_blocks - 1) / split_blocks : work;
+    int64_t g = sms;
+    if (g > MSA_MAX_GRID)
+        g = MSA_MAX_GRID;
+    if (units < g)
+        g = units;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
+template <int KMAX>
+static msa_status launch_score(const void *q, const void *kcache_pool, int64_t num_pages,
+                               const int32_t *block_table, int64_t bt_stride,
+                               const int32_t *seq_lens, int batch, int max_model_len, int n_sink,
+                               int n_window, float *out_block_scores, void *workspace,
+                               int slot_capacity, int grid, int split_blocks, cudaStream_t st,
+                               int dev)
+{
+    ScoreParams p;
+    std::memset(&p, 0, sizeof p);
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc)
+        return MSA_ERR_CUDA;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim),
+                                static_cast<cuuint64_t>(num_pages) * kPage};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kPage)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&p.tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(kcache_pool), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return MSA_ERR_CUDA;
+    p.q = static_cast<const uint16_t *>(q);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out_block_scores = out_block_scores;
+    p.ws = static_cast<uint8_t *>(workspace);
+    p.bt_stride = bt_stride;
+    p.num_pages = num_pages;
+    p.batch = batch;
+    const int64_t lim = bt_stride * kPage < max_model_len ? bt_stride * kPage : max_model_len;
+    p.seq_limit = static_cast<int>(lim);
+    p.n_sink = n_sink;
+    p.n_window = n_window;
+    p.split_blocks = split_blocks;
+    p.slot_capacity = slot_capacity;
+    if (!ensure_smem_attr<KMAX>(dev))
+        return MSA_ERR_CUDA;
+    const size_t smem = SmemLayout<KMAX>::bytes(batch);
+    score_kernel<KMAX><<<grid, kThreads, smem, st>>>(p);
+    return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+struct Plan {
+    int grid;
+    int slot_capacity;
+    int dev;
+};
+
+static msa_status plan(int batch, int max_batch, int max_model_len, int k, int split_blocks,
+                       size_t workspace_bytes, Plan &out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return MSA_ERR_CUDA;
+    const int sms = device_sms(dev);
+    if (sms <= 0)
+        return MSA_ERR_CUDA;
+    const int64_t max_blocks = blocks_for(max_model_len);
+    const int grid = score_grid(sms, batch, max_blocks, split_blocks);
+    const int kmax = kmax_for(k);
+    const size_t off = slots_offset(batch);
+    const int64_t need_slots = chunk_bound(batch, max_blocks, split_blocks, grid) + batch;
+    if (workspace_bytes < off)
+        return MSA_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t cap = static_cast<int64_t>((workspace_bytes - off) / slot_bytes(kmax));
+    if (cap < need_slots)
+        return MSA_ERR_WORKSPACE_TOO_SMALL;
+    out.grid = grid;
+    out.slot_capacity = static_cast<int>(cap > (int64_t{1} << 30) ? (int64_t{1} << 30) : cap);
+    out.dev = dev;
+    (void)max_batch;
+    return MSA_OK;
+}
+
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" size_t msa_indexer_workspace_bytes(int max_batch, int max_model_len, int k,
+                                              int split_blocks)
+{
+    if (!bounds_ok(max_batch, max_model_len, k, split_blocks))
+        return 0;
+    const int64_t chunks = chunk_bound(max_batch, blocks_for(max_model_len), split_blocks, MSA_MAX_GRID);
+    return slots_offset(max_batch) +
+           static_cast<size_t>(chunks + max_batch) * slot_bytes(kmax_for(k));
+}
+
+extern "C" msa_status msa_indexer_score(const void *q, const void *kcache_pool, int64_t num_pages,
+                                        const int32_t *block_table, int64_t bt_stride,
+                                        const int32_t *seq_lens, int batch, int max_batch,
+                                        int max_model_len, int k, int n_sink, int n_window,
+                                        float *out_block_scores, void *workspace,
+                                        size_t workspace_bytes, int split_blocks, void *stream)
+{
+    msa_status st = validate(q, kcache_pool, num_pages, block_table, bt_stride, seq_lens, batch,
+                             max_batch, max_model_len, k, n_sink, n_window, workspace, split_blocks);
+    if (st != MSA_OK || batch == 0)
+        return st;
+    Plan pl;
+    st = plan(batch, max_batch, max_model_len, k, split_blocks, workspace_bytes, pl);
+    if (st != MSA_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (kmax_for(k) == 16)
+        return launch_score<16>(q, kcache_pool, num_pages, block_table, bt_stride, seq_lens, batch,
+                                max_model_len, n_sink, n_window, out_block_scores, workspace,
+                                pl.slot_capacity, pl.grid, split_blocks, s, pl.dev);
+    return launch_score<32>(q, kcache_pool, num_pages, block_table, bt_stride, seq_lens, batch,
+                            max_model_len, n_sink, n_window, out_block_scores, workspace,
+                            pl.slot_capacity, pl.grid, split_blocks, s, pl.dev);
+}
+
+extern "C" msa_status msa_indexer_merge(int batch, int k, int32_t *out_ids, float *out_scores,
+                                        const void *workspace, size_t workspace_bytes,
+                                        void *stream)
+{
+    if (!out_ids || !out_scores || !workspace || batch < 0 || batch > MSA_MAX_BATCH)
+        return MSA_ERR_INVALID_ARG;
+    if (k < 1)
+        return MSA_ERR_INVALID_ARG;
+    if (k > MSA_MAX_TOPK)
+        return MSA_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255)
+        return MSA_ERR_INVALID_ARG;
+    if (batch == 0)
+        return MSA_OK;
+    const int kmax = kmax_for(k);
+    const size_t off = slots_offset(batch);
+    if (workspace_bytes < off + slot_bytes(kmax))
+        return MSA_ERR_WORKSPACE_TOO_SMALL;
+    const int64_t cap = static_cast<int64_t>((workspace_bytes - off) / slot_bytes(kmax));
+    const int capacity = static_cast<int>(cap > (int64_t{1} << 30) ? (int64_t{1} << 30) : cap);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const dim3 grid(kHeads, static_cast<unsigned>(batch));
+    const uint8_t *ws = static_cast<const uint8_t *>(workspace);
+    if (kmax == 16)
+        merge_kernel<16><<<grid, 128, 0, s>>>(ws, batch, k, capacity, out_ids, out_scores);
+    else
+        merge_kernel<32><<<grid, 128, 0, s>>>(ws, batch, k, capacity, out_ids, out_scores);
+    return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+extern "C" msa_status msa_indexer_decode(const void *q, const void *kcache_pool, int64_t num_pages,
+                                         const int32_t *block_table, int64_t bt_stride,
+                                         const int32_t *seq_lens, int batch, int max_batch,
+                                         int max_model_len, int k, int n_sink, int n_window,
+                                         int32_t *out_ids, float *out_scores,
+                                         float *out_block_scores, void *workspace,
+                                         size_t workspace_bytes, int split_blocks, void *stream)
+{
+    if (!out_ids || !out_scores)
+        return MSA_ERR_INVALID_ARG;
+    msa_status st = msa_indexer_score(q, kcache_pool, num_pages, block_table, bt_stride, seq_lens,
+                                      batch, max_batch, max_model_len, k, n_sink, n_window,
+                                      out_block_scores, workspace, workspace_bytes, split_blocks,
+                                      stream);
+    if (st != MSA_OK || batch == 0)
+        return st;
+    return msa_indexer_merge(batch, k, out_ids, out_scores, workspace, workspace_bytes, stream);
+}
+
+extern "C" msa_status msa_indexer_get_error(void *workspace, void *stream, uint32_t *flags)
+{
+    if (!workspace || !flags)
+        return MSA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t *word = &static_cast<WorkspaceHeader *>(workspace)->fault;
+    uint32_t host = 0;
+    if (cudaMemcpyAsync(&host, word, sizeof host, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MSA_ERR_CUDA;
+    if (cudaMemsetAsync(word, 0, sizeof host, s) != cudaSuccess)
+        return MSA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return MSA_ERR_CUDA;
+    *flags = host;
+    return MSA_OK;
+}
+
+extern "C" const char *msa_status_string(int status)
+{
+    switch (status) {
+    case MSA_OK:
+        return "ok";
+    case MSA_ERR_INVALID_ARG:
+        return "invalid argument";
+    case MSA_ERR_UNSUPPORTED:
+        return "unsupported size";
+    case MSA_ERR_WORKSPACE_TOO_SMALL:
+        return "workspace too small";
+    case MSA_ERR_CUDA:
+        return "CUDA error";
+    default:
+        return "unknown status";
+    }
+}

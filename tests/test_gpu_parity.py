@@ -1,0 +1,128 @@
+"""CUDA path vs the CPU oracle on identical seeded inputs (through the C ABI)."""
+
+import numpy as np
+import pytest
+
+import parity
+import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import sparse_attention_decode_gb300 as msa
+    msa.load()
+    return msa
+
+
+def _compare(orc, w, **kw):
+    o_scores, o_ids, _ = orc.run(w, k=kw.get("k"), n_sink=kw.get("n_sink"), n_window=kw.get("n_window"))
+    g_ids, g_sc, g_blk, fault = parity.run_gpu(w, **kw)
+    assert fault == 0, f"fault word {fault:#x}"
+    return parity.check(w, o_scores, o_ids, g_ids, g_sc, g_blk, k=kw.get("k"),
+                        n_sink=kw.get("n_sink"), n_window=kw.get("n_window"))
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_point", "ragged"])
+def test_config_parity(lib, orc, name):
+    _compare(orc, wl.make(name))
+
+
+def test_ragged_permuted_rows(lib, orc):
+    _compare(orc, wl.ragged(permute_rows=True))
+
+
+@pytest.mark.parametrize("split", [64, 0])
+def test_adversarial_exact(lib, orc, split):
+    """Integer scores: ids, order and scores bit-exact; all winners in one split at W=64."""
+    w = wl.adversarial()
+    _compare(orc, w, split_blocks=split)
+
+
+@pytest.mark.slow
+def test_long_context_full(lib, orc):
+    """B=32 x 128K: the launch configuration the benchmark times (automatic split)."""
+    w = wl.long_context()
+    _compare(orc, w)
+
+
+@pytest.mark.parametrize("k,n_sink,n_window", [(1, 0, 0), (1, 1, 0), (2, 0, 1), (3, 1, 1),
+                                               (16, 0, 0), (16, 16, 0), (16, 0, 16), (17, 1, 2),
+                                               (32, 1, 2), (32, 4, 8)])
+def test_k_and_pins(lib, orc, k, n_sink, n_window):
+    w = wl.random_workload([1, 127, 128, 129, 2000, 5000, 8700, 0], num_pages=200, seed=31,
+                           q_scale=1 / np.sqrt(128), max_model_len=8704)
+    _compare(orc, w, k=k, n_sink=n_sink, n_window=n_window)
+
+
+def _grid_lengths():
+    return [1, 127, 128, 129, 256, 1000, 4096, 8699, 8700, 8701, 16384]
+
+
+@pytest.mark.parametrize("B", [1, 2, 4, 8, 15, 16, 32])
+def test_batch_by_length_grid(lib, orc, B):
+    """Batch {1..32} x kv_len {1..16384} incl. consecutive decode lengths."""
+    lens = _grid_lengths()
+    for i, L in enumerate(lens):
+        seq = [L] * B if i % 2 == 0 else [lens[(i + r) % len(lens)] for r in range(B)]
+        w = wl.random_workload(seq, seed=100 + B * 31 + i, q_scale=1 / np.sqrt(128),
+                               max_model_len=16384)
+        _compare(orc, w)
+
+
+def test_split_width_is_bitwise_invariant(lib):
+    """Block scores and ids do not depend on how the pages are split over CTAs."""
+    for w in (wl.decode_point(), wl.ragged()):
+        ref_ids, ref_sc, ref_blk, f0 = parity.run_gpu(w, split_blocks=0)
+        assert f0 == 0
+        for W in (1, 2, 3, 8, 64, 1024):
+            ids, sc, blk, f = parity.run_gpu(w, split_blocks=W)
+            assert f == 0
+            np.testing.assert_array_equal(blk, ref_blk, err_msg=f"{w.name} W={W}")
+            np.testing.assert_array_equal(ids, ref_ids, err_msg=f"{w.name} W={W}")
+            np.testing.assert_array_equal(sc, ref_sc, err_msg=f"{w.name} W={W}")
+
+
+def test_shape_bound_is_bitwise_invariant(lib):
+    """Sizing for an 8x larger batch and context bound changes nothing."""
+    w = wl.decode_point()
+    a = parity.run_gpu(w)
+    b = parity.run_gpu(w, max_batch=8 * w.batch, max_model_len=8 * w.max_model_len)
+    for x, y in zip(a[:3], b[:3]):
+        np.testing.assert_array_equal(x, y)
+    assert a[3] == 0 and b[3] == 0
+
+
+def test_graph_replay_with_changed_lengths(lib, orc):
+    """Capture once at one set of lengths; replay after changing lengths and tables."""
+    import torch
+    import sparse_attention_decode_gb300 as msa
+    max_len, B, k = 16384, 8, 16
+    first = wl.random_workload([4096] * B, num_pages=1024, seed=41, q_scale=1 / np.sqrt(128),
+                               max_model_len=max_len)
+    q, pool, bt, seq = parity.to_device(first)
+    ids = torch.empty((B, 4, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((B, 4, k), dtype=torch.float32, device="cuda")
+    ws = msa.new_workspace(B, max_len, k)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        msa.msa_indexer_decode(q, pool, bt, seq, k, 1, 2, ids, sc, ws, max_model_len=max_len)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        msa.msa_indexer_decode(q, pool, bt, seq, k, 1, 2, ids, sc, ws, max_model_len=max_len)
+    for seed, lens in ((42, [1, 0, 129, 16384, 700, 8700, 128, 3000]), (43, [16000] * 8)):
+        w = wl.random_workload(lens, num_pages=1024, seed=seed, q_scale=1 / np.sqrt(128),
+                               max_model_len=max_len)
+        q2, pool2, bt2, seq2 = parity.to_device(w)
+        q.copy_(q2)
+        pool.copy_(pool2)
+        bt.copy_(bt2)
+        seq.copy_(seq2)
+        g.replay()
+        torch.cuda.synchronize()
+        o_scores, o_ids, _ = orc.run(w)
+        parity.check(w, o_scores, o_ids, ids.cpu().numpy(), sc.cpu().numpy())
+    assert msa.msa_indexer_get_error(ws) == 0
