@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     MSA_HEAD_DIM,
     MSA_MAX_BATCH,
     MSA_MAX_TOPK,
+    MSA_NOALLOC_WORKSPACE_BYTES,
     MSA_NUM_HEADS,
     MSA_OK,
     MSA_PAGE_TOKENS,
@@ -25,6 +26,7 @@ from ._binding import (  # noqa: F401
     library_path,
     load,
     msa_indexer_decode,
+    msa_indexer_decode_noalloc,
     msa_indexer_get_error,
     msa_indexer_merge,
     msa_indexer_score,

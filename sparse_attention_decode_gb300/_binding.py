@@ -30,6 +30,7 @@ MSA_HEAD_DIM = 128
 MSA_PAGE_TOKENS = 128
 MSA_MAX_TOPK = 32
 MSA_MAX_BATCH = 4096
+MSA_NOALLOC_WORKSPACE_BYTES = 2 * 1024 * 1024
 
 EXPORTED = (
     "msa_indexer_workspace_bytes",
@@ -38,6 +39,7 @@ EXPORTED = (
     "msa_indexer_merge",
     "msa_indexer_get_error",
     "msa_status_string",
+    "msa_indexer_decode_noalloc",
 )
 
 _lib = None
@@ -76,6 +78,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.msa_indexer_merge.restype = c_int
     lib.msa_indexer_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
     lib.msa_indexer_get_error.restype = c_int
+    lib.msa_indexer_decode_noalloc.argtypes = common[:7] + common[8:] + [P, P, P, P]
+    lib.msa_indexer_decode_noalloc.restype = c_int
     lib.msa_status_string.argtypes = [c_int]
     lib.msa_status_string.restype = ctypes.c_char_p
     if path is None:
@@ -156,6 +160,23 @@ def msa_indexer_merge(batch: int, k: int, out_ids, out_scores, workspace, *, str
                                   int(workspace.numel() * workspace.element_size()),
                                   _stream_ptr(stream))
     _check(st, "msa_indexer_merge")
+
+
+def msa_indexer_decode_noalloc(q, kcache_pool, block_table, seq_lens, k: int, n_sink: int,
+                               n_window: int, out_ids, out_scores, *, max_model_len: int,
+                               out_block_scores=None, stream=None) -> None:
+    """msa_indexer_decode_noalloc(): the decode step for callers that cannot allocate.
+
+    No workspace argument: the library uses a fixed scratch array of its own
+    (see the C header).  Calls that overlap on the GPU share that array and
+    race, so serialise them.
+    """
+    B, num_pages, bt_stride = _shape_args(q, kcache_pool, block_table, seq_lens)
+    st = load().msa_indexer_decode_noalloc(
+        _ptr(q), _ptr(kcache_pool), num_pages, _ptr(block_table), bt_stride, _ptr(seq_lens), B,
+        max_model_len, k, n_sink, n_window, _ptr(out_ids), _ptr(out_scores),
+        _ptr(out_block_scores), _stream_ptr(stream))
+    _check(st, "msa_indexer_decode_noalloc")
 
 
 def msa_indexer_get_error(workspace, *, stream=None) -> int:

@@ -806,6 +806,69 @@ extern "C" msa_status msa_indexer_decode(const void *q, const void *kcache_pool,
     return msa_indexer_merge(batch, k, out_ids, out_scores, workspace, workspace_bytes, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the scratch of msa_indexer_decode in a fixed
+// device array of this library, for callers that cannot allocate.
+// ---------------------------------------------------------------------------
+
+namespace msa {
+
+static __device__ __align__(256) uint8_t g_noalloc_workspace[MSA_NOALLOC_WORKSPACE_BYTES];
+
+// Device address of g_noalloc_workspace on device `dev` (the current device),
+// looked up once per device.  In host code the array's name only stands in
+// for it; the kernels must be given this address.
+static void *noalloc_workspace(int dev)
+{
+    static std::atomic<void *> addr[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    void *p = addr[dev].load(std::memory_order_acquire);
+    if (p != nullptr)
+        return p;
+    if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || p == nullptr)
+        return nullptr;
+    addr[dev].store(p, std::memory_order_release);
+    return p;
+}
+
+}  // namespace msa
+
+extern "C" msa_status msa_indexer_decode_noalloc(const void *q, const void *kcache_pool,
+                                                 int64_t num_pages, const int32_t *block_table,
+                                                 int64_t bt_stride, const int32_t *seq_lens,
+                                                 int batch, int max_model_len, int k, int n_sink,
+                                                 int n_window, int32_t *out_ids, float *out_scores,
+                                                 float *out_block_scores, void *stream)
+{
+    if (!out_ids || !out_scores)
+        return MSA_ERR_INVALID_ARG;
+    const int max_batch = batch > 0 ? batch : 1;
+    // argument checks that need no device (a placeholder stands in for the scratch)
+    msa_status st = validate(q, kcache_pool, num_pages, block_table, bt_stride, seq_lens, batch,
+                             max_batch, max_model_len, k, n_sink, n_window,
+                             reinterpret_cast<const void *>(uintptr_t{256}), 0);
+    if (st != MSA_OK || batch == 0)
+        return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return MSA_ERR_CUDA;
+    const int sms = device_sms(dev);
+    if (sms <= 0)
+        return MSA_ERR_CUDA;
+    const int grid = score_grid(sms, batch, blocks_for(max_model_len), 0);
+    const size_t need = slots_offset(batch) +
+                        static_cast<size_t>(grid + batch) * slot_bytes(kmax_for(k));
+    if (need > MSA_NOALLOC_WORKSPACE_BYTES)
+        return MSA_ERR_UNSUPPORTED;
+    void *ws = noalloc_workspace(dev);
+    if (ws == nullptr)
+        return MSA_ERR_CUDA;
+    return msa_indexer_decode(q, kcache_pool, num_pages, block_table, bt_stride, seq_lens, batch,
+                              max_batch, max_model_len, k, n_sink, n_window, out_ids, out_scores,
+                              out_block_scores, ws, MSA_NOALLOC_WORKSPACE_BYTES, 0, stream);
+}
+
 extern "C" msa_status msa_indexer_get_error(void *workspace, void *stream, uint32_t *flags)
 {
     if (!workspace || !flags)
