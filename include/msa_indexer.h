@@ -183,21 +183,24 @@ msa_status msa_indexer_get_error(void *workspace, void *stream, uint32_t *flags)
  * The scratch lives in one fixed array of MSA_NOALLOC_WORKSPACE_BYTES in the
  * library's device memory (every GPU that loads the library keeps it until
  * the process exits).  The call allocates and frees nothing.  Its first call
- * on a device looks up that array's device address (once per device, with
- * that device current); make that first call before any stream capture.
+ * on a device does a one-time set-up with that device current: it looks up
+ * the array's device address and zero-fills the array's 256-byte header
+ * (a blocking cudaMemset); make that first call before any stream capture.
  *
  * Arguments are those of msa_indexer_decode with max_batch = batch and the
  * automatic split.  A batch whose scratch would not fit
- * (256 + round_up(4*(batch+1), 256) + (CTAs + batch) * 4 * kmax * 8 bytes,
+ * (256 + round_up(4*(batch+1), 256) + (7*CTAs + batch) * 4 * kmax * 8 bytes,
  * CTAs <= the SM count, kmax = 16 for k <= 16 else 32) returns
  * MSA_ERR_UNSUPPORTED before anything is enqueued; on GB300 (152 SMs) every
- * batch up to 1024 fits for any k.  Every call uses the same array and leaves its contents
- * behind; nothing in it needs clearing, because a call reads only what it
- * wrote earlier on the GPU.  Calls that can overlap on the GPU (different
- * streams, different threads) race on the array: serialise them.  Data
- * faults are handled as in msa_indexer_decode but are not reported.
+ * batch up to 1024 fits for any k.  Every call uses the same array and leaves
+ * its contents behind; the only words that must start at zero (two ticket
+ * counters in the header) are zeroed at set-up and returned to zero by every
+ * call, and everything else a call reads it wrote earlier on the GPU.  Calls
+ * that can overlap on the GPU (different streams, different threads) race on
+ * the array: serialise them.  Data faults are handled as in
+ * msa_indexer_decode but are not reported.
  */
-#define MSA_NOALLOC_WORKSPACE_BYTES (2u * 1024u * 1024u)
+#define MSA_NOALLOC_WORKSPACE_BYTES (4u * 1024u * 1024u)
 msa_status msa_indexer_decode_noalloc(const void *q, const void *kcache_pool, int64_t num_pages,
                                       const int32_t *block_table, int64_t bt_stride,
                                       const int32_t *seq_lens, int batch, int max_model_len, int k,

@@ -30,7 +30,7 @@ MSA_HEAD_DIM = 128
 MSA_PAGE_TOKENS = 128
 MSA_MAX_TOPK = 32
 MSA_MAX_BATCH = 4096
-MSA_NOALLOC_WORKSPACE_BYTES = 2 * 1024 * 1024
+MSA_NOALLOC_WORKSPACE_BYTES = 4 * 1024 * 1024
 
 EXPORTED = (
     "msa_indexer_workspace_bytes",

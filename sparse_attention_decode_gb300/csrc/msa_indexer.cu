@@ -31,6 +31,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/msa_indexer.h"
 #include "keys.cuh"
@@ -50,7 +51,6 @@ constexpr int kHeadsPerConsumer = kHeads / kConsumerWarps;
 constexpr int kProducerWarp = kConsumerWarps;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
-constexpr int kListBarrier = 1;  // named barrier id for the consumer warps
 
 __host__ __device__ constexpr int stage_of(uint32_t it)
 {
@@ -78,12 +78,19 @@ struct ScoreParams {
     int slot_capacity;
 };
 
+constexpr int kChunkQueue = 8;  // chunk ids the producer may post ahead of the consumers
+
 struct SmemCtl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    int2 meta[kStages];  // (valid tokens, page ok)
+    uint64_t full[kStages];          // page landed (1 producer arrival + TMA bytes)
+    uint64_t empty[kStages];         // page consumed (its owner warp)
+    uint64_t cq_full[kChunkQueue];   // chunk id posted (producer)
+    uint64_t cq_empty[kChunkQueue];  // chunk id read (every consumer warp)
+    uint64_t list_bar[2];            // lists of a segment written (every consumer thread)
+    int2 meta[kStages];              // (valid tokens, page ok)
+    int chunk_q[kChunkQueue];
     int warp_sums[kConsumerWarps + 1];
     volatile int abort_flag;
+    Partition part;  // this pass's chunking, the same in every CTA
 };
 
 template <int KMAX>
@@ -209,10 +216,26 @@ __device__ __forceinline__ void score_page(uint32_t stage, const uint32_t (&bq)[
     }
 }
 
+// Bounded wait for the whole warp; false (and the CTA's abort flag set) when
+// the wait ran out or another warp already gave up.
+__device__ __forceinline__ bool warp_wait(SmemCtl *ctl, WorkspaceHeader *hdr, uint32_t bar,
+                                          uint32_t parity)
+{
+    bool ok = false;
+    if (!ctl->abort_flag) {
+        ok = mbar_wait(bar, parity);
+        if (!ok) {
+            atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
+            ctl->abort_flag = 1;
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
 template <int KMAX>
-__device__ void run_consumer(const ScoreParams &p, uint8_t *smem, SmemCtl *ctl, const int *prefix,
-                             WorkspaceHeader *hdr, uint64_t *g_slots, int total, int split,
-                             int chunks)
+__device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_t *smem,
+                             SmemCtl *ctl, const int *prefix, WorkspaceHeader *hdr,
+                             uint64_t *g_slots)
 {
     constexpr int NR = KMAX / 8;  // list registers per lane: 4 heads x KMAX / 32 lanes
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -232,11 +255,22 @@ __device__ void run_consumer(const ScoreParams &p, uint8_t *smem, SmemCtl *ctl, 
     const int g = lane >> 2, t = lane & 3;
     uint32_t bq[8][2];
     int q_row = -1;
-    uint32_t it = 0;
-    int buf = 0;
+    uint32_t it = 0;       // pages of this CTA so far (same count as the producer's)
+    uint32_t segments = 0; // (chunk, request) segments finished so far
 
-    for (int c = blockIdx.x; c < chunks; c += gridDim.x) {
-        const int p0 = c * split, p1 = min(total, p0 + split);
+    for (uint32_t n = 0;; ++n) {
+        // next chunk id from the producer
+        const int qs = static_cast<int>(n % kChunkQueue);
+        if (!warp_wait(ctl, hdr, smem_addr(&ctl->cq_full[qs]), (n / kChunkQueue) & 1u))
+            break;
+        const int c = ctl->chunk_q[qs];
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_addr(&ctl->cq_empty[qs]));
+        if (c < 0)
+            break;
+        int p0, p1;
+        part.range(c, p0, p1);
         int pg = p0;
         while (pg < p1) {
             const int b = find_row(prefix, p.batch, pg);
@@ -252,7 +286,6 @@ __device__ void run_consumer(const ScoreParams &p, uint8_t *smem, SmemCtl *ctl, 
             for (int x = pg + skip; x < seg_end; x += kConsumerWarps) {
                 const uint32_t my = it + static_cast<uint32_t>(x - pg);
                 const int s = stage_of(my);
-                const uint32_t parity = use_of(my) & 1u;
                 const int j = x - row_first;
 
                 if (b != q_row) {  // issue the query loads before waiting on the page
@@ -266,15 +299,7 @@ __device__ void run_consumer(const ScoreParams &p, uint8_t *smem, SmemCtl *ctl, 
                     q_row = b;
                 }
 
-                bool ready = false;
-                if (!ctl->abort_flag) {
-                    ready = mbar_wait(smem_addr(&ctl->full[s]), parity);
-                    if (!ready) {
-                        atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
-                        ctl->abort_flag = 1;
-                    }
-                }
-                ready = __all_sync(0xffffffffu, ready);  // warp-uniform before any shuffle
+                const bool ready = warp_wait(ctl, hdr, smem_addr(&ctl->full[s]), use_of(my) & 1u);
                 const int2 meta = ctl->meta[s];
                 float sc[4] = {neg_inf, neg_inf, neg_inf, neg_inf};
                 const bool ok = ready && meta.y != 0;
@@ -317,104 +342,183 @@ __device__ void run_consumer(const ScoreParams &p, uint8_t *smem, SmemCtl *ctl, 
 
             // a6: combine the consumer warps' lists of this (chunk, request);
             // warp w merges heads 2w and 2w+1 and stores them in slot c + b.
+            // Double-buffered: buffer `buf` is written again two segments
+            // later, after every warp has passed the next segment's barrier
+            // (and so has finished reading this one).
+            const int buf = static_cast<int>(segments & 1u);
             uint64_t *lb = listbuf + static_cast<size_t>(buf) * kConsumerWarps * kHeads * KMAX;
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
                 const int head = r * (32 / KMAX) + lane / KMAX;
                 lb[(w * kHeads + head) * KMAX + lane % KMAX] = lst[r];
             }
-            named_barrier_sync(kListBarrier, kConsumerThreads);
+            mbar_arrive(smem_addr(&ctl->list_bar[buf]));  // every consumer thread
+            const bool lists_ready =
+                warp_wait(ctl, hdr, smem_addr(&ctl->list_bar[buf]), (segments >> 1) & 1u);
+            ++segments;
+            if (!lists_ready)
+                continue;
             static_assert(kConsumerWarps == 2, "the list merge below combines two warps' lists");
             const int slot = c + b;
+            if (slot >= p.slot_capacity) {
+                if (lane == 0)
+                    atomicOr(&hdr->fault, MSA_FAULT_SLOTS);
+                continue;
+            }
             if constexpr (KMAX == 16) {
                 // lanes 0-15: head 2w, lanes 16-31: head 2w+1; merge warp 0's and warp 1's list
                 const int h = kHeadsPerConsumer * w + (lane >> 4), r = lane & 15;
                 const uint64_t v = merge_top<16>(lb[(0 * kHeads + h) * KMAX + r],
                                                  lb[(1 * kHeads + h) * KMAX + (15 - r)], lane);
-                if (slot < p.slot_capacity)
-                    g_slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + r] = v;
+                g_slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + r] = v;
             } else {
 #pragma unroll
                 for (int hh = 0; hh < kHeadsPerConsumer; ++hh) {
                     const int h = kHeadsPerConsumer * w + hh;
                     const uint64_t v = merge_top<32>(lb[(0 * kHeads + h) * KMAX + lane],
                                                      lb[(1 * kHeads + h) * KMAX + (31 - lane)], lane);
-                    if (slot < p.slot_capacity)
-                        g_slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + lane] = v;
+                    g_slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + lane] = v;
                 }
             }
-            if (slot >= p.slot_capacity && lane == 0)
-                atomicOr(&hdr->fault, MSA_FAULT_SLOTS);
-            buf ^= 1;
         }
     }
 }
 
+// Lane-parallel lookup of up to 32 pages [pb, pe) of the batch: lane i gets
+// page pb + i's physical page, valid-token count and a validity bit.
+struct PageLookup {
+    int page, valid, ok;
+};
+
+__device__ __forceinline__ PageLookup lookup_pages(const ScoreParams &p, const int *prefix,
+                                                   WorkspaceHeader *hdr, int pb, int pe, int lane)
+{
+    PageLookup r{0, 0, 0};
+    const int pg = pb + lane;
+    if (pg < pe) {
+        const int b = find_row(prefix, p.batch, pg);
+        const int j = pg - prefix[b];
+        r.page = p.block_table[static_cast<int64_t>(b) * p.bt_stride + j];
+        r.valid = min(kPage, p.seq_lens[b] - j * kPage);
+        r.ok = (r.page >= 0 && r.page < p.num_pages) ? 1 : 0;
+        if (!r.ok)
+            atomicOr(&hdr->fault, MSA_FAULT_PAGE_ID);
+    }
+    return r;
+}
+
+// A pool ticket (valid in lane 0); its atomic stays in flight until resolved.
+__device__ __forceinline__ unsigned take_ticket(WorkspaceHeader *hdr, int lane)
+{
+    return lane == 0 ? atomicAdd(&hdr->pool_next, 1u) : 0u;
+}
+
+// The chunk behind a ticket; tickets past the batch are skipped.  -1: none left.
+__device__ __forceinline__ int resolve_ticket(const Partition &part, WorkspaceHeader *hdr,
+                                              unsigned ticket, int lane)
+{
+    if (part.pool == 0)
+        return -1;
+    int c = part.pool_chunk(static_cast<int>(__shfl_sync(0xffffffffu, ticket, 0)));
+    while (c == -2)
+        c = part.pool_chunk(static_cast<int>(__shfl_sync(0xffffffffu, take_ticket(hdr, lane), 0)));
+    return c;
+}
+
 template <int KMAX>
-__device__ void run_producer(const ScoreParams &p, uint8_t *smem, SmemCtl *ctl, const int *prefix,
-                             WorkspaceHeader *hdr, int total, int split, int chunks)
+__device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_t *smem,
+                             SmemCtl *ctl, const int *prefix, WorkspaceHeader *hdr)
 {
     const int lane = threadIdx.x & 31;
     const uint32_t stage0 = smem_addr(smem + SmemLayout<KMAX>::stages);
-    uint32_t it = 0;
+    uint32_t it = 0;  // pages issued
+    uint32_t n = 0;   // chunk ids posted
 
-    for (int c = blockIdx.x; c < chunks; c += gridDim.x) {
-        const int p0 = c * split, p1 = min(total, p0 + split);
-        // lane-parallel lookup of 32 pages, one batch ahead of the issue loop
-        auto lookup = [&](int pb, int &page, int &valid, int &ok) {
-            const int pg = pb + lane;
-            page = 0;
-            valid = 0;
-            ok = 0;
-            if (pg < p1) {
-                const int b = find_row(prefix, p.batch, pg);
-                const int j = pg - prefix[b];
-                page = p.block_table[static_cast<int64_t>(b) * p.bt_stride + j];
-                valid = min(kPage, p.seq_lens[b] - j * kPage);
-                ok = (page >= 0 && page < p.num_pages) ? 1 : 0;
-                if (!ok)
-                    atomicOr(&hdr->fault, MSA_FAULT_PAGE_ID);
+    auto post = [&](int c) {
+        if (lane == 0) {
+            const int qs = static_cast<int>(n % kChunkQueue);
+            if (n >= kChunkQueue && !ctl->abort_flag &&
+                !mbar_wait(smem_addr(&ctl->cq_empty[qs]), ((n / kChunkQueue) - 1) & 1u)) {
+                atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
+                ctl->abort_flag = 1;
             }
-        };
-        int n_page, n_valid, n_ok;
-        lookup(p0, n_page, n_valid, n_ok);
-        for (int pb = p0; pb < p1; pb += 32) {
-            const int c_page = n_page, c_valid = n_valid, c_ok = n_ok;
-            if (pb + 32 < p1)
-                lookup(pb + 32, n_page, n_valid, n_ok);
-            const int n = min(32, p1 - pb);
-            for (int i = 0; i < n; ++i, ++it) {
-                const int page = __shfl_sync(0xffffffffu, c_page, i);
-                const int valid = __shfl_sync(0xffffffffu, c_valid, i);
-                const int ok = __shfl_sync(0xffffffffu, c_ok, i);
-                if (lane == 0) {
-                    const int s = stage_of(it);
-                    const uint32_t full = smem_addr(&ctl->full[s]);
-                    if (it >= kStages && !ctl->abort_flag) {
-                        if (!mbar_wait(smem_addr(&ctl->empty[s]), (use_of(it) - 1) & 1u)) {
-                            atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
-                            ctl->abort_flag = 1;
-                        }
-                    }
-                    const bool issue = ok && !ctl->abort_flag;
-                    ctl->meta[s] = make_int2(valid, issue ? 1 : 0);
-                    if (issue) {
-                        const uint32_t dst = stage0 + s * kPageBytes;
-                        mbar_arrive_expect_tx(full, kPageBytes);
-                        tma_load_2d(dst, &p.tmap, 0, page * kPage, full);
-                        tma_load_2d(dst + kHalfPageBytes, &p.tmap, 64, page * kPage, full);
-                    } else {
-                        mbar_arrive(full);
+            ctl->chunk_q[qs] = c;
+            mbar_arrive(smem_addr(&ctl->cq_full[qs]));
+        }
+        ++n;
+        __syncwarp();
+    };
+
+    // This CTA's static chunk first, then pool chunks.  A batch of up to 32
+    // pages is always issued before anything that waits on global memory
+    // (the next batch's lookups, a pool ticket): the pages already in the
+    // stage ring keep the consumers and HBM busy across those waits.
+    int cur = part.first_chunk(blockIdx.x);
+    if (cur < 0 && part.pool > 0)
+        cur = resolve_ticket(part, hdr, take_ticket(hdr, lane), lane);
+    int a = 0, e = 0;
+    PageLookup look{0, 0, 0};
+    if (cur >= 0) {
+        post(cur);  // consumers can start their query loads at once
+        part.range(cur, a, e);
+        look = lookup_pages(p, prefix, hdr, a, e, lane);
+    }
+    while (cur >= 0) {
+        const int cnt = min(32, e - a);
+        for (int i = 0; i < cnt; ++i, ++it) {
+            const int page = __shfl_sync(0xffffffffu, look.page, i);
+            const int valid = __shfl_sync(0xffffffffu, look.valid, i);
+            const int ok = __shfl_sync(0xffffffffu, look.ok, i);
+            if (lane == 0) {
+                const int s = stage_of(it);
+                const uint32_t full = smem_addr(&ctl->full[s]);
+                if (it >= kStages && !ctl->abort_flag) {
+                    if (!mbar_wait(smem_addr(&ctl->empty[s]), (use_of(it) - 1) & 1u)) {
+                        atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
+                        ctl->abort_flag = 1;
                     }
                 }
-                __syncwarp();
+                const bool issue = ok && !ctl->abort_flag;
+                ctl->meta[s] = make_int2(valid, issue ? 1 : 0);
+                if (issue) {
+                    const uint32_t dst = stage0 + s * kPageBytes;
+                    mbar_arrive_expect_tx(full, kPageBytes);
+                    tma_load_2d(dst, &p.tmap, 0, page * kPage, full);
+                    tma_load_2d(dst + kHalfPageBytes, &p.tmap, 64, page * kPage, full);
+                } else {
+                    mbar_arrive(full);
+                }
             }
+            __syncwarp();
+        }
+        if (a + 32 < e) {  // next batch of the same chunk
+            a += 32;
+            look = lookup_pages(p, prefix, hdr, a, e, lane);
+            continue;
+        }
+        cur = part.pool > 0 ? resolve_ticket(part, hdr, take_ticket(hdr, lane), lane) : -1;
+        if (cur < 0)
+            break;
+        post(cur);
+        part.range(cur, a, e);
+        look = lookup_pages(p, prefix, hdr, a, e, lane);
+    }
+    post(-1);  // no more chunks
+
+    // This CTA takes no more tickets; the last CTA to get here resets the
+    // counters for the next pass (every other CTA has stopped claiming).
+    // Without a pool no ticket was taken and the counters stay at zero.
+    if (lane == 0 && part.pool > 0) {
+        __threadfence();
+        if (atomicAdd(&hdr->done, 1u) == gridDim.x - 1) {
+            atomicExch(&hdr->pool_next, 0u);
+            atomicExch(&hdr->done, 0u);
         }
     }
     // Drain: no copy may still be landing in shared memory when the CTA exits.
     if (lane == 0) {
-        const uint32_t n = it < kStages ? it : kStages;
-        for (uint32_t i = 0; i < n; ++i) {
+        const uint32_t cnt = it < kStages ? it : kStages;
+        for (uint32_t i = 0; i < cnt; ++i) {
             const uint32_t q = it - 1 - i;
             if (!mbar_wait(smem_addr(&ctl->full[stage_of(q)]), use_of(q) & 1u))
                 atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
@@ -439,79 +543,110 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
             mbar_init(smem_addr(&ctl->full[s]), 1);
             mbar_init(smem_addr(&ctl->empty[s]), 1);
         }
+        for (int i = 0; i < kChunkQueue; ++i) {
+            mbar_init(smem_addr(&ctl->cq_full[i]), 1);
+            mbar_init(smem_addr(&ctl->cq_empty[i]), kConsumerWarps);
+        }
+        for (int i = 0; i < 2; ++i)
+            mbar_init(smem_addr(&ctl->list_bar[i]), kConsumerThreads);
         ctl->abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == kProducerWarp && (threadIdx.x & 31) == 0)
         prefetch_tensormap(&p.tmap);
+    // Everything above touched only this CTA's shared memory and the kernel
+    // parameters; global memory is read and written only after the previous
+    // kernel on the stream has finished.
+    griddep_wait();
+    griddep_launch_dependents();
 
     build_prefix(p, prefix, ctl, hdr);  // ends with __syncthreads
 
-    const int total = prefix[p.batch];
-    const int split = p.split_blocks > 0 ? p.split_blocks : max(1, ceil_div_i(total, gridDim.x));
-    const int chunks = total > 0 ? ceil_div_i(total, split) : 0;
-
+    if (threadIdx.x == 0)
+        ctl->part = Partition::make(prefix[p.batch], gridDim.x, p.split_blocks);
+    __syncthreads();
+    const Partition &part = ctl->part;
     if (blockIdx.x == 0) {
         int *g_prefix = reinterpret_cast<int *>(p.ws + prefix_offset());
         for (int b = threadIdx.x; b <= p.batch; b += kThreads)
             g_prefix[b] = prefix[b];
         if (threadIdx.x == 0) {
-            hdr->split = split;
-            hdr->total = total;
-            hdr->chunks = chunks;
+            hdr->part = part;
             hdr->batch = p.batch;
             hdr->kmax = KMAX;
         }
     }
 
     if (warp == kProducerWarp)
-        run_producer<KMAX>(p, smem, ctl, prefix, hdr, total, split, chunks);
+        run_producer<KMAX>(p, part, smem, ctl, prefix, hdr);
     else
-        run_consumer<KMAX>(p, smem, ctl, prefix, hdr, g_slots, total, split, chunks);
+        run_consumer<KMAX>(p, part, smem, ctl, prefix, hdr, g_slots);
 }
 
-// a7: one CTA per (head, request).  Groups of KMAX lanes each fold a share of
-// the request's chunk lists into a running top-KMAX, then a tree in shared
-// memory merges the groups.
+// a7: one CTA per (head, request).  The request's chunk lists are staged in
+// shared memory a tile at a time (all loads in flight together), each group of
+// KMAX lanes folds every kGroups-th list of the tile into a running top-KMAX,
+// and a tree over the groups yields the request's top-KMAX for the head.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeTileKeys = 2048;  // 16 KiB of keys staged per pass
+
 template <int KMAX>
-__global__ void __launch_bounds__(128) merge_kernel(const uint8_t *ws, int batch, int k,
-                                                    int slot_capacity, int32_t *out_ids,
-                                                    float *out_scores)
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const uint8_t *ws, int batch, int k,
+                                                              int slot_capacity, int32_t *out_ids,
+                                                              float *out_scores)
 {
-    constexpr int kGroups = 128 / KMAX;
-    __shared__ uint64_t part[128];
+    constexpr int kGroups = kMergeThreads / KMAX;
+    constexpr int kTileLists = kMergeTileKeys / KMAX;
+    __shared__ uint64_t tile[kMergeTileKeys];
+    __shared__ uint64_t tree[kMergeThreads];
+    // the score grid's workspace writes are complete and visible after this
+    griddep_wait();
+    griddep_launch_dependents();
+
     const int h = blockIdx.x, b = blockIdx.y;
     const int lane = threadIdx.x & 31, grp = threadIdx.x / KMAX, rank = threadIdx.x % KMAX;
     const WorkspaceHeader *hdr = reinterpret_cast<const WorkspaceHeader *>(ws);
     const int *prefix = reinterpret_cast<const int *>(ws + prefix_offset());
     const uint64_t *slots = reinterpret_cast<const uint64_t *>(ws + slots_offset(batch));
 
-    const int split = hdr->split;
+    const Partition &part = hdr->part;
     const int p0 = prefix[b], p1 = prefix[b + 1];
     int c_first = 0, n_lists = 0;
-    if (p1 > p0 && split > 0) {
-        c_first = p0 / split;
-        n_lists = min((p1 - 1) / split - c_first + 1, slot_capacity);
+    if (p1 > p0 && part.unit > 0 && p1 <= part.total) {
+        c_first = part.chunk_of(p0);
+        n_lists = min(part.chunk_of(p1 - 1) - c_first + 1, slot_capacity);
     }
 
     uint64_t run = 0;
-    for (int base = 0; base < n_lists; base += kGroups) {
-        const int i = base + grp;
-        const int slot = c_first + i + b;
-        uint64_t other = 0;
-        if (i < n_lists && slot < slot_capacity)
-            other = slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + (KMAX - 1 - rank)];
-        run = merge_top<KMAX>(run, other, lane);
+    for (int t0 = 0; t0 < n_lists; t0 += kTileLists) {
+        const int nt = min(kTileLists, n_lists - t0);
+        for (int e = threadIdx.x; e < nt * KMAX; e += kMergeThreads) {
+            const int li = e / KMAX, r = e % KMAX;
+            const int slot = c_first + t0 + li + b;
+            tile[e] = slot < slot_capacity
+                          ? slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + r]
+                          : 0ull;
+        }
+        __syncthreads();
+        for (int base = 0; base < nt; base += kGroups) {
+            const int li = base + grp;
+            const uint64_t other = li < nt ? tile[li * KMAX + (KMAX - 1 - rank)] : 0ull;
+            run = merge_top<KMAX>(run, other, lane);
+        }
+        __syncthreads();
     }
-    part[threadIdx.x] = run;
+    tree[threadIdx.x] = run;
     __syncthreads();
+    const int used = min(n_lists, kGroups);  // groups holding anything
 #pragma unroll
     for (int step = 1; step < kGroups; step <<= 1) {
+        if (step >= used)
+            break;  // uniform across the CTA
         const bool active = (grp % (2 * step)) == 0 && grp + step < kGroups;
-        const uint64_t other = active ? part[(grp + step) * KMAX + (KMAX - 1 - rank)] : 0ull;
+        const uint64_t other = active ? tree[(grp + step) * KMAX + (KMAX - 1 - rank)] : 0ull;
         run = merge_top<KMAX>(run, other, lane);
         __syncthreads();
-        part[threadIdx.x] = run;
+        tree[threadIdx.x] = run;
         __syncthreads();
     }
     if (grp == 0 && rank < k) {
@@ -527,6 +662,26 @@ __global__ void __launch_bounds__(128) merge_kernel(const uint8_t *ws, int batch
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+
+// Launch configuration with programmatic dependent launch: the grid may be
+// scheduled while the previous kernel on the stream is still running; it
+// calls griddep_wait() before touching global memory, so it observes all of
+// that kernel's writes (and the previous kernel cannot see any of its own).
+static cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                     cudaLaunchAttribute (&attr)[1])
+{
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -577,12 +732,6 @@ static bool ensure_smem_attr(int dev)
     return true;
 }
 
-struct Geometry {
-    int grid;
-    int64_t chunks_bound;
-    int64_t max_blocks;
-};
-
 static int64_t blocks_for(int max_model_len) { return (static_cast<int64_t>(max_model_len) + kPage - 1) / kPage; }
 
 static bool bounds_ok(int max_batch, int max_model_len, int k, int split_blocks)
@@ -596,9 +745,7 @@ static bool bounds_ok(int max_batch, int max_model_len, int k, int split_blocks)
 
 static int64_t chunk_bound(int batch, int64_t max_blocks, int split_blocks, int grid)
 {
-    if (split_blocks == 0)
-        return grid;
-    return (static_cast<int64_t>(batch) * max_blocks + split_blocks - 1) / split_blocks;
+    return chunk_capacity(grid, static_cast<int64_t>(batch) * max_blocks, split_blocks);
 }
 
 static msa_status validate(const void *q, const void *kcache_pool, int64_t num_pages,
@@ -682,8 +829,9 @@ static msa_status launch_score(const void *q, const void *kcache_pool, int64_t n
     if (!ensure_smem_attr<KMAX>(dev))
         return MSA_ERR_CUDA;
     const size_t smem = SmemLayout<KMAX>::bytes(batch);
-    score_kernel<KMAX><<<grid, kThreads, smem, st>>>(p);
-    return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kThreads), smem, st, attr);
+    return cudaLaunchKernelEx(&cfg, score_kernel<KMAX>, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 struct Plan {
@@ -778,13 +926,16 @@ extern "C" msa_status msa_indexer_merge(int batch, int k, int32_t *out_ids, floa
     const int64_t cap = static_cast<int64_t>((workspace_bytes - off) / slot_bytes(kmax));
     const int capacity = static_cast<int>(cap > (int64_t{1} << 30) ? (int64_t{1} << 30) : cap);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const dim3 grid(kHeads, static_cast<unsigned>(batch));
     const uint8_t *ws = static_cast<const uint8_t *>(workspace);
-    if (kmax == 16)
-        merge_kernel<16><<<grid, 128, 0, s>>>(ws, batch, k, capacity, out_ids, out_scores);
-    else
-        merge_kernel<32><<<grid, 128, 0, s>>>(ws, batch, k, capacity, out_ids, out_scores);
-    return cudaGetLastError() == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(kHeads, static_cast<unsigned>(batch)),
+                                        dim3(kMergeThreads), 0, s, attr);
+    cudaError_t e = kmax == 16
+                        ? cudaLaunchKernelEx(&cfg, merge_kernel<16>, ws, batch, k, capacity,
+                                             out_ids, out_scores)
+                        : cudaLaunchKernelEx(&cfg, merge_kernel<32>, ws, batch, k, capacity,
+                                             out_ids, out_scores);
+    return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 extern "C" msa_status msa_indexer_decode(const void *q, const void *kcache_pool, int64_t num_pages,
@@ -817,16 +968,25 @@ static __device__ __align__(256) uint8_t g_noalloc_workspace[MSA_NOALLOC_WORKSPA
 
 // Device address of g_noalloc_workspace on device `dev` (the current device),
 // looked up once per device.  In host code the array's name only stands in
-// for it; the kernels must be given this address.
+// for it; the kernels must be given this address.  The same set-up clears
+// the header once: its ticket counters must start at zero (the score kernel
+// returns them to zero at the end of every pass).
 static void *noalloc_workspace(int dev)
 {
     static std::atomic<void *> addr[kMaxDevices];
+    static std::mutex setup;
     if (dev < 0 || dev >= kMaxDevices)
         return nullptr;
     void *p = addr[dev].load(std::memory_order_acquire);
     if (p != nullptr)
         return p;
+    std::lock_guard<std::mutex> lock(setup);
+    p = addr[dev].load(std::memory_order_acquire);
+    if (p != nullptr)
+        return p;
     if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || p == nullptr)
+        return nullptr;
+    if (cudaMemset(p, 0, kHeaderBytes) != cudaSuccess)
         return nullptr;
     addr[dev].store(p, std::memory_order_release);
     return p;
@@ -858,7 +1018,9 @@ extern "C" msa_status msa_indexer_decode_noalloc(const void *q, const void *kcac
         return MSA_ERR_CUDA;
     const int grid = score_grid(sms, batch, blocks_for(max_model_len), 0);
     const size_t need = slots_offset(batch) +
-                        static_cast<size_t>(grid + batch) * slot_bytes(kmax_for(k));
+                        static_cast<size_t>(chunk_bound(batch, blocks_for(max_model_len), 0, grid) +
+                                            batch) *
+                            slot_bytes(kmax_for(k));
     if (need > MSA_NOALLOC_WORKSPACE_BYTES)
         return MSA_ERR_UNSUPPORTED;
     void *ws = noalloc_workspace(dev);

@@ -105,9 +105,19 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads)
+// Programmatic dependent launch: wait until the preceding grid on the stream
+// has completed and its memory is visible (no-op without a preceding grid).
+__device__ __forceinline__ void griddep_wait()
 {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+
+// Allow the next grid on the stream to be scheduled (it still waits for this
+// grid's completion before reading memory).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 
 }  // namespace msa
