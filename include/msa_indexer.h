@@ -167,6 +167,34 @@ msa_status msa_indexer_merge(int batch, int k, int32_t *out_ids, float *out_scor
                              const void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Expands each selected 128-token block into the ids of the smaller KV-cache
+ * pages it spans, so a sparse attention kernel that reads the KV cache in
+ * `page_tokens`-token pages can consume the selection through a compact page
+ * table without moving KV data (vLLM blog "Following the Bottleneck:
+ * Optimizing MiniMax M3 on AMD Instinct MI355X", section 3 "Which bytes
+ * move?", figure 5: each selected block id becomes eight 16-token page ids).
+ *
+ *   ids            int32 [batch, 4, k]: selected block ids as written by
+ *                  msa_indexer_decode (-1 = none; ids outside the request
+ *                  are ignored).
+ *   seq_lens       int32 [batch]: the same lengths the selection used.
+ *   kv_block_table int32 [batch, kv_bt_stride]: small page p of request b ->
+ *                  physical KV page.  Entries p < min(ceil(seq_len /
+ *                  page_tokens), kv_bt_stride) are read.
+ *   page_tokens    a divisor of 128 (16 for eight pages per block).
+ *   out_pages      int32 [batch, 4, k * 128 / page_tokens]: per (request,
+ *                  head) the selected blocks in increasing block id, each as
+ *                  its existing small pages in order, then -1.
+ *   out_num_pages  int32 [batch, 4]: entries used in each row of out_pages.
+ *
+ * All device memory, enqueued on `stream`; one kernel, no workspace.
+ */
+msa_status msa_indexer_expand_pages(const int32_t *ids, int batch, int k, const int32_t *seq_lens,
+                                    const int32_t *kv_block_table, int64_t kv_bt_stride,
+                                    int page_tokens, int32_t *out_pages, int32_t *out_num_pages,
+                                    void *stream);
+
+/*
  * Reads the workspace fault word (MSA_FAULT_* bits) into *flags and clears
  * it.  Synchronises `stream`.  Returns MSA_ERR_INVALID_ARG for null
  * pointers, MSA_ERR_CUDA if a CUDA call fails.

@@ -60,6 +60,8 @@ class Oracle:
         lib.msa_oracle_select.restype = c_int
         lib.msa_oracle_select_split.argtypes = [P, c_int, c_i64, P, c_int, c_int, c_int, c_i64, P, P]
         lib.msa_oracle_select_split.restype = c_int
+        lib.msa_oracle_expand_pages.argtypes = [P, c_int, c_int, P, P, c_i64, c_int, P, P]
+        lib.msa_oracle_expand_pages.restype = c_int
         lib.msa_oracle_num_threads.argtypes = []
         lib.msa_oracle_num_threads.restype = c_int
         self.lib = lib
@@ -118,6 +120,23 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle refused the selection arguments (code {rc})")
         return ids, out
+
+    def expand_pages(self, ids: np.ndarray, seq_lens: np.ndarray, kv_block_table: np.ndarray,
+                     page_tokens: int = 16) -> Tuple[np.ndarray, np.ndarray]:
+        """Selected blocks -> small KV page ids: (pages [B,4,k*128/pt], counts [B,4])."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        seq = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        kvb = np.ascontiguousarray(kv_block_table, dtype=np.int32)
+        B, H, k = ids.shape
+        width = k * (PAGE // page_tokens)
+        pages = np.empty((B, HEADS, width), dtype=np.int32)
+        num = np.empty((B, HEADS), dtype=np.int32)
+        rc = self.lib.msa_oracle_expand_pages(self._ptr(ids), B, k, self._ptr(seq), self._ptr(kvb),
+                                              kvb.shape[1], page_tokens, self._ptr(pages),
+                                              self._ptr(num))
+        if rc != 0:
+            raise ValueError(f"oracle refused the expansion arguments (code {rc})")
+        return pages, num
 
     def run(self, w, k: Optional[int] = None, n_sink: Optional[int] = None,
             n_window: Optional[int] = None):

@@ -48,6 +48,16 @@
  *      and selects again over that candidate set.  It must agree with the
  *      unsplit selection.
  *
+ *   5. Page expansion.  The downstream sparse attention reads the KV cache in
+ *      pages smaller than the indexer's 128-token blocks; each selected block
+ *      is turned into the ids of the small pages it spans, through the KV
+ *      cache's own block table, without moving KV data (vLLM blog "Following
+ *      the Bottleneck", section 3 "Which bytes move?" and its figure 5: every
+ *      selected block id becomes eight 16-token page ids in a compact page
+ *      table).  msa_oracle_expand_pages() lists, per (request, head), the
+ *      selected blocks in increasing block id, each expanded to its existing
+ *      small pages in order, then pads with -1 and reports the count.
+ *
  * Layouts (all host memory, row-major, caller-owned):
  *   q        uint16 bf16 bits [B][4][128]
  *   pool     uint16 bf16 bits [num_pages][128][128]   (page, token, dim)
@@ -312,5 +322,58 @@ int msa_oracle_select_split(const double *scores, int batch, int64_t bt_stride,
     free(scratch);
     free(sid);
     free(ssc);
+    return 0;
+}
+
+static int cmp_int(const void *pa, const void *pb)
+{
+    int a = *(const int *)pa, b = *(const int *)pb;
+    return (a > b) - (a < b);
+}
+
+/*
+ * Step 5: ids int32 [B][4][k] (as from msa_oracle_select, -1 = none);
+ * kv_bt int32 [B][kv_stride]: small page p of request b -> physical page;
+ * out_pages int32 [B][4][k * (128 / page_tokens)]; out_num int32 [B][4].
+ */
+int msa_oracle_expand_pages(const int32_t *ids, int batch, int k, const int32_t *seq_lens,
+                            const int32_t *kv_bt, int64_t kv_stride, int page_tokens,
+                            int32_t *out_pages, int32_t *out_num)
+{
+    if (batch < 0 || k < 1 || page_tokens < 1 || PAGE % page_tokens != 0 || kv_stride < 1)
+        return -1;
+    const int per_block = PAGE / page_tokens;
+    const int64_t width = (int64_t)k * per_block;
+    int *sel = (int *)malloc((size_t)k * sizeof(int));
+    if (!sel)
+        return -5;
+    for (int b = 0; b < batch; ++b) {
+        int64_t small_pages = seq_lens[b] > 0 ? ((int64_t)seq_lens[b] + page_tokens - 1) / page_tokens : 0;
+        if (small_pages > kv_stride) {
+            free(sel);
+            return -2;
+        }
+        for (int h = 0; h < HEADS; ++h) {
+            const int32_t *row = ids + ((int64_t)b * HEADS + h) * k;
+            int32_t *out = out_pages + ((int64_t)b * HEADS + h) * width;
+            int n_sel = 0;
+            for (int r = 0; r < k; ++r)
+                if (row[r] >= 0)
+                    sel[n_sel++] = row[r];
+            qsort(sel, (size_t)n_sel, sizeof(int), cmp_int);
+            int64_t n = 0;
+            for (int i = 0; i < n_sel; ++i) {
+                for (int s = 0; s < per_block; ++s) {
+                    int64_t p = (int64_t)sel[i] * per_block + s;
+                    if (p < small_pages)
+                        out[n++] = kv_bt[(int64_t)b * kv_stride + p];
+                }
+            }
+            out_num[b * HEADS + h] = (int32_t)n;
+            for (; n < width; ++n)
+                out[n] = -1;
+        }
+    }
+    free(sel);
     return 0;
 }

@@ -40,6 +40,7 @@ EXPORTED = (
     "msa_indexer_get_error",
     "msa_status_string",
     "msa_indexer_decode_noalloc",
+    "msa_indexer_expand_pages",
 )
 
 _lib = None
@@ -80,6 +81,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.msa_indexer_get_error.restype = c_int
     lib.msa_indexer_decode_noalloc.argtypes = common[:7] + common[8:] + [P, P, P, P]
     lib.msa_indexer_decode_noalloc.restype = c_int
+    lib.msa_indexer_expand_pages.argtypes = [P, c_int, c_int, P, P, c_i64, c_int, P, P, P]
+    lib.msa_indexer_expand_pages.restype = c_int
     lib.msa_status_string.argtypes = [c_int]
     lib.msa_status_string.restype = ctypes.c_char_p
     if path is None:
@@ -177,6 +180,19 @@ def msa_indexer_decode_noalloc(q, kcache_pool, block_table, seq_lens, k: int, n_
         max_model_len, k, n_sink, n_window, _ptr(out_ids), _ptr(out_scores),
         _ptr(out_block_scores), _stream_ptr(stream))
     _check(st, "msa_indexer_decode_noalloc")
+
+
+def msa_indexer_expand_pages(ids, seq_lens, kv_block_table, out_pages, out_num_pages, *,
+                             page_tokens: int = 16, stream=None) -> None:
+    """msa_indexer_expand_pages(): selected blocks -> small KV page ids."""
+    import torch
+    assert ids.dtype == torch.int32 and ids.is_contiguous() and ids.dim() == 3
+    assert kv_block_table.dtype == torch.int32 and kv_block_table.stride(1) == 1
+    B, _, k = ids.shape
+    st = load().msa_indexer_expand_pages(_ptr(ids), B, k, _ptr(seq_lens), _ptr(kv_block_table),
+                                         int(kv_block_table.stride(0)), page_tokens,
+                                         _ptr(out_pages), _ptr(out_num_pages), _stream_ptr(stream))
+    _check(st, "msa_indexer_expand_pages")
 
 
 def msa_indexer_get_error(workspace, *, stream=None) -> int:

@@ -659,6 +659,61 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const uint8_t *ws,
     }
 }
 
+// Selected blocks -> small KV pages.  One warp per (request, head): the
+// <= 32 selected ids are sorted ascending across the lanes (bitonic), each
+// lane counts the small pages of its block, a lane prefix gives the output
+// offsets, and each lane copies its pages' ids from the KV block table.
+__global__ void __launch_bounds__(128) expand_pages_kernel(const int32_t *ids, int k,
+                                                          const int32_t *seq_lens,
+                                                          const int32_t *kv_bt, int64_t kv_stride,
+                                                          int per_block, int page_tokens,
+                                                          int32_t *out_pages, int32_t *out_num)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    const int b = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int L = seq_lens[b];
+    const int nb = L > 0 ? (L + kPage - 1) / kPage : 0;
+    long long small = L > 0 ? (static_cast<long long>(L) + page_tokens - 1) / page_tokens : 0;
+    if (small > kv_stride)
+        small = kv_stride;
+    const size_t row = static_cast<size_t>(b) * kHeads + h;
+    int id = lane < k ? ids[row * k + lane] : -1;
+    int key = (id >= 0 && id < nb) ? id : 0x7fffffff;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int j = size >> 1; j > 0; j >>= 1) {
+            const int other = __shfl_xor_sync(0xffffffffu, key, j);
+            const bool ascending = (lane & size) == 0;
+            const bool low = (lane & j) == 0;
+            key = (low == ascending) ? min(key, other) : max(key, other);
+        }
+    }
+    const bool valid = key != 0x7fffffff;
+    long long first = valid ? static_cast<long long>(key) * per_block : 0;
+    int count = 0;
+    if (valid && first < small)
+        count = static_cast<int>(min(static_cast<long long>(per_block), small - first));
+    int incl = count;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int width = k * per_block;
+    int32_t *out = out_pages + row * width;
+    const int32_t *src = kv_bt + static_cast<size_t>(b) * kv_stride;
+    for (int s = 0; s < count; ++s)
+        out[incl - count + s] = src[first + s];
+    for (int e = total + lane; e < width; e += 32)
+        out[e] = -1;
+    if (lane == 0)
+        out_num[row] = total;
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -1029,6 +1084,30 @@ extern "C" msa_status msa_indexer_decode_noalloc(const void *q, const void *kcac
     return msa_indexer_decode(q, kcache_pool, num_pages, block_table, bt_stride, seq_lens, batch,
                               max_batch, max_model_len, k, n_sink, n_window, out_ids, out_scores,
                               out_block_scores, ws, MSA_NOALLOC_WORKSPACE_BYTES, 0, stream);
+}
+
+extern "C" msa_status msa_indexer_expand_pages(const int32_t *ids, int batch, int k,
+                                               const int32_t *seq_lens,
+                                               const int32_t *kv_block_table,
+                                               int64_t kv_bt_stride, int page_tokens,
+                                               int32_t *out_pages, int32_t *out_num_pages,
+                                               void *stream)
+{
+    if (!ids || !seq_lens || !kv_block_table || !out_pages || !out_num_pages)
+        return MSA_ERR_INVALID_ARG;
+    if (batch < 0 || k < 1 || kv_bt_stride < 1 || page_tokens < 1 || kPage % page_tokens != 0)
+        return MSA_ERR_INVALID_ARG;
+    if (k > MSA_MAX_TOPK || batch > MSA_MAX_BATCH)
+        return MSA_ERR_UNSUPPORTED;
+    if (batch == 0)
+        return MSA_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(batch)), dim3(32 * kHeads), 0, s, attr);
+    const cudaError_t e =
+        cudaLaunchKernelEx(&cfg, expand_pages_kernel, ids, k, seq_lens, kv_block_table,
+                           kv_bt_stride, kPage / page_tokens, page_tokens, out_pages, out_num_pages);
+    return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 extern "C" msa_status msa_indexer_get_error(void *workspace, void *stream, uint32_t *flags)

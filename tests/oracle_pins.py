@@ -61,10 +61,54 @@ def build_planted(fx: dict):
 
 def load_golden():
     out = []
-    for path in sorted(glob.glob(os.path.join(GOLDEN_DIR, "*.json"))):
+    for path in sorted(glob.glob(os.path.join(GOLDEN_DIR, "planted_*.json"))):
         with open(path) as f:
             out.append(json.load(f))
     return out
+
+
+def check_expand_golden(orc) -> None:
+    with open(os.path.join(GOLDEN_DIR, "expand_pages.json")) as f:
+        fx = json.load(f)
+    seq = np.asarray(fx["seq_lens"], dtype=np.int32)
+    B, stride = seq.shape[0], int(fx["kv_stride"])
+    kvb = np.array([[1000 * b + 100 + p for p in range(stride)] for b in range(B)], dtype=np.int32)
+    ids = np.asarray(fx["ids"], dtype=np.int32)
+    pages, num = orc.expand_pages(ids, seq, kvb, int(fx["page_tokens"]))
+    np.testing.assert_array_equal(num, np.asarray(fx["expected_num"], dtype=np.int32))
+    for b in range(B):
+        for h in range(HEADS):
+            exp = fx["expected_pages_prefix"][b][h]
+            assert list(pages[b, h, :len(exp)]) == exp, (b, h)
+            assert np.all(pages[b, h, len(exp):] == -1)
+
+
+def check_expand_invariants(orc) -> None:
+    """Brute-force set view: the pages listed are exactly those of the selected blocks."""
+    rng = np.random.default_rng(17)
+    for page_tokens in (16, 32, 64, 128, 8):
+        per = 128 // page_tokens
+        for _ in range(20):
+            B, k = int(rng.integers(1, 4)), int(rng.integers(1, 17))
+            seq = rng.integers(0, 2000, size=B).astype(np.int32)
+            stride = int(-(-2000 // page_tokens)) + 1
+            kvb = rng.permutation(B * stride).astype(np.int32).reshape(B, stride)
+            ids = np.full((B, HEADS, k), -1, dtype=np.int32)
+            for b in range(B):
+                nb = -(-int(seq[b]) // 128)
+                for h in range(HEADS):
+                    m = min(k, nb)
+                    if m:
+                        ids[b, h, :m] = rng.choice(nb, size=m, replace=False)
+            pages, num = orc.expand_pages(ids, seq, kvb, page_tokens)
+            for b in range(B):
+                small = -(-int(seq[b]) // page_tokens)
+                for h in range(HEADS):
+                    want = [int(kvb[b, j * per + s]) for j in sorted(x for x in ids[b, h] if x >= 0)
+                            for s in range(per) if j * per + s < small]
+                    assert int(num[b, h]) == len(want)
+                    assert list(pages[b, h, :len(want)]) == want
+                    assert np.all(pages[b, h, len(want):] == -1)
 
 
 def check_golden(orc) -> None:
@@ -220,4 +264,5 @@ def check_invariants(orc) -> None:
     np.testing.assert_array_equal(ids_a, ids_b)
 
 
-ALL_CHECKS = (check_golden, check_scores_vs_numpy, check_select_vs_rank_count, check_invariants)
+ALL_CHECKS = (check_golden, check_scores_vs_numpy, check_select_vs_rank_count, check_invariants,
+              check_expand_golden, check_expand_invariants)

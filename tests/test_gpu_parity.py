@@ -126,3 +126,26 @@ def test_graph_replay_with_changed_lengths(lib, orc):
         o_scores, o_ids, _ = orc.run(w)
         parity.check(w, o_scores, o_ids, ids.cpu().numpy(), sc.cpu().numpy())
     assert msa.msa_indexer_get_error(ws) == 0
+
+
+@pytest.mark.parametrize("page_tokens", [16, 8, 32, 64, 128])
+def test_expand_pages_matches_oracle(lib, orc, page_tokens):
+    """Selected blocks -> small KV page ids, bit-exact against the oracle's expansion."""
+    import torch
+    for w in (wl.ragged(), wl.decode_point()):
+        ids, sc, blk, fault = parity.run_gpu(w)
+        assert fault == 0
+        per = 128 // page_tokens
+        stride = int(w.num_blocks.max()) * per + 3
+        rng = np.random.default_rng(page_tokens)
+        kvb = rng.permutation(w.batch * stride).astype(np.int32).reshape(w.batch, stride)
+        d_ids = torch.from_numpy(ids).cuda()
+        d_seq = torch.from_numpy(w.seq_lens).cuda()
+        d_kvb = torch.from_numpy(kvb).cuda()
+        pages = torch.full((w.batch, 4, w.k * per), -7, dtype=torch.int32, device="cuda")
+        num = torch.full((w.batch, 4), -7, dtype=torch.int32, device="cuda")
+        lib.msa_indexer_expand_pages(d_ids, d_seq, d_kvb, pages, num, page_tokens=page_tokens)
+        torch.cuda.synchronize()
+        e_pages, e_num = orc.expand_pages(ids, w.seq_lens, kvb, page_tokens)
+        np.testing.assert_array_equal(num.cpu().numpy(), e_num)
+        np.testing.assert_array_equal(pages.cpu().numpy(), e_pages)

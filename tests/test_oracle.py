@@ -70,3 +70,11 @@ def test_oracle_refuses_bad_pins(orc):
     s = np.zeros((1, 4, 4))
     with pytest.raises(ValueError):
         orc.select(s, np.array([512], dtype=np.int32), 2, 2, 1)
+
+
+def test_expand_pages_golden(orc):
+    pins.check_expand_golden(orc)
+
+
+def test_expand_pages_invariants(orc):
+    pins.check_expand_invariants(orc)

@@ -31,6 +31,8 @@ MUTANTS = [
     ("sink pin off by one", "return j < n_sink ||", "return j <= n_sink ||"),
     ("pad ids with 0", "out_ids[filled] = -1;", "out_ids[filled] = 0;"),
     ("bf16 read as the low half", "((uint32_t)bits) << 16", "((uint32_t)bits) << 15"),
+    ("expansion keeps the selection order", "qsort(sel, (size_t)n_sel, sizeof(int), cmp_int);", ""),
+    ("expansion includes the pages past the end", "if (p < small_pages)\n                        out[n++]", "if (p <= small_pages)\n                        out[n++]"),
 ]
 
 
