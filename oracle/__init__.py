@@ -62,6 +62,10 @@ class Oracle:
         lib.msa_oracle_select_split.restype = c_int
         lib.msa_oracle_expand_pages.argtypes = [P, c_int, c_int, P, P, c_i64, c_int, P, P]
         lib.msa_oracle_expand_pages.restype = c_int
+        lib.msa_oracle_block_scores_fp8.argtypes = [P, P, P, c_i64, P, c_i64, P, c_int, P]
+        lib.msa_oracle_block_scores_fp8.restype = c_int
+        lib.msa_oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.msa_oracle_e4m3_value.restype = ctypes.c_double
         lib.msa_oracle_num_threads.argtypes = []
         lib.msa_oracle_num_threads.restype = c_int
         self.lib = lib
@@ -87,6 +91,28 @@ class Oracle:
         rc = self.lib.msa_oracle_block_scores(self._ptr(q), self._ptr(pool), pool.shape[0],
                                               self._ptr(bt), stride, self._ptr(seq), B,
                                               self._ptr(out))
+        if rc != 0:
+            raise ValueError(f"oracle refused the inputs (code {rc})")
+        return out
+
+    def e4m3_value(self, code: int) -> float:
+        return float(self.lib.msa_oracle_e4m3_value(code))
+
+    def block_scores_fp8(self, q: np.ndarray, pool8: np.ndarray, kscale: np.ndarray,
+                         block_table: np.ndarray, seq_lens: np.ndarray) -> np.ndarray:
+        """fp64 block scores on an E4M3 cache with per-token scales."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        pool8 = np.ascontiguousarray(pool8, dtype=np.uint8)
+        kscale = np.ascontiguousarray(kscale, dtype=np.float32)
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        seq = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        B, stride = bt.shape
+        assert pool8.ndim == 3 and pool8.shape[1:] == (PAGE, DIM)
+        assert kscale.shape == pool8.shape[:2]
+        out = np.empty((B, HEADS, stride), dtype=np.float64)
+        rc = self.lib.msa_oracle_block_scores_fp8(self._ptr(q), self._ptr(pool8), self._ptr(kscale),
+                                                  pool8.shape[0], self._ptr(bt), stride,
+                                                  self._ptr(seq), B, self._ptr(out))
         if rc != 0:
             raise ValueError(f"oracle refused the inputs (code {rc})")
         return out
@@ -140,11 +166,14 @@ class Oracle:
 
     def run(self, w, k: Optional[int] = None, n_sink: Optional[int] = None,
             n_window: Optional[int] = None):
-        """Block scores and selection for a `workloads.Workload`."""
+        """Block scores and selection for a `workloads.Workload` (bf16 or fp8 cache)."""
         k = w.k if k is None else k
         n_sink = w.n_sink if n_sink is None else n_sink
         n_window = w.n_window if n_window is None else n_window
-        s = self.block_scores(w.q, w.pool, w.block_table, w.seq_lens)
+        if getattr(w, "pool8", None) is not None:
+            s = self.block_scores_fp8(w.q, w.pool8, w.kscale, w.block_table, w.seq_lens)
+        else:
+            s = self.block_scores(w.q, w.pool, w.block_table, w.seq_lens)
         ids, sc = self.select(s, w.seq_lens, k, n_sink, n_window)
         return s, ids, sc
 

@@ -58,6 +58,15 @@
  *      selected blocks in increasing block id, each expanded to its existing
  *      small pages in order, then pads with -1 and reports the count.
  *
+ *   6. fp8 index-K cache.  The index cache may be stored as FP8 E4M3 (vLLM PR
+ *      #57832, "Solution": the fp8 index cache is a separate path; SGLang PR
+ *      #41488 measured "BF16 queries, FP8 E4M3 index cache").  The pages do
+ *      not give the scale convention; the reading taken here is one fp32
+ *      scale per token: K[t,d] = e4m3(code[t,d]) * scale[t].  E4M3 (OCP FP8):
+ *      1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0
+ *      encodes subnormals m/8 * 2^-6; S.1111.111 is NaN; there is no inf.
+ *      msa_oracle_block_scores_fp8() is step 1 on that cache, in fp64.
+ *
  * Layouts (all host memory, row-major, caller-owned):
  *   q        uint16 bf16 bits [B][4][128]
  *   pool     uint16 bf16 bits [num_pages][128][128]   (page, token, dim)
@@ -90,6 +99,22 @@ static double bf16_to_double(uint16_t bits)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* The value of an FP8 E4M3 code, from the format's definition. */
+double msa_oracle_e4m3_value(uint8_t code)
+{
+    int sign = code >> 7;
+    int exponent = (code >> 3) & 0xF;
+    int mantissa = code & 0x7;
+    double magnitude;
+    if (exponent == 0xF && mantissa == 0x7)
+        return NAN;
+    if (exponent == 0)
+        magnitude = ldexp(mantissa / 8.0, -6);
+    else
+        magnitude = ldexp(1.0 + mantissa / 8.0, exponent - 7);
+    return sign ? -magnitude : magnitude;
 }
 
 static int64_t blocks_of(int32_t seq_len)
@@ -375,5 +400,52 @@ int msa_oracle_expand_pages(const int32_t *ids, int batch, int k, const int32_t 
         }
     }
     free(sel);
+    return 0;
+}
+
+/* Step 6: block scores on the fp8 cache: pool8 uint8 [num_pages][128][128]
+ * E4M3 codes, kscale float [num_pages][128] per-token scales. */
+int msa_oracle_block_scores_fp8(const uint16_t *q, const uint8_t *pool8, const float *kscale,
+                                int64_t num_pages, const int32_t *bt, int64_t bt_stride,
+                                const int32_t *seq_lens, int batch, double *scores)
+{
+    if (batch < 0 || bt_stride <= 0 || num_pages < 0)
+        return -1;
+    for (int b = 0; b < batch; ++b) {
+        if (seq_lens[b] < 0 || blocks_of(seq_lens[b]) > bt_stride)
+            return -2;
+        for (int64_t j = 0; j < blocks_of(seq_lens[b]); ++j) {
+            int32_t page = bt[(int64_t)b * bt_stride + j];
+            if (page < 0 || page >= num_pages)
+                return -3;
+        }
+    }
+    int64_t units = (int64_t)batch * bt_stride;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t u = 0; u < units; ++u) {
+        int b = (int)(u / bt_stride);
+        int64_t j = u % bt_stride;
+        int64_t nb = blocks_of(seq_lens[b]);
+        for (int h = 0; h < HEADS; ++h) {
+            double best = -INFINITY;
+            if (j < nb) {
+                int32_t page = bt[(int64_t)b * bt_stride + j];
+                int64_t valid = seq_lens[b] - j * PAGE;
+                if (valid > PAGE)
+                    valid = PAGE;
+                for (int64_t t = 0; t < valid; ++t) {
+                    const uint8_t *krow = pool8 + ((int64_t)page * PAGE + t) * DIM;
+                    const uint16_t *qrow = q + ((int64_t)b * HEADS + h) * DIM;
+                    double scale = (double)kscale[(int64_t)page * PAGE + t];
+                    double dot = 0.0;
+                    for (int d = 0; d < DIM; ++d)
+                        dot += bf16_to_double(qrow[d]) * (msa_oracle_e4m3_value(krow[d]) * scale);
+                    if (dot > best)
+                        best = dot;
+                }
+            }
+            scores[((int64_t)b * HEADS + h) * bt_stride + j] = best;
+        }
+    }
     return 0;
 }

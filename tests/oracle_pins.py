@@ -264,5 +264,62 @@ def check_invariants(orc) -> None:
     np.testing.assert_array_equal(ids_a, ids_b)
 
 
+# ----------------------------------------------------------------------------
+# fp8 E4M3 cache
+# ----------------------------------------------------------------------------
+
+def check_e4m3_codes(orc) -> None:
+    """Every E4M3 code against torch's float8_e4m3fn decoding, plus closed forms."""
+    import torch
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([orc.e4m3_value(c) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[fin], ref[fin])
+    assert got[0x38] == 1.0 and got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+    assert got[0x08] == 2.0 ** -6 and got[0x07] == 7 * 2.0 ** -9 and got[0xC0] == -2.0
+
+
+def check_fp8_golden(orc) -> None:
+    with open(os.path.join(GOLDEN_DIR, "fp8_per_token_scale.json")) as f:
+        fx = json.load(f)
+    L = int(fx["seq_len"])
+    codes = np.zeros((2, PAGE, DIM), dtype=np.uint8)
+    scale = np.ones((2, PAGE), dtype=np.float32)
+    codes[:, :, 0] = fx["code_dim0"]
+    t = np.arange(PAGE)
+    scale[0] = (t % 5) + 1
+    scale[1] = 0.5 * ((t % 3) + 1)
+    rem = L - PAGE
+    codes[1, rem::2, :] = 0x7F
+    codes[1, rem + 1::2, :] = 0x7E
+    scale[1, rem:] = 1e4
+    q = np.zeros((1, HEADS, DIM), dtype=np.float32)
+    q[0, :, 0] = fx["alpha"]
+    bt = np.array([[0, 1]], dtype=np.int32)
+    seq = np.array([L], dtype=np.int32)
+    s = orc.block_scores_fp8(wl.f32_to_bf16_bits(q), codes, scale, bt, seq)
+    ids, sc = orc.select(s, seq, int(fx["k"]), int(fx["n_sink"]), int(fx["n_window"]))
+    np.testing.assert_array_equal(ids, np.asarray(fx["expected_ids"], dtype=np.int32))
+    np.testing.assert_array_equal(sc, np.asarray(fx["expected_scores"], dtype=np.float64))
+
+
+def check_fp8_vs_numpy(orc) -> None:
+    import torch
+    table = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    w = wl.to_fp8(mixed_workload(13))
+    s = orc.block_scores_fp8(w.q, w.pool8, w.kscale, w.block_table, w.seq_lens)
+    qf = wl.bf16_bits_to_f32(w.q).astype(np.float64)
+    for b in range(w.batch):
+        L = int(w.seq_lens[b])
+        for j in range((L + PAGE - 1) // PAGE):
+            valid = min(PAGE, L - j * PAGE)
+            page = int(w.block_table[b, j])
+            kf = table[w.pool8[page, :valid]] * w.kscale[page, :valid, None].astype(np.float64)
+            ref = (qf[b] @ kf.T).max(axis=1)
+            np.testing.assert_allclose(s[b, :, j], ref, rtol=1e-12, atol=1e-12)
+
+
 ALL_CHECKS = (check_golden, check_scores_vs_numpy, check_select_vs_rank_count, check_invariants,
-              check_expand_golden, check_expand_invariants)
+              check_expand_golden, check_expand_invariants, check_e4m3_codes, check_fp8_golden,
+              check_fp8_vs_numpy)

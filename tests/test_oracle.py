@@ -78,3 +78,15 @@ def test_expand_pages_golden(orc):
 
 def test_expand_pages_invariants(orc):
     pins.check_expand_invariants(orc)
+
+
+def test_e4m3_codes(orc):
+    pins.check_e4m3_codes(orc)
+
+
+def test_fp8_golden(orc):
+    pins.check_fp8_golden(orc)
+
+
+def test_fp8_scores_match_numpy(orc):
+    pins.check_fp8_vs_numpy(orc)

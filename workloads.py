@@ -80,6 +80,8 @@ class Workload:
     exact_integers: bool = False
     split_blocks_hint: int = 0
     notes: Dict[str, object] = field(default_factory=dict)
+    pool8: Optional[np.ndarray] = None   # uint8 [num_pages, 128, 128] E4M3 codes (fp8 cache)
+    kscale: Optional[np.ndarray] = None  # float32 [num_pages, 128] per-token scales (fp8 cache)
 
     @property
     def batch(self) -> int:
@@ -99,8 +101,10 @@ class Workload:
 
     @property
     def index_k_bytes(self) -> int:
-        """Algorithmic index-K bytes: every valid token's 128 bf16 values, once."""
-        return int(self.seq_lens.astype(np.int64).sum()) * DIM * 2
+        """Algorithmic index-K bytes: every valid token's key, once (bf16: 256 B;
+        fp8: 128 B of codes + its 4-byte scale)."""
+        per_token = DIM + 4 if self.pool8 is not None else DIM * 2
+        return int(self.seq_lens.astype(np.int64).sum()) * per_token
 
     @property
     def page_bytes(self) -> int:
@@ -261,6 +265,42 @@ def adversarial(seed: int = 4, batch: int = 32, seq_len: int = 32768,
                     n_sink=1, n_window=2, max_model_len=int(nb * PAGE), seed=seed,
                     exact_integers=True, split_blocks_hint=biased_first,
                     notes={"biased_blocks": (biased_first, biased_first + biased_count)})
+
+
+FP8_MAX = 448.0
+E4M3_NAN = np.uint8(0x7F)
+E4M3_MAX_CODE = np.uint8(0x7E)
+
+
+def to_fp8(w: Workload, name: Optional[str] = None) -> Workload:
+    """The same batch with its index-K cache stored as FP8 E4M3 + one fp32 scale per token.
+
+    Each token's 128 values (the bf16 keys of `w`) are divided by
+    scale = max|K[t,:]| / 448 and rounded to E4M3 (nearest even, saturating);
+    an all-zero token gets scale 1.  Tail slots of partial last pages hold
+    NaN / 448 codes with a 1e4 scale, so a result that reads them is wrong.
+    """
+    import torch
+    pool = bf16_bits_to_f32(w.pool)  # [P, 128, 128]
+    amax = np.abs(np.nan_to_num(pool, nan=0.0)).max(axis=2)
+    scale = np.where(amax > 0, amax / np.float32(FP8_MAX), np.float32(1.0)).astype(np.float32)
+    codes = np.empty(pool.shape, dtype=np.uint8)
+    for p0 in range(0, pool.shape[0], _GEN_CHUNK_PAGES):
+        p1 = min(pool.shape[0], p0 + _GEN_CHUNK_PAGES)
+        x = torch.from_numpy(np.nan_to_num(pool[p0:p1] / scale[p0:p1, :, None], nan=0.0))
+        codes[p0:p1] = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for b, L in enumerate(w.seq_lens.tolist()):
+        rem = L % PAGE
+        if L <= 0 or rem == 0:
+            continue
+        page = int(w.block_table[b, (L - 1) // PAGE])
+        codes[page, rem::2, :] = E4M3_NAN
+        codes[page, rem + 1::2, :] = E4M3_MAX_CODE
+        scale[page, rem:] = np.float32(1e4)
+    return Workload(name=name or (w.name + "_fp8"), q=w.q, pool=w.pool, block_table=w.block_table,
+                    seq_lens=w.seq_lens, k=w.k, n_sink=w.n_sink, n_window=w.n_window,
+                    max_model_len=w.max_model_len, seed=w.seed, pool8=codes, kscale=scale,
+                    notes=dict(w.notes))
 
 
 CONFIGS = {
