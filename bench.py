@@ -33,7 +33,8 @@ if ROOT not in sys.path:
 METRIC = "indexer decode µs/call and index-K HBM GB/s (B=32, 128K ctx) vs GB300 peak"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "score_kernel_long_context.md")
+PROFILE_SUMMARY = {"bf16": os.path.join(ROOT, "profiles", "score_kernel_long_context.md"),
+                   "fp8": os.path.join(ROOT, "profiles", "score_kernel_fp8_long_context.md")}
 CSRC = os.path.join(ROOT, "sparse_attention_decode_gb300", "csrc")
 
 
@@ -45,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--batch", type=int, default=32,
                     help="requests per step (32 is the headline workload; smaller only for profiling)")
+    ap.add_argument("--cache", choices=["bf16", "fp8"], default="bf16",
+                    help="index-K cache format (bf16 is the headline; fp8 = E4M3 + per-token scale)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args(argv)
@@ -113,10 +116,10 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(batch: int):
+def profiled_traffic(batch: int, cache: str = "bf16"):
     """DRAM bytes per score launch from the committed ncu summary, if it is current."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(PROFILE_SUMMARY[cache]).read()
     except OSError:
         return None
     m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
@@ -199,10 +202,18 @@ def run_ours(args):
     msa.load()
 
     w = wl.long_context(batch=args.batch)
+    fp8 = args.cache == "fp8"
+    if fp8:
+        w = wl.to_fp8(w)
     B, k, L = w.batch, w.k, w.max_model_len
     bytes_per_step = w.index_k_bytes
     q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).to(device)
-    pool = torch.from_numpy(w.pool.view(np.int16)).view(torch.bfloat16).to(device)
+    if fp8:
+        pool8 = torch.from_numpy(w.pool8).to(device)
+        kscale = torch.from_numpy(w.kscale).to(device)
+        pool = None
+    else:
+        pool = torch.from_numpy(w.pool.view(np.int16)).view(torch.bfloat16).to(device)
     bt = torch.from_numpy(w.block_table).to(device)
     seq = torch.from_numpy(w.seq_lens).to(device)
     ids = torch.empty((B, 4, k), dtype=torch.int32, device=device)
@@ -211,12 +222,20 @@ def run_ours(args):
     stream = torch.cuda.current_stream(device)
 
     def decode(st):
-        msa.msa_indexer_decode(q, pool, bt, seq, k, w.n_sink, w.n_window, ids, sc, ws,
-                               max_model_len=L, stream=st)
+        if fp8:
+            msa.msa_indexer_decode_fp8(q, pool8, kscale, bt, seq, k, w.n_sink, w.n_window, ids, sc,
+                                       ws, max_model_len=L, stream=st)
+        else:
+            msa.msa_indexer_decode(q, pool, bt, seq, k, w.n_sink, w.n_window, ids, sc, ws,
+                                   max_model_len=L, stream=st)
 
     def score_only(st):
-        msa.msa_indexer_score(q, pool, bt, seq, k, w.n_sink, w.n_window, ws, max_model_len=L,
-                              stream=st)
+        if fp8:
+            msa.msa_indexer_score_fp8(q, pool8, kscale, bt, seq, k, w.n_sink, w.n_window, ws,
+                                      max_model_len=L, stream=st)
+        else:
+            msa.msa_indexer_score(q, pool, bt, seq, k, w.n_sink, w.n_window, ws, max_model_len=L,
+                                  stream=st)
 
     # Decode steps run from CUDA graphs, as in the serving stacks the indexer
     # lives in: one graph holds `calls` consecutive decode calls (each a whole
@@ -300,8 +319,7 @@ def run_ours(args):
             q.copy_(h_q, non_blocking=True)
             bt.copy_(h_bt, non_blocking=True)
             seq.copy_(h_seq, non_blocking=True)
-            msa.msa_indexer_decode(q, pool, bt, seq, k, w.n_sink, w.n_window, ids, sc, ws,
-                                   max_model_len=L, stream=stream)
+            decode(stream)
             h_ids.copy_(ids, non_blocking=True)
             h_sc.copy_(sc, non_blocking=True)
 
@@ -339,27 +357,30 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "fp8-e4m3 keys x bf16 q (f16 products, fp32 accumulate)" if fp8 else "bf16",
         "data": "synthetic",
         "config": {
             "workload": f"long_context: B={B} x 131072 tokens, 4 index heads, d=128, 128-token "
-                        f"pages, k=16, n_sink=1, n_window=2, {w.num_pages}-page shuffled pool",
+                        f"pages, k=16, n_sink=1, n_window=2, {w.num_pages}-page shuffled pool"
+                        + (", fp8 E4M3 cache + fp32 per-token scales" if fp8 else ""),
+            "cache": args.cache,
             "batch": B, "seq_len": 131072, "index_k_bytes_per_step": bytes_per_step,
             "split_blocks": "auto", "parallelism": f"replicas x{world}",
             "timing": "one CUDA graph of K consecutive decode calls, CUDA events on the stream",
-            "l2": "inputs larger than L2 (1 GiB index-K pool vs 129 MB L2); no flush",
+            "l2": f"inputs larger than L2 ({bytes_per_step / 2**20:.0f} MiB of index-K per step "
+                  "vs 129 MB L2); no flush",
         },
         "roofline": {
             "bound": "hbm", "kernel": "score_kernel", "achieved": round(achieved, 1),
             "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(B),
+            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(B, args.cache),
             "score_us": round(score_ms * 1e3, 2),
         },
         "gpu_launches": gpu_launches,
         "clocks": clocks,
         "e2e": e2e,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and not fp8:
         line["cpu_baseline"] = cpu_baseline(w, bytes_per_step)
     return line
 

@@ -157,6 +157,38 @@ msa_status msa_indexer_score(const void *q, const void *kcache_pool, int64_t num
                              int split_blocks, void *stream);
 
 /*
+ * msa_indexer_score / msa_indexer_decode on an FP8 E4M3 index-K cache (the
+ * cache format SGLang PR #41488 measured: "BF16 queries, FP8 E4M3 index
+ * cache").  The pages do not give the scale convention; here every token has
+ * one fp32 scale: K[t, d] = e4m3(code[t, d]) * kscale[page, t].
+ *
+ *   kcache_fp8  uint8 [num_pages, 128, 128] E4M3 codes (page, token, dim),
+ *               contiguous, 16-byte aligned.
+ *   kscale      fp32 [num_pages, 128] per-token scales, 16-byte aligned.
+ *
+ * Everything else is as for the bf16 calls (same workspace, same outputs,
+ * same msa_indexer_merge).  The products run on f16 tensor cores: E4M3 codes
+ * convert exactly to f16, and q is converted to f16 after multiplying each
+ * head by a power of two that puts its largest |q| in [2^13, 2^14), which is
+ * exact for bf16 inputs whose magnitude lies within 2^-14 .. 2^14 of that
+ * largest value.
+ */
+msa_status msa_indexer_score_fp8(const void *q, const void *kcache_fp8, const float *kscale,
+                                 int64_t num_pages, const int32_t *block_table, int64_t bt_stride,
+                                 const int32_t *seq_lens, int batch, int max_batch,
+                                 int max_model_len, int k, int n_sink, int n_window,
+                                 float *out_block_scores, void *workspace, size_t workspace_bytes,
+                                 int split_blocks, void *stream);
+
+msa_status msa_indexer_decode_fp8(const void *q, const void *kcache_fp8, const float *kscale,
+                                  int64_t num_pages, const int32_t *block_table, int64_t bt_stride,
+                                  const int32_t *seq_lens, int batch, int max_batch,
+                                  int max_model_len, int k, int n_sink, int n_window,
+                                  int32_t *out_ids, float *out_scores, float *out_block_scores,
+                                  void *workspace, size_t workspace_bytes, int split_blocks,
+                                  void *stream);
+
+/*
  * The second stage alone: merges the per-unit top-k lists that the last
  * msa_indexer_score() on this workspace left, per (request, head), into the
  * exact top-k (vLLM PR #57832, "Solution", step 4: merge per head) and

@@ -41,6 +41,8 @@ EXPORTED = (
     "msa_status_string",
     "msa_indexer_decode_noalloc",
     "msa_indexer_expand_pages",
+    "msa_indexer_score_fp8",
+    "msa_indexer_decode_fp8",
 )
 
 _lib = None
@@ -83,6 +85,11 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.msa_indexer_decode_noalloc.restype = c_int
     lib.msa_indexer_expand_pages.argtypes = [P, c_int, c_int, P, P, c_i64, c_int, P, P, P]
     lib.msa_indexer_expand_pages.restype = c_int
+    common8 = [P, P, P, c_i64, P, c_i64, P, c_int, c_int, c_int, c_int, c_int, c_int]
+    lib.msa_indexer_decode_fp8.argtypes = common8 + [P, P, P, P, c_size, c_int, P]
+    lib.msa_indexer_decode_fp8.restype = c_int
+    lib.msa_indexer_score_fp8.argtypes = common8 + [P, P, c_size, c_int, P]
+    lib.msa_indexer_score_fp8.restype = c_int
     lib.msa_status_string.argtypes = [c_int]
     lib.msa_status_string.restype = ctypes.c_char_p
     if path is None:
@@ -144,6 +151,46 @@ def msa_indexer_decode(q, kcache_pool, block_table, seq_lens, k: int, n_sink: in
         _ptr(out_scores), _ptr(out_block_scores), _ptr(workspace),
         int(workspace.numel() * workspace.element_size()), split_blocks, _stream_ptr(stream))
     _check(st, "msa_indexer_decode")
+
+
+def _fp8_args(q, kcache_fp8, kscale, block_table, seq_lens):
+    import torch
+    assert q.dtype == torch.bfloat16 and q.is_contiguous() and tuple(q.shape[1:]) == (4, 128)
+    assert kcache_fp8.element_size() == 1 and kcache_fp8.is_contiguous(), "kcache_fp8: 1-byte E4M3 codes"
+    assert tuple(kcache_fp8.shape[1:]) == (MSA_PAGE_TOKENS, MSA_HEAD_DIM)
+    assert kscale.dtype == torch.float32 and kscale.is_contiguous()
+    assert tuple(kscale.shape) == tuple(kcache_fp8.shape[:2])
+    assert block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.stride(1) == 1
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+    B = int(q.shape[0])
+    return B, int(kcache_fp8.shape[0]), int(block_table.stride(0))
+
+
+def msa_indexer_decode_fp8(q, kcache_fp8, kscale, block_table, seq_lens, k: int, n_sink: int,
+                           n_window: int, out_ids, out_scores, workspace, *,
+                           max_batch: Optional[int] = None, max_model_len: int,
+                           out_block_scores=None, split_blocks: int = 0, stream=None) -> None:
+    """msa_indexer_decode_fp8(): the decode step on an E4M3 cache with per-token scales."""
+    B, num_pages, bt_stride = _fp8_args(q, kcache_fp8, kscale, block_table, seq_lens)
+    st = load().msa_indexer_decode_fp8(
+        _ptr(q), _ptr(kcache_fp8), _ptr(kscale), num_pages, _ptr(block_table), bt_stride,
+        _ptr(seq_lens), B, B if max_batch is None else max_batch, max_model_len, k, n_sink,
+        n_window, _ptr(out_ids), _ptr(out_scores), _ptr(out_block_scores), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), split_blocks, _stream_ptr(stream))
+    _check(st, "msa_indexer_decode_fp8")
+
+
+def msa_indexer_score_fp8(q, kcache_fp8, kscale, block_table, seq_lens, k: int, n_sink: int,
+                          n_window: int, workspace, *, max_batch: Optional[int] = None,
+                          max_model_len: int, out_block_scores=None, split_blocks: int = 0,
+                          stream=None) -> None:
+    B, num_pages, bt_stride = _fp8_args(q, kcache_fp8, kscale, block_table, seq_lens)
+    st = load().msa_indexer_score_fp8(
+        _ptr(q), _ptr(kcache_fp8), _ptr(kscale), num_pages, _ptr(block_table), bt_stride,
+        _ptr(seq_lens), B, B if max_batch is None else max_batch, max_model_len, k, n_sink,
+        n_window, _ptr(out_block_scores), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), split_blocks, _stream_ptr(stream))
+    _check(st, "msa_indexer_score_fp8")
 
 
 def msa_indexer_score(q, kcache_pool, block_table, seq_lens, k: int, n_sink: int, n_window: int,

@@ -40,30 +40,54 @@
 
 namespace msa {
 
-// Pipeline shape.  Page number `it` (counted per CTA) is scored by consumer
-// warp it % kConsumerWarps in stage stage_of(it); every stage belongs to one
-// consumer warp, so each full/empty barrier has a single waiter that sees its
-// phases strictly in order (no warp can lap another warp's stage).
-constexpr int kConsumerWarps = 2;
-constexpr int kStagesPerConsumer = 3;
-constexpr int kStages = kConsumerWarps * kStagesPerConsumer;
-constexpr int kHeadsPerConsumer = kHeads / kConsumerWarps;
-constexpr int kProducerWarp = kConsumerWarps;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kConsumerThreads = 32 * kConsumerWarps;
+// Cache formats.  A page of the index-K cache is 128 tokens x 128 dims:
+//  Bf16Fmt: 32 KiB of bf16, moved as two 64x128 TMA boxes (128B swizzle);
+//  Fp8Fmt:  16 KiB of E4M3 codes (one 128x128-byte TMA box) + 512 B of
+//           per-token fp32 scales (one bulk copy).
+// Pipeline shape per format: page number `it` (counted per CTA) is scored by
+// consumer warp it % kConsumers in stage stage_of(it); every stage belongs to
+// one consumer warp, so each full/empty barrier has a single waiter that sees
+// its phases strictly in order (no warp can lap another warp's stage).  fp8
+// pages arrive twice as often and cost more to score per byte, so that
+// format runs four consumer warps.
+struct Bf16Fmt {
+    static constexpr bool kFp8 = false;
+    static constexpr int kConsumers = 2;
+    static constexpr int kStagesPer = 3;
+    static constexpr int kDataBytes = kPageBytes;
+    static constexpr int kScaleBytes = 0;
+};
 
-__host__ __device__ constexpr int stage_of(uint32_t it)
-{
-    return static_cast<int>(it % kConsumerWarps) +
-           kConsumerWarps * static_cast<int>((it / kConsumerWarps) % kStagesPerConsumer);
-}
+struct Fp8Fmt {
+    static constexpr bool kFp8 = true;
+    static constexpr int kConsumers = 4;
+    static constexpr int kStagesPer = 3;
+    static constexpr int kDataBytes = kPage * kDim;  // 16 KiB of E4M3 codes
+    static constexpr int kScaleBytes = kPage * 4;    // 512 B: one fp32 per token
+};
 
-// Use index of page `it` in its stage (its phase number on the barriers).
-__host__ __device__ constexpr uint32_t use_of(uint32_t it) { return it / kStages; }
+template <class F>
+struct Pipe {
+    static constexpr int kConsumers = F::kConsumers;
+    static constexpr int kStages = F::kConsumers * F::kStagesPer;
+    static constexpr int kProducerWarp = kConsumers;
+    static constexpr int kThreads = 32 * (kConsumers + 1);
+    static constexpr int kConsumerThreads = 32 * kConsumers;
+    static constexpr uint32_t kTxBytes = F::kDataBytes + F::kScaleBytes;
+
+    __host__ __device__ static constexpr int stage_of(uint32_t it)
+    {
+        return static_cast<int>(it % kConsumers) +
+               kConsumers * static_cast<int>((it / kConsumers) % F::kStagesPer);
+    }
+    // Use index of page `it` in its stage (its phase number on the barriers).
+    __host__ __device__ static constexpr uint32_t use_of(uint32_t it) { return it / kStages; }
+};
 
 struct ScoreParams {
-    CUtensorMap tmap;  // pool viewed as [num_pages*128 rows][128 bf16]; 64x128 boxes, 128B swizzle
+    CUtensorMap tmap;  // pool as [num_pages*128 rows][128 elements] (format-specific boxes)
     const uint16_t *q;
+    const float *kscale;  // fp8 only: [num_pages, 128] per-token scales
     const int32_t *block_table;
     const int32_t *seq_lens;
     float *out_block_scores;
@@ -80,25 +104,28 @@ struct ScoreParams {
 
 constexpr int kChunkQueue = 8;  // chunk ids the producer may post ahead of the consumers
 
+template <class F>
 struct SmemCtl {
-    uint64_t full[kStages];          // page landed (1 producer arrival + TMA bytes)
-    uint64_t empty[kStages];         // page consumed (its owner warp)
+    static constexpr int S = Pipe<F>::kStages;
+    uint64_t full[S];                // page landed (1 producer arrival + TMA bytes)
+    uint64_t empty[S];               // page consumed (its owner warp)
     uint64_t cq_full[kChunkQueue];   // chunk id posted (producer)
     uint64_t cq_empty[kChunkQueue];  // chunk id read (every consumer warp)
     uint64_t list_bar[2];            // lists of a segment written (every consumer thread)
-    int2 meta[kStages];              // (valid tokens, page ok)
+    int2 meta[S];                    // (valid tokens, page ok)
     int chunk_q[kChunkQueue];
-    int warp_sums[kConsumerWarps + 1];
+    int warp_sums[F::kConsumers + 1];
     volatile int abort_flag;
     Partition part;  // this pass's chunking, the same in every CTA
 };
 
-template <int KMAX>
+template <int KMAX, class F>
 struct SmemLayout {
-    static constexpr size_t stages = 0;
-    static constexpr size_t ctl = stages + static_cast<size_t>(kStages) * kPageBytes;
-    static constexpr size_t lists = round_up(ctl + sizeof(SmemCtl), 16);
-    static constexpr size_t list_entries = 2 * kConsumerWarps * kHeads * KMAX;
+    static constexpr size_t stages = 0;  // kStages x kDataBytes, 1024-aligned
+    static constexpr size_t scales = stages + static_cast<size_t>(Pipe<F>::kStages) * F::kDataBytes;
+    static constexpr size_t ctl = round_up(scales + static_cast<size_t>(Pipe<F>::kStages) * F::kScaleBytes, 16);
+    static constexpr size_t lists = round_up(ctl + sizeof(SmemCtl<F>), 16);
+    static constexpr size_t list_entries = 2 * F::kConsumers * kHeads * KMAX;
     static constexpr size_t prefix = lists + list_entries * sizeof(uint64_t);
     static __host__ __device__ size_t bytes(int batch)
     {
@@ -132,8 +159,10 @@ __device__ __forceinline__ int pages_of_request(const ScoreParams &p, int b)
 
 // a1: prefix[b] = pages of requests 0..b-1, computed by every CTA from the
 // live seq_lens (the grid itself never depends on them).
-__device__ void build_prefix(const ScoreParams &p, int *prefix, SmemCtl *ctl, WorkspaceHeader *hdr)
+template <class F>
+__device__ void build_prefix(const ScoreParams &p, int *prefix, SmemCtl<F> *ctl, WorkspaceHeader *hdr)
 {
+    constexpr int kThreads = Pipe<F>::kThreads;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = p.batch;
     const int per = (B + kThreads - 1) / kThreads;
@@ -218,7 +247,8 @@ __device__ __forceinline__ void score_page(uint32_t stage, const uint32_t (&bq)[
 
 // Bounded wait for the whole warp; false (and the CTA's abort flag set) when
 // the wait ran out or another warp already gave up.
-__device__ __forceinline__ bool warp_wait(SmemCtl *ctl, WorkspaceHeader *hdr, uint32_t bar,
+template <class F>
+__device__ __forceinline__ bool warp_wait(SmemCtl<F> *ctl, WorkspaceHeader *hdr, uint32_t bar,
                                           uint32_t parity)
 {
     bool ok = false;
@@ -232,18 +262,136 @@ __device__ __forceinline__ bool warp_wait(SmemCtl *ctl, WorkspaceHeader *hdr, ui
     return __all_sync(0xffffffffu, ok);
 }
 
-template <int KMAX>
+// a3 + a4 on an fp8 page.  The stage holds 128 rows of 128 E4M3 bytes with
+// the TMA 128-byte swizzle (16-byte chunk index XOR row % 8).  Lane (g, t)
+// gets bytes 4t..4t+3 of chunk ks of rows g and g+8 of each 16-row tile
+// (ldmatrix in its 16-bit view) and converts them exactly to f16 (e4m3 -> f16
+// is exact): bytes 4t, 4t+1 fill the A-fragment columns 2t, 2t+1 and bytes
+// 4t+2, 4t+3 the columns 2t+8, 2t+9.
+// q (bf16) is laid out with the same byte-to-column map, times a per-head
+// power of two that keeps it in f16's normal range; f16 mma with fp32
+// accumulation.  The per-token scale multiplies each row before the max, the
+// per-head power of two is undone after it.
+__device__ __forceinline__ void score_page_fp8(uint32_t stage, const float *scl,
+                                               const uint32_t (&bq)[8][2], int valid, int lane,
+                                               float &m0, float &m1)
+{
+    const float neg_inf = -__int_as_float(0x7f800000);
+    const int g = lane >> 2, t = lane & 3;
+    m0 = neg_inf;
+    m1 = neg_inf;
+#pragma unroll
+    for (int mt0 = 0; mt0 < 8; mt0 += 4) {
+        float acc[4][4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                acc[u][e] = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ks += 2) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                // one ldmatrix.x4 (16-bit view: a lane gets 4 bytes of one row):
+                // r0/r1 = rows g / g+8 of chunk ks, r2/r3 = the same of chunk ks+1
+                const uint32_t row = static_cast<uint32_t>((mt0 + u) * 16 + ((lane >> 3) & 1) * 8 + (lane & 7));
+                const uint32_t chunk = static_cast<uint32_t>(ks + (lane >> 4));
+                uint32_t r[4];
+                ldsm_x4(r, stage + row * 128 + ((chunk ^ (lane & 7)) << 4));
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t a[4];
+                    a[0] = e4m3x2_to_f16x2(static_cast<uint16_t>(r[2 * h] & 0xffffu));
+                    a[2] = e4m3x2_to_f16x2(static_cast<uint16_t>(r[2 * h] >> 16));
+                    a[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(r[2 * h + 1] & 0xffffu));
+                    a[3] = e4m3x2_to_f16x2(static_cast<uint16_t>(r[2 * h + 1] >> 16));
+                    mma_f16_16816(acc[u], a, bq[ks + h][0], bq[ks + h][1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int row = (mt0 + u) * 16 + g;
+            const bool v0 = row < valid, v1 = row + 8 < valid;
+            const float s0 = scl[row], s1 = scl[row + 8];
+            m0 = fmaxf(m0, v0 ? acc[u][0] * s0 : neg_inf);
+            m1 = fmaxf(m1, v0 ? acc[u][1] * s0 : neg_inf);
+            m0 = fmaxf(m0, v1 ? acc[u][2] * s1 : neg_inf);
+            m1 = fmaxf(m1, v1 ? acc[u][3] * s1 : neg_inf);
+        }
+    }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    }
+}
+
+// The query fragment of request b for the page scorer of format F.
+// bf16: the B fragment of m16n8k16 (heads in columns 0-3, 4-7 zero).
+// fp8: f16 pairs in the byte-to-column map of score_page_fp8, scaled by 2^e
+// per head so the largest |q| lands in [2^13, 2^14); inv_lo / inv_hi receive
+// 2^-e of heads 2t and 2t+1 (t = lane % 4).
+template <class F>
+__device__ __forceinline__ void load_query(const ScoreParams &p, int b, int lane,
+                                           uint32_t (&bq)[8][2], float &inv_lo, float &inv_hi)
+{
+    const int g = lane >> 2, t = lane & 3;
+    const uint16_t *qrow = p.q + (static_cast<size_t>(b) * kHeads + (g & 3)) * kDim;
+    if constexpr (!F::kFp8) {
+        const uint32_t *qw = reinterpret_cast<const uint32_t *>(qrow);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            bq[ks][0] = g < kHeads ? __ldg(qw + 8 * ks + t) : 0u;
+            bq[ks][1] = g < kHeads ? __ldg(qw + 8 * ks + 4 + t) : 0u;
+        }
+        inv_lo = inv_hi = 1.0f;
+    } else {
+        const uint2 *q8 = reinterpret_cast<const uint2 *>(qrow);  // 4 bf16 per load
+        float v[8][4];
+        float amax = 0.0f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint2 raw = g < kHeads ? __ldg(q8 + 4 * ks + t) : make_uint2(0u, 0u);
+            v[ks][0] = __uint_as_float(raw.x << 16);
+            v[ks][1] = __uint_as_float(raw.x & 0xffff0000u);
+            v[ks][2] = __uint_as_float(raw.y << 16);
+            v[ks][3] = __uint_as_float(raw.y & 0xffff0000u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                amax = fmaxf(amax, fabsf(v[ks][e]));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        int ex = 0;
+        if (amax > 0.0f)
+            frexpf(amax, &ex);              // amax = m * 2^ex, m in [0.5, 1)
+        const int sh = max(-100, min(100, 14 - ex));
+        const float up = __int_as_float((127 + sh) << 23), down = __int_as_float((127 - sh) << 23);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            bq[ks][0] = f32x2_to_f16x2(v[ks][0] * up, v[ks][1] * up);
+            bq[ks][1] = f32x2_to_f16x2(v[ks][2] * up, v[ks][3] * up);
+        }
+        inv_lo = __shfl_sync(0xffffffffu, down, (8 * t) & 31);
+        inv_hi = __shfl_sync(0xffffffffu, down, (8 * t + 4) & 31);
+    }
+}
+
+template <int KMAX, class F>
 __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_t *smem,
-                             SmemCtl *ctl, const int *prefix, WorkspaceHeader *hdr,
+                             SmemCtl<F> *ctl, const int *prefix, WorkspaceHeader *hdr,
                              uint64_t *g_slots)
 {
+    using P = Pipe<F>;
+    constexpr int C = P::kConsumers;
     constexpr int NR = KMAX / 8;  // list registers per lane: 4 heads x KMAX / 32 lanes
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const float neg_inf = -__int_as_float(0x7f800000);
-    uint64_t *listbuf = reinterpret_cast<uint64_t *>(smem + SmemLayout<KMAX>::lists);
+    uint64_t *listbuf = reinterpret_cast<uint64_t *>(smem + SmemLayout<KMAX, F>::lists);
 
-    // ldmatrix lane geometry: matrix mi = lane / 8 (rows +8 for odd, dims +8
-    // for mi >= 2), row-in-matrix r = lane % 8.
+    // ldmatrix lane geometry (bf16): matrix mi = lane / 8 (rows +8 for odd,
+    // dims +8 for mi >= 2), row-in-matrix r = lane % 8.
     const int mi = lane >> 3, rr = lane & 7;
     const uint32_t lane_off = static_cast<uint32_t>(((mi & 1) * 8 + rr) * 128);
     uint32_t xo[4];
@@ -251,9 +399,10 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
     for (int c4 = 0; c4 < 4; ++c4)
         xo[c4] = static_cast<uint32_t>((((c4 * 2 + (mi >> 1)) ^ rr) & 7) << 4);
 
-    const uint32_t stage0 = smem_addr(smem + SmemLayout<KMAX>::stages);
-    const int g = lane >> 2, t = lane & 3;
+    const uint32_t stage0 = smem_addr(smem + SmemLayout<KMAX, F>::stages);
+    const float *scales = reinterpret_cast<const float *>(smem + SmemLayout<KMAX, F>::scales);
     uint32_t bq[8][2];
+    float inv_lo = 1.0f, inv_hi = 1.0f;
     int q_row = -1;
     uint32_t it = 0;       // pages of this CTA so far (same count as the producer's)
     uint32_t segments = 0; // (chunk, request) segments finished so far
@@ -282,30 +431,31 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
             for (int r = 0; r < NR; ++r)
                 lst[r] = 0;
 
-            const int skip = (w - static_cast<int>(it % kConsumerWarps) + kConsumerWarps) % kConsumerWarps;
-            for (int x = pg + skip; x < seg_end; x += kConsumerWarps) {
+            const int skip = (w - static_cast<int>(it % C) + C) % C;
+            for (int x = pg + skip; x < seg_end; x += C) {
                 const uint32_t my = it + static_cast<uint32_t>(x - pg);
-                const int s = stage_of(my);
+                const int s = P::stage_of(my);
                 const int j = x - row_first;
 
                 if (b != q_row) {  // issue the query loads before waiting on the page
-                    const uint32_t *qw = reinterpret_cast<const uint32_t *>(
-                        p.q + (static_cast<size_t>(b) * kHeads + (g & 3)) * kDim);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        bq[ks][0] = g < kHeads ? __ldg(qw + 8 * ks + t) : 0u;
-                        bq[ks][1] = g < kHeads ? __ldg(qw + 8 * ks + 4 + t) : 0u;
-                    }
+                    load_query<F>(p, b, lane, bq, inv_lo, inv_hi);
                     q_row = b;
                 }
 
-                const bool ready = warp_wait(ctl, hdr, smem_addr(&ctl->full[s]), use_of(my) & 1u);
+                const bool ready = warp_wait(ctl, hdr, smem_addr(&ctl->full[s]), P::use_of(my) & 1u);
                 const int2 meta = ctl->meta[s];
                 float sc[4] = {neg_inf, neg_inf, neg_inf, neg_inf};
                 const bool ok = ready && meta.y != 0;
                 if (ok) {
                     float m0, m1;
-                    score_page(stage0 + s * kPageBytes, bq, meta.x, lane_off, xo, lane, m0, m1);
+                    if constexpr (F::kFp8) {
+                        score_page_fp8(stage0 + s * F::kDataBytes, scales + s * kPage, bq, meta.x,
+                                       lane, m0, m1);
+                        m0 *= inv_lo;
+                        m1 *= inv_hi;
+                    } else {
+                        score_page(stage0 + s * F::kDataBytes, bq, meta.x, lane_off, xo, lane, m0, m1);
+                    }
                     sc[0] = __shfl_sync(0xffffffffu, m0, 0);
                     sc[1] = __shfl_sync(0xffffffffu, m1, 0);
                     sc[2] = __shfl_sync(0xffffffffu, m0, 1);
@@ -340,13 +490,13 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
             it += static_cast<uint32_t>(seg_end - pg);
             pg = seg_end;
 
-            // a6: combine the consumer warps' lists of this (chunk, request);
-            // warp w merges heads 2w and 2w+1 and stores them in slot c + b.
-            // Double-buffered: buffer `buf` is written again two segments
-            // later, after every warp has passed the next segment's barrier
-            // (and so has finished reading this one).
+            // a6: combine the consumer warps' lists of this (chunk, request)
+            // and store the result in slot c + b.  Double-buffered: buffer
+            // `buf` is written again two segments later, after every warp has
+            // passed the next segment's barrier (and so has finished reading
+            // this one).
             const int buf = static_cast<int>(segments & 1u);
-            uint64_t *lb = listbuf + static_cast<size_t>(buf) * kConsumerWarps * kHeads * KMAX;
+            uint64_t *lb = listbuf + static_cast<size_t>(buf) * C * kHeads * KMAX;
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
                 const int head = r * (32 / KMAX) + lane / KMAX;
@@ -358,27 +508,39 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
             ++segments;
             if (!lists_ready)
                 continue;
-            static_assert(kConsumerWarps == 2, "the list merge below combines two warps' lists");
             const int slot = c + b;
             if (slot >= p.slot_capacity) {
                 if (lane == 0)
                     atomicOr(&hdr->fault, MSA_FAULT_SLOTS);
                 continue;
             }
-            if constexpr (KMAX == 16) {
-                // lanes 0-15: head 2w, lanes 16-31: head 2w+1; merge warp 0's and warp 1's list
-                const int h = kHeadsPerConsumer * w + (lane >> 4), r = lane & 15;
-                const uint64_t v = merge_top<16>(lb[(0 * kHeads + h) * KMAX + r],
-                                                 lb[(1 * kHeads + h) * KMAX + (15 - r)], lane);
-                g_slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + r] = v;
-            } else {
+            auto L = [&](int src, int h, int rank) { return lb[(src * kHeads + h) * KMAX + rank]; };
+            auto store = [&](int h, int rank, uint64_t v) {
+                g_slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + rank] = v;
+            };
+            if constexpr (C == 2 && KMAX == 16) {
+                // lanes 0-15: head 2w, lanes 16-31: head 2w+1
+                const int h = 2 * w + (lane >> 4), r = lane & 15;
+                store(h, r, merge_top<16>(L(0, h, r), L(1, h, 15 - r), lane));
+            } else if constexpr (C == 2) {
 #pragma unroll
-                for (int hh = 0; hh < kHeadsPerConsumer; ++hh) {
-                    const int h = kHeadsPerConsumer * w + hh;
-                    const uint64_t v = merge_top<32>(lb[(0 * kHeads + h) * KMAX + lane],
-                                                     lb[(1 * kHeads + h) * KMAX + (31 - lane)], lane);
-                    g_slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + lane] = v;
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int h = 2 * w + hh;
+                    store(h, lane, merge_top<32>(L(0, h, lane), L(1, h, 31 - lane), lane));
                 }
+            } else if constexpr (C == 4 && KMAX == 16) {
+                // head w: lanes 0-15 merge lists 0,1, lanes 16-31 lists 2,3, then the halves
+                const int half = lane >> 4, r = lane & 15;
+                uint64_t v = merge_top<16>(L(2 * half, w, r), L(2 * half + 1, w, 15 - r), lane);
+                v = merge_top<16>(v, __shfl_sync(0xffffffffu, v, 31 - lane), lane);
+                if (lane < 16)
+                    store(w, r, v);
+            } else {
+                static_assert(C == 4, "two or four consumer warps");
+                uint64_t v = merge_top<32>(L(0, w, lane), L(1, w, 31 - lane), lane);
+                const uint64_t u = merge_top<32>(L(2, w, lane), L(3, w, 31 - lane), lane);
+                v = merge_top<32>(v, __shfl_sync(0xffffffffu, u, 31 - lane), lane);
+                store(w, lane, v);
             }
         }
     }
@@ -407,7 +569,7 @@ __device__ __forceinline__ PageLookup lookup_pages(const ScoreParams &p, const i
     return r;
 }
 
-// A pool ticket (valid in lane 0); its atomic stays in flight until resolved.
+// A pool ticket (valid in lane 0).
 __device__ __forceinline__ unsigned take_ticket(WorkspaceHeader *hdr, int lane)
 {
     return lane == 0 ? atomicAdd(&hdr->pool_next, 1u) : 0u;
@@ -425,14 +587,17 @@ __device__ __forceinline__ int resolve_ticket(const Partition &part, WorkspaceHe
     return c;
 }
 
-template <int KMAX>
+template <int KMAX, class F>
 __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_t *smem,
-                             SmemCtl *ctl, const int *prefix, WorkspaceHeader *hdr)
+                             SmemCtl<F> *ctl, const int *prefix, WorkspaceHeader *hdr)
 {
+    using P = Pipe<F>;
     const int lane = threadIdx.x & 31;
-    const uint32_t stage0 = smem_addr(smem + SmemLayout<KMAX>::stages);
+    const uint32_t stage0 = smem_addr(smem + SmemLayout<KMAX, F>::stages);
+    const uint32_t scale0 = smem_addr(smem + SmemLayout<KMAX, F>::scales);
     uint32_t it = 0;  // pages issued
     uint32_t n = 0;   // chunk ids posted
+    const uint64_t stream_policy = l2_evict_first_policy();  // K is read once per pass
 
     auto post = [&](int c) {
         if (lane == 0) {
@@ -470,10 +635,10 @@ __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_
             const int valid = __shfl_sync(0xffffffffu, look.valid, i);
             const int ok = __shfl_sync(0xffffffffu, look.ok, i);
             if (lane == 0) {
-                const int s = stage_of(it);
+                const int s = P::stage_of(it);
                 const uint32_t full = smem_addr(&ctl->full[s]);
-                if (it >= kStages && !ctl->abort_flag) {
-                    if (!mbar_wait(smem_addr(&ctl->empty[s]), (use_of(it) - 1) & 1u)) {
+                if (it >= P::kStages && !ctl->abort_flag) {
+                    if (!mbar_wait(smem_addr(&ctl->empty[s]), (P::use_of(it) - 1) & 1u)) {
                         atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
                         ctl->abort_flag = 1;
                     }
@@ -481,10 +646,18 @@ __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_
                 const bool issue = ok && !ctl->abort_flag;
                 ctl->meta[s] = make_int2(valid, issue ? 1 : 0);
                 if (issue) {
-                    const uint32_t dst = stage0 + s * kPageBytes;
-                    mbar_arrive_expect_tx(full, kPageBytes);
-                    tma_load_2d(dst, &p.tmap, 0, page * kPage, full);
-                    tma_load_2d(dst + kHalfPageBytes, &p.tmap, 64, page * kPage, full);
+                    const uint32_t dst = stage0 + s * F::kDataBytes;
+                    mbar_arrive_expect_tx(full, P::kTxBytes);
+                    if constexpr (F::kFp8) {
+                        tma_load_2d_hint(dst, &p.tmap, 0, page * kPage, full, stream_policy);
+                        bulk_load_hint(scale0 + s * F::kScaleBytes,
+                                       p.kscale + static_cast<size_t>(page) * kPage, F::kScaleBytes,
+                                       full, stream_policy);
+                    } else {
+                        tma_load_2d_hint(dst, &p.tmap, 0, page * kPage, full, stream_policy);
+                        tma_load_2d_hint(dst + kHalfPageBytes, &p.tmap, 64, page * kPage, full,
+                                         stream_policy);
+                    }
                 } else {
                     mbar_arrive(full);
                 }
@@ -517,42 +690,44 @@ __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_
     }
     // Drain: no copy may still be landing in shared memory when the CTA exits.
     if (lane == 0) {
-        const uint32_t cnt = it < kStages ? it : kStages;
+        const uint32_t cnt = it < P::kStages ? it : P::kStages;
         for (uint32_t i = 0; i < cnt; ++i) {
             const uint32_t q = it - 1 - i;
-            if (!mbar_wait(smem_addr(&ctl->full[stage_of(q)]), use_of(q) & 1u))
+            if (!mbar_wait(smem_addr(&ctl->full[P::stage_of(q)]), P::use_of(q) & 1u))
                 atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
         }
     }
 }
 
-template <int KMAX>
-__global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constant__ ScoreParams p)
+template <int KMAX, class F>
+__global__ void __launch_bounds__(Pipe<F>::kThreads, 1)
+    score_kernel(const __grid_constant__ ScoreParams p)
 {
+    using P = Pipe<F>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + SmemLayout<KMAX>::ctl);
-    int *prefix = reinterpret_cast<int *>(smem + SmemLayout<KMAX>::prefix);
+    SmemCtl<F> *ctl = reinterpret_cast<SmemCtl<F> *>(smem + SmemLayout<KMAX, F>::ctl);
+    int *prefix = reinterpret_cast<int *>(smem + SmemLayout<KMAX, F>::prefix);
     WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(p.ws);
     uint64_t *g_slots = reinterpret_cast<uint64_t *>(p.ws + slots_offset(p.batch));
     const int warp = threadIdx.x >> 5;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < P::kStages; ++s) {
             mbar_init(smem_addr(&ctl->full[s]), 1);
             mbar_init(smem_addr(&ctl->empty[s]), 1);
         }
         for (int i = 0; i < kChunkQueue; ++i) {
             mbar_init(smem_addr(&ctl->cq_full[i]), 1);
-            mbar_init(smem_addr(&ctl->cq_empty[i]), kConsumerWarps);
+            mbar_init(smem_addr(&ctl->cq_empty[i]), P::kConsumers);
         }
         for (int i = 0; i < 2; ++i)
-            mbar_init(smem_addr(&ctl->list_bar[i]), kConsumerThreads);
+            mbar_init(smem_addr(&ctl->list_bar[i]), P::kConsumerThreads);
         ctl->abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == kProducerWarp && (threadIdx.x & 31) == 0)
+    if (warp == P::kProducerWarp && (threadIdx.x & 31) == 0)
         prefetch_tensormap(&p.tmap);
     // Everything above touched only this CTA's shared memory and the kernel
     // parameters; global memory is read and written only after the previous
@@ -560,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     griddep_wait();
     griddep_launch_dependents();
 
-    build_prefix(p, prefix, ctl, hdr);  // ends with __syncthreads
+    build_prefix<F>(p, prefix, ctl, hdr);  // ends with __syncthreads
 
     if (threadIdx.x == 0)
         ctl->part = Partition::make(prefix[p.batch], gridDim.x, p.split_blocks);
@@ -568,7 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
     const Partition &part = ctl->part;
     if (blockIdx.x == 0) {
         int *g_prefix = reinterpret_cast<int *>(p.ws + prefix_offset());
-        for (int b = threadIdx.x; b <= p.batch; b += kThreads)
+        for (int b = threadIdx.x; b <= p.batch; b += P::kThreads)
             g_prefix[b] = prefix[b];
         if (threadIdx.x == 0) {
             hdr->part = part;
@@ -577,10 +752,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
         }
     }
 
-    if (warp == kProducerWarp)
-        run_producer<KMAX>(p, part, smem, ctl, prefix, hdr);
+    if (warp == P::kProducerWarp)
+        run_producer<KMAX, F>(p, part, smem, ctl, prefix, hdr);
     else
-        run_consumer<KMAX>(p, part, smem, ctl, prefix, hdr, g_slots);
+        run_consumer<KMAX, F>(p, part, smem, ctl, prefix, hdr, g_slots);
 }
 
 // a7: one CTA per (head, request).  The request's chunk lists are staged in
@@ -772,14 +947,14 @@ static int device_sms(int dev)
     return v;
 }
 
-template <int KMAX>
+template <int KMAX, class F>
 static bool ensure_smem_attr(int dev)
 {
     static std::atomic<bool> done[kMaxDevices];
     if (dev >= 0 && dev < kMaxDevices && done[dev].load(std::memory_order_acquire))
         return true;
-    const size_t bytes = SmemLayout<KMAX>::bytes(MSA_MAX_BATCH);
-    if (cudaFuncSetAttribute(score_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t bytes = SmemLayout<KMAX, F>::bytes(MSA_MAX_BATCH);
+    if (cudaFuncSetAttribute(score_kernel<KMAX, F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(bytes)) != cudaSuccess)
         return false;
     if (dev >= 0 && dev < kMaxDevices)
@@ -845,9 +1020,30 @@ static int score_grid(int sms, int batch, int64_t max_blocks, int split_blocks)
     return static_cast<int>(g < 1 ? 1 : g);
 }
 
-template <int KMAX>
-static msa_status launch_score(const void *q, const void *kcache_pool, int64_t num_pages,
-                               const int32_t *block_table, int64_t bt_stride,
+// The pool as a 2-D tensor map: rows = num_pages * 128 tokens, 128 elements
+// per row, 128-byte swizzle.  bf16: 64x128 boxes (two per page); fp8
+// (unsigned bytes): one 128x128 box per page.
+template <class F>
+static bool make_pool_map(CUtensorMap *map, const void *pool, int64_t num_pages)
+{
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc)
+        return false;
+    const cuuint64_t elem = F::kFp8 ? 1 : 2;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim),
+                                static_cast<cuuint64_t>(num_pages) * kPage};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * elem};
+    const cuuint32_t box[2] = {F::kFp8 ? 128u : 64u, static_cast<cuuint32_t>(kPage)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, F::kFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void *>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KMAX, class F>
+static msa_status launch_score(const void *q, const void *kcache_pool, const float *kscale,
+                               int64_t num_pages, const int32_t *block_table, int64_t bt_stride,
                                const int32_t *seq_lens, int batch, int max_model_len, int n_sink,
                                int n_window, float *out_block_scores, void *workspace,
                                int slot_capacity, int grid, int split_blocks, cudaStream_t st,
@@ -855,19 +1051,10 @@ static msa_status launch_score(const void *q, const void *kcache_pool, int64_t n
 {
     ScoreParams p;
     std::memset(&p, 0, sizeof p);
-    EncodeTiledFn enc = encode_tiled();
-    if (!enc)
-        return MSA_ERR_CUDA;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim),
-                                static_cast<cuuint64_t>(num_pages) * kPage};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kPage)};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&p.tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(kcache_pool), dims,
-            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    if (!make_pool_map<F>(&p.tmap, kcache_pool, num_pages))
         return MSA_ERR_CUDA;
     p.q = static_cast<const uint16_t *>(q);
+    p.kscale = kscale;
     p.block_table = block_table;
     p.seq_lens = seq_lens;
     p.out_block_scores = out_block_scores;
@@ -881,12 +1068,12 @@ static msa_status launch_score(const void *q, const void *kcache_pool, int64_t n
     p.n_window = n_window;
     p.split_blocks = split_blocks;
     p.slot_capacity = slot_capacity;
-    if (!ensure_smem_attr<KMAX>(dev))
+    if (!ensure_smem_attr<KMAX, F>(dev))
         return MSA_ERR_CUDA;
-    const size_t smem = SmemLayout<KMAX>::bytes(batch);
+    const size_t smem = SmemLayout<KMAX, F>::bytes(batch);
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(kThreads), smem, st, attr);
-    return cudaLaunchKernelEx(&cfg, score_kernel<KMAX>, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(Pipe<F>::kThreads), smem, st, attr);
+    return cudaLaunchKernelEx(&cfg, score_kernel<KMAX, F>, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 struct Plan {
@@ -921,6 +1108,37 @@ static msa_status plan(int batch, int max_batch, int max_model_len, int k, int s
     return MSA_OK;
 }
 
+template <class F>
+static msa_status score_entry(const void *q, const void *kcache_pool, const float *kscale,
+                              int64_t num_pages, const int32_t *block_table, int64_t bt_stride,
+                              const int32_t *seq_lens, int batch, int max_batch, int max_model_len,
+                              int k, int n_sink, int n_window, float *out_block_scores,
+                              void *workspace, size_t workspace_bytes, int split_blocks,
+                              void *stream)
+{
+    msa_status st = validate(q, kcache_pool, num_pages, block_table, bt_stride, seq_lens, batch,
+                             max_batch, max_model_len, k, n_sink, n_window, workspace, split_blocks);
+    if (st != MSA_OK)
+        return st;
+    if (F::kFp8 && (!kscale || (reinterpret_cast<uintptr_t>(kscale) & 15)))
+        return MSA_ERR_INVALID_ARG;
+    if (batch == 0)
+        return MSA_OK;
+    Plan pl;
+    st = plan(batch, max_batch, max_model_len, k, split_blocks, workspace_bytes, pl);
+    if (st != MSA_OK)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (kmax_for(k) == 16)
+        return launch_score<16, F>(q, kcache_pool, kscale, num_pages, block_table, bt_stride,
+                                   seq_lens, batch, max_model_len, n_sink, n_window,
+                                   out_block_scores, workspace, pl.slot_capacity, pl.grid,
+                                   split_blocks, s, pl.dev);
+    return launch_score<32, F>(q, kcache_pool, kscale, num_pages, block_table, bt_stride, seq_lens,
+                               batch, max_model_len, n_sink, n_window, out_block_scores, workspace,
+                               pl.slot_capacity, pl.grid, split_blocks, s, pl.dev);
+}
+
 }  // namespace msa
 
 using namespace msa;
@@ -935,6 +1153,7 @@ extern "C" size_t msa_indexer_workspace_bytes(int max_batch, int max_model_len, 
            static_cast<size_t>(chunks + max_batch) * slot_bytes(kmax_for(k));
 }
 
+
 extern "C" msa_status msa_indexer_score(const void *q, const void *kcache_pool, int64_t num_pages,
                                         const int32_t *block_table, int64_t bt_stride,
                                         const int32_t *seq_lens, int batch, int max_batch,
@@ -942,22 +1161,22 @@ extern "C" msa_status msa_indexer_score(const void *q, const void *kcache_pool, 
                                         float *out_block_scores, void *workspace,
                                         size_t workspace_bytes, int split_blocks, void *stream)
 {
-    msa_status st = validate(q, kcache_pool, num_pages, block_table, bt_stride, seq_lens, batch,
-                             max_batch, max_model_len, k, n_sink, n_window, workspace, split_blocks);
-    if (st != MSA_OK || batch == 0)
-        return st;
-    Plan pl;
-    st = plan(batch, max_batch, max_model_len, k, split_blocks, workspace_bytes, pl);
-    if (st != MSA_OK)
-        return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (kmax_for(k) == 16)
-        return launch_score<16>(q, kcache_pool, num_pages, block_table, bt_stride, seq_lens, batch,
-                                max_model_len, n_sink, n_window, out_block_scores, workspace,
-                                pl.slot_capacity, pl.grid, split_blocks, s, pl.dev);
-    return launch_score<32>(q, kcache_pool, num_pages, block_table, bt_stride, seq_lens, batch,
-                            max_model_len, n_sink, n_window, out_block_scores, workspace,
-                            pl.slot_capacity, pl.grid, split_blocks, s, pl.dev);
+    return score_entry<Bf16Fmt>(q, kcache_pool, nullptr, num_pages, block_table, bt_stride,
+                                seq_lens, batch, max_batch, max_model_len, k, n_sink, n_window,
+                                out_block_scores, workspace, workspace_bytes, split_blocks, stream);
+}
+
+extern "C" msa_status msa_indexer_score_fp8(const void *q, const void *kcache_fp8,
+                                            const float *kscale, int64_t num_pages,
+                                            const int32_t *block_table, int64_t bt_stride,
+                                            const int32_t *seq_lens, int batch, int max_batch,
+                                            int max_model_len, int k, int n_sink, int n_window,
+                                            float *out_block_scores, void *workspace,
+                                            size_t workspace_bytes, int split_blocks, void *stream)
+{
+    return score_entry<Fp8Fmt>(q, kcache_fp8, kscale, num_pages, block_table, bt_stride, seq_lens,
+                               batch, max_batch, max_model_len, k, n_sink, n_window,
+                               out_block_scores, workspace, workspace_bytes, split_blocks, stream);
 }
 
 extern "C" msa_status msa_indexer_merge(int batch, int k, int32_t *out_ids, float *out_scores,
@@ -1108,6 +1327,27 @@ extern "C" msa_status msa_indexer_expand_pages(const int32_t *ids, int batch, in
         cudaLaunchKernelEx(&cfg, expand_pages_kernel, ids, k, seq_lens, kv_block_table,
                            kv_bt_stride, kPage / page_tokens, page_tokens, out_pages, out_num_pages);
     return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+extern "C" msa_status msa_indexer_decode_fp8(const void *q, const void *kcache_fp8,
+                                             const float *kscale, int64_t num_pages,
+                                             const int32_t *block_table, int64_t bt_stride,
+                                             const int32_t *seq_lens, int batch, int max_batch,
+                                             int max_model_len, int k, int n_sink, int n_window,
+                                             int32_t *out_ids, float *out_scores,
+                                             float *out_block_scores, void *workspace,
+                                             size_t workspace_bytes, int split_blocks,
+                                             void *stream)
+{
+    if (!out_ids || !out_scores)
+        return MSA_ERR_INVALID_ARG;
+    msa_status st = msa_indexer_score_fp8(q, kcache_fp8, kscale, num_pages, block_table, bt_stride,
+                                          seq_lens, batch, max_batch, max_model_len, k, n_sink,
+                                          n_window, out_block_scores, workspace, workspace_bytes,
+                                          split_blocks, stream);
+    if (st != MSA_OK || batch == 0)
+        return st;
+    return msa_indexer_merge(batch, k, out_ids, out_scores, workspace, workspace_bytes, stream);
 }
 
 extern "C" msa_status msa_indexer_get_error(void *workspace, void *stream, uint32_t *flags)

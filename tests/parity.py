@@ -25,9 +25,13 @@ def within(g, o, rtol=RTOL, atol=ATOL):
 
 
 def to_device(w, device="cuda"):
+    """(q, pool, bt, seq) on the device; for an fp8 workload `pool` is (codes, scales)."""
     import torch
     q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).to(device)
-    pool = torch.from_numpy(w.pool.view(np.int16)).view(torch.bfloat16).to(device)
+    if w.pool8 is not None:
+        pool = (torch.from_numpy(w.pool8).to(device), torch.from_numpy(w.kscale).to(device))
+    else:
+        pool = torch.from_numpy(w.pool.view(np.int16)).view(torch.bfloat16).to(device)
     bt = torch.from_numpy(w.block_table).to(device)
     seq = torch.from_numpy(w.seq_lens).to(device)
     return q, pool, bt, seq
@@ -52,9 +56,14 @@ def run_gpu(w, *, k=None, n_sink=None, n_window=None, split_blocks=0, max_batch=
         blk = torch.full((B, 4, w.bt_stride), float("nan"), dtype=torch.float32, device=device)
     if ws is None:
         ws = msa.new_workspace(max_batch, max_model_len, k, split_blocks, device=device)
-    msa.msa_indexer_decode(q, pool, bt, seq, k, n_sink, n_window, ids, sc, ws, max_batch=max_batch,
-                           max_model_len=max_model_len, out_block_scores=blk,
-                           split_blocks=split_blocks)
+    if isinstance(pool, tuple):
+        msa.msa_indexer_decode_fp8(q, pool[0], pool[1], bt, seq, k, n_sink, n_window, ids, sc, ws,
+                                   max_batch=max_batch, max_model_len=max_model_len,
+                                   out_block_scores=blk, split_blocks=split_blocks)
+    else:
+        msa.msa_indexer_decode(q, pool, bt, seq, k, n_sink, n_window, ids, sc, ws,
+                               max_batch=max_batch, max_model_len=max_model_len,
+                               out_block_scores=blk, split_blocks=split_blocks)
     fault = msa.msa_indexer_get_error(ws)
     return (ids.cpu().numpy(), sc.cpu().numpy(),
             None if blk is None else blk.cpu().numpy(), fault)

@@ -65,7 +65,7 @@ def test_clock_sampler_parses_nvidia_smi_rows():
 
 def test_profiled_traffic_requires_a_current_summary(tmp_path, monkeypatch):
     path = tmp_path / "summary.md"
-    monkeypatch.setattr(bench, "PROFILE_SUMMARY", str(path))
+    monkeypatch.setattr(bench, "PROFILE_SUMMARY", {"bf16": str(path)})
     assert bench.profiled_traffic(32) is None
     path.write_text(f"source_sha256_16: {bench.kernel_source_hash()}\n"
                     "dram_bytes_per_launch_full_batch: 1000\n")
