@@ -164,6 +164,35 @@ class Oracle:
             raise ValueError(f"oracle refused the expansion arguments (code {rc})")
         return pages, num
 
+    def run_multi(self, q: np.ndarray, pool: np.ndarray, block_table: np.ndarray,
+                  seq_lens: np.ndarray, k: int, n_sink: int, n_window: int,
+                  pool8: Optional[np.ndarray] = None, kscale: Optional[np.ndarray] = None):
+        """Several query positions per request (speculative-decode verification).
+
+        q is [B, Q, 4, 128]: the last Q tokens of each request.  Position i
+        sees the first seq_len - (Q - 1 - i) tokens: TensorRT-LLM PR #17008,
+        "Description", causal clamp eff_kv = min(q_end + offset_q, kv_len) with
+        offset_q = kv_len - Q.  Each position is then one decode query over
+        its own context, so this is the single-query oracle on B*Q rows.
+        Returns (scores [B,Q,4,stride], ids [B,Q,4,k], sel [B,Q,4,k], lens [B,Q]).
+        """
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        B, Q = q.shape[:2]
+        seq = np.asarray(seq_lens, dtype=np.int64)
+        lens = seq[:, None] - (Q - 1 - np.arange(Q))[None, :]
+        lens = np.maximum(lens, 0).astype(np.int32)
+        rows_q = q.reshape(B * Q, HEADS, DIM)
+        rows_bt = np.repeat(np.ascontiguousarray(block_table, dtype=np.int32), Q, axis=0)
+        rows_len = lens.reshape(B * Q)
+        if pool8 is not None:
+            s = self.block_scores_fp8(rows_q, pool8, kscale, rows_bt, rows_len)
+        else:
+            s = self.block_scores(rows_q, pool, rows_bt, rows_len)
+        ids, sel = self.select(s, rows_len, k, n_sink, n_window)
+        stride = s.shape[2]
+        return (s.reshape(B, Q, HEADS, stride), ids.reshape(B, Q, HEADS, k),
+                sel.reshape(B, Q, HEADS, k), lens)
+
     def run(self, w, k: Optional[int] = None, n_sink: Optional[int] = None,
             n_window: Optional[int] = None):
         """Block scores and selection for a `workloads.Workload` (bf16 or fp8 cache)."""

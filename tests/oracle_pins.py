@@ -320,6 +320,43 @@ def check_fp8_vs_numpy(orc) -> None:
             np.testing.assert_allclose(s[b, :, j], ref, rtol=1e-12, atol=1e-12)
 
 
+# ----------------------------------------------------------------------------
+# several query positions per request
+# ----------------------------------------------------------------------------
+
+def check_multi_query_golden(orc) -> None:
+    with open(os.path.join(GOLDEN_DIR, "multi_query_causal.json")) as f:
+        fx = json.load(f)
+    L, Q = int(fx["seq_len"]), int(fx["q_len"])
+    pool = np.zeros((2, PAGE, DIM), dtype=np.float32)
+    for tok, v in fx["planted_dim0"].items():
+        t = int(tok)
+        pool[t // PAGE, t % PAGE, 0] = v
+    q = np.zeros((1, Q, HEADS, DIM), dtype=np.float32)
+    q[0, :, :, 0] = np.asarray(fx["alpha"], dtype=np.float32)[None, :]
+    s, ids, sel, lens = orc.run_multi(wl.f32_to_bf16_bits(q), wl.f32_to_bf16_bits(pool),
+                                      np.array([[0, 1]], dtype=np.int32),
+                                      np.array([L], dtype=np.int32), int(fx["k"]),
+                                      int(fx["n_sink"]), int(fx["n_window"]))
+    assert list(lens[0]) == [127, 128, 129, 130]
+    np.testing.assert_array_equal(ids, np.asarray(fx["expected_ids"], dtype=np.int32))
+    for i in range(Q):
+        for h in range(HEADS):
+            row = fx["expected_scores"][0][i][h]
+            exp = np.full(int(fx["k"]), -np.inf)
+            exp[:len(row)] = row
+            np.testing.assert_array_equal(sel[0, i, h], exp, err_msg=f"position {i} head {h}")
+
+
+def check_multi_query_one_position_is_decode(orc) -> None:
+    w = mixed_workload(14)
+    s1, ids1, sel1 = orc.run(w)
+    s, ids, sel, _ = orc.run_multi(w.q[:, None], w.pool, w.block_table, w.seq_lens, w.k,
+                                   w.n_sink, w.n_window)
+    np.testing.assert_array_equal(ids[:, 0], ids1)
+    np.testing.assert_array_equal(s[:, 0], s1)
+
+
 ALL_CHECKS = (check_golden, check_scores_vs_numpy, check_select_vs_rank_count, check_invariants,
               check_expand_golden, check_expand_invariants, check_e4m3_codes, check_fp8_golden,
-              check_fp8_vs_numpy)
+              check_fp8_vs_numpy, check_multi_query_golden, check_multi_query_one_position_is_decode)

@@ -90,3 +90,11 @@ def test_fp8_golden(orc):
 
 def test_fp8_scores_match_numpy(orc):
     pins.check_fp8_vs_numpy(orc)
+
+
+def test_multi_query_golden(orc):
+    pins.check_multi_query_golden(orc)
+
+
+def test_multi_query_single_position_is_decode(orc):
+    pins.check_multi_query_one_position_is_decode(orc)
