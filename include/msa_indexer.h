@@ -189,6 +189,35 @@ msa_status msa_indexer_decode_fp8(const void *q, const void *kcache_fp8, const f
                                   void *stream);
 
 /*
+ * Several query positions per request: speculative-decode verification runs
+ * the indexer for the last q_len tokens at once (vLLM PR #57832, "Test
+ * Plan": query_len 1/4; vLLM blog "Following the Bottleneck", section 2: one
+ * workgroup per request processes all draft positions together, reusing the
+ * key loads).  Position i (0-based) sees the first seq_len - (q_len - 1 - i)
+ * tokens (TensorRT-LLM PR #17008, "Description": the causal clamp
+ * eff_kv = min(q_end + offset_q, kv_len)); pins and the top-k are per
+ * position and head.  Each index-K page is read once for all q_len x 4
+ * (position, head) columns.
+ *
+ *   q          bf16 [batch, q_len, 4, 128], q_len in {1, 2, 4}.
+ *   out_ids    int32 [batch, q_len, 4, k]; out_scores fp32 [batch, q_len, 4, k];
+ *   out_block_scores  optional fp32 [batch, q_len, 4, bt_stride].
+ *   workspace  >= msa_indexer_workspace_bytes_mq(..., q_len) bytes.
+ *
+ * Other arguments as for msa_indexer_decode (bf16 cache).
+ */
+size_t msa_indexer_workspace_bytes_mq(int max_batch, int max_model_len, int k, int split_blocks,
+                                      int q_len);
+
+msa_status msa_indexer_decode_mq(const void *q, int q_len, const void *kcache_pool,
+                                 int64_t num_pages, const int32_t *block_table, int64_t bt_stride,
+                                 const int32_t *seq_lens, int batch, int max_batch,
+                                 int max_model_len, int k, int n_sink, int n_window,
+                                 int32_t *out_ids, float *out_scores, float *out_block_scores,
+                                 void *workspace, size_t workspace_bytes, int split_blocks,
+                                 void *stream);
+
+/*
  * The second stage alone: merges the per-unit top-k lists that the last
  * msa_indexer_score() on this workspace left, per (request, head), into the
  * exact top-k (vLLM PR #57832, "Solution", step 4: merge per head) and

@@ -28,6 +28,8 @@ from ._binding import (  # noqa: F401
     msa_indexer_decode,
     msa_indexer_decode_noalloc,
     msa_indexer_decode_fp8,
+    msa_indexer_decode_mq,
+    msa_indexer_workspace_bytes_mq,
     msa_indexer_score_fp8,
     msa_indexer_expand_pages,
     msa_indexer_get_error,

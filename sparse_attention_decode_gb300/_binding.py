@@ -43,6 +43,8 @@ EXPORTED = (
     "msa_indexer_expand_pages",
     "msa_indexer_score_fp8",
     "msa_indexer_decode_fp8",
+    "msa_indexer_decode_mq",
+    "msa_indexer_workspace_bytes_mq",
 )
 
 _lib = None
@@ -90,6 +92,10 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.msa_indexer_decode_fp8.restype = c_int
     lib.msa_indexer_score_fp8.argtypes = common8 + [P, P, c_size, c_int, P]
     lib.msa_indexer_score_fp8.restype = c_int
+    lib.msa_indexer_workspace_bytes_mq.argtypes = [c_int, c_int, c_int, c_int, c_int]
+    lib.msa_indexer_workspace_bytes_mq.restype = c_size
+    lib.msa_indexer_decode_mq.argtypes = [P, c_int] + common[1:] + [P, P, P, P, c_size, c_int, P]
+    lib.msa_indexer_decode_mq.restype = c_int
     lib.msa_status_string.argtypes = [c_int]
     lib.msa_status_string.restype = ctypes.c_char_p
     if path is None:
@@ -242,6 +248,33 @@ def msa_indexer_expand_pages(ids, seq_lens, kv_block_table, out_pages, out_num_p
     _check(st, "msa_indexer_expand_pages")
 
 
+def msa_indexer_workspace_bytes_mq(max_batch: int, max_model_len: int, k: int,
+                                   split_blocks: int = 0, q_len: int = 1) -> int:
+    return int(load().msa_indexer_workspace_bytes_mq(max_batch, max_model_len, k, split_blocks,
+                                                     q_len))
+
+
+def msa_indexer_decode_mq(q, kcache_pool, block_table, seq_lens, k: int, n_sink: int,
+                          n_window: int, out_ids, out_scores, workspace, *,
+                          max_batch: Optional[int] = None, max_model_len: int,
+                          out_block_scores=None, split_blocks: int = 0, stream=None) -> None:
+    """msa_indexer_decode_mq(): q is bf16 [B, q_len, 4, 128] (the last q_len tokens)."""
+    import torch
+    assert q.dtype == torch.bfloat16 and q.is_contiguous() and q.dim() == 4
+    assert tuple(q.shape[2:]) == (MSA_NUM_HEADS, MSA_HEAD_DIM)
+    assert kcache_pool.dtype == torch.bfloat16 and kcache_pool.is_contiguous()
+    assert block_table.dtype == torch.int32 and block_table.stride(1) == 1
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+    B, q_len = int(q.shape[0]), int(q.shape[1])
+    st = load().msa_indexer_decode_mq(
+        _ptr(q), q_len, _ptr(kcache_pool), int(kcache_pool.shape[0]), _ptr(block_table),
+        int(block_table.stride(0)), _ptr(seq_lens), B, B if max_batch is None else max_batch,
+        max_model_len, k, n_sink, n_window, _ptr(out_ids), _ptr(out_scores),
+        _ptr(out_block_scores), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+        split_blocks, _stream_ptr(stream))
+    _check(st, "msa_indexer_decode_mq")
+
+
 def msa_indexer_get_error(workspace, *, stream=None) -> int:
     flags = ctypes.c_uint32(0)
     st = load().msa_indexer_get_error(_ptr(workspace), _stream_ptr(stream), ctypes.byref(flags))
@@ -250,10 +283,10 @@ def msa_indexer_get_error(workspace, *, stream=None) -> int:
 
 
 def new_workspace(max_batch: int, max_model_len: int, k: int, split_blocks: int = 0,
-                  device=None):
-    """A zero-filled uint8 CUDA tensor of msa_indexer_workspace_bytes() bytes."""
+                  device=None, q_len: int = 1):
+    """A zero-filled uint8 CUDA tensor of msa_indexer_workspace_bytes_mq() bytes."""
     import torch
-    n = msa_indexer_workspace_bytes(max_batch, max_model_len, k, split_blocks)
+    n = msa_indexer_workspace_bytes_mq(max_batch, max_model_len, k, split_blocks, q_len)
     if n == 0:
         raise MsaError(MSA_ERR_UNSUPPORTED, "msa_indexer_workspace_bytes")
     return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")

@@ -84,6 +84,14 @@ struct Pipe {
     __host__ __device__ static constexpr uint32_t use_of(uint32_t it) { return it / kStages; }
 };
 
+// Query columns of one request: NQ positions x 4 heads (column c = 4 * position
+// + head), scored as the n dimension of m16n8k16 in kFrags fragments of 8.
+template <int NQ>
+struct Cols {
+    static constexpr int kCols = 4 * NQ;
+    static constexpr int kFrags = (kCols + 7) / 8;
+};
+
 struct ScoreParams {
     CUtensorMap tmap;  // pool as [num_pages*128 rows][128 elements] (format-specific boxes)
     const uint16_t *q;
@@ -119,13 +127,13 @@ struct SmemCtl {
     Partition part;  // this pass's chunking, the same in every CTA
 };
 
-template <int KMAX, class F>
+template <int KMAX, class F, int NQ = 1>
 struct SmemLayout {
     static constexpr size_t stages = 0;  // kStages x kDataBytes, 1024-aligned
     static constexpr size_t scales = stages + static_cast<size_t>(Pipe<F>::kStages) * F::kDataBytes;
     static constexpr size_t ctl = round_up(scales + static_cast<size_t>(Pipe<F>::kStages) * F::kScaleBytes, 16);
     static constexpr size_t lists = round_up(ctl + sizeof(SmemCtl<F>), 16);
-    static constexpr size_t list_entries = 2 * F::kConsumers * kHeads * KMAX;
+    static constexpr size_t list_entries = 2 * F::kConsumers * Cols<NQ>::kCols * KMAX;
     static constexpr size_t prefix = lists + list_entries * sizeof(uint64_t);
     static __host__ __device__ size_t bytes(int batch)
     {
@@ -197,27 +205,37 @@ __device__ void build_prefix(const ScoreParams &p, int *prefix, SmemCtl<F> *ctl,
     __syncthreads();
 }
 
-// a3 + a4: the four heads' block scores of one resident page.  The page sits
-// in two 16 KiB halves (dims 0-63, 64-127), each 128 rows of 128 bytes with
-// the TMA 128-byte swizzle (16-byte chunk index XOR row % 8).  A = 16 tokens
-// x 16 dims via ldmatrix; B = q (16 dims x 8 columns: heads 0-3, 4-7 zero).
-// C row = token, column = head.  Returns m0/m1 = max over valid tokens of
-// heads 2t and 2t+1 (t = lane % 4), reduced over the warp.
-__device__ __forceinline__ void score_page(uint32_t stage, const uint32_t (&bq)[8][2], int valid,
-                                           uint32_t lane_off, const uint32_t (&xo)[4], int lane,
-                                           float &m0, float &m1)
+// a3 + a4: the block scores of one resident page for every query column.
+// The page sits in two 16 KiB halves (dims 0-63, 64-127), each 128 rows of
+// 128 bytes with the TMA 128-byte swizzle (16-byte chunk index XOR row % 8).
+// A = 16 tokens x 16 dims via ldmatrix; B = q (16 dims x 8 columns per
+// fragment; with one position the columns are heads 0-3 and four zero
+// columns).  C row = token, column = query column.  vrows[f] = valid token
+// rows of this lane's columns in fragment f (positions see different
+// lengths).  Returns m[f][0..1] = max over valid rows of columns 8f + 2t and
+// 8f + 2t + 1 (t = lane % 4), reduced over the warp.
+template <int NQ>
+__device__ __forceinline__ void score_page(uint32_t stage,
+                                           const uint32_t (&bq)[Cols<NQ>::kFrags][8][2],
+                                           const int (&vrows)[Cols<NQ>::kFrags], uint32_t lane_off,
+                                           const uint32_t (&xo)[4], int lane,
+                                           float (&m)[Cols<NQ>::kFrags][2])
 {
+    constexpr int NF = Cols<NQ>::kFrags;
     const float neg_inf = -__int_as_float(0x7f800000);
-    m0 = neg_inf;
-    m1 = neg_inf;
+#pragma unroll
+    for (int f = 0; f < NF; ++f)
+        m[f][0] = m[f][1] = neg_inf;
 #pragma unroll
     for (int mt0 = 0; mt0 < 8; mt0 += 4) {
-        float acc[4][4];
+        float acc[4][NF][4];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                acc[u][e] = 0.0f;
+            for (int f = 0; f < NF; ++f)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    acc[u][f][e] = 0.0f;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
@@ -225,23 +243,31 @@ __device__ __forceinline__ void score_page(uint32_t stage, const uint32_t (&bq)[
                 uint32_t a[4];
                 ldsm_x4(a, stage + (ks >> 2) * kHalfPageBytes + (mt0 + u) * 16 * 128 + lane_off +
                                xo[ks & 3]);
-                mma_bf16_16816(acc[u], a, bq[ks][0], bq[ks][1]);
+#pragma unroll
+                for (int f = 0; f < NF; ++f)
+                    mma_bf16_16816(acc[u][f], a, bq[f][ks][0], bq[f][ks][1]);
             }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int row = (mt0 + u) * 16 + (lane >> 2);
-            const bool v0 = row < valid, v1 = row + 8 < valid;
-            m0 = fmaxf(m0, v0 ? acc[u][0] : neg_inf);
-            m1 = fmaxf(m1, v0 ? acc[u][1] : neg_inf);
-            m0 = fmaxf(m0, v1 ? acc[u][2] : neg_inf);
-            m1 = fmaxf(m1, v1 ? acc[u][3] : neg_inf);
+#pragma unroll
+            for (int f = 0; f < NF; ++f) {
+                const bool v0 = row < vrows[f], v1 = row + 8 < vrows[f];
+                m[f][0] = fmaxf(m[f][0], v0 ? acc[u][f][0] : neg_inf);
+                m[f][1] = fmaxf(m[f][1], v0 ? acc[u][f][1] : neg_inf);
+                m[f][0] = fmaxf(m[f][0], v1 ? acc[u][f][2] : neg_inf);
+                m[f][1] = fmaxf(m[f][1], v1 ? acc[u][f][3] : neg_inf);
+            }
         }
     }
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
-        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+#pragma unroll
+        for (int f = 0; f < NF; ++f) {
+            m[f][0] = fmaxf(m[f][0], __shfl_xor_sync(0xffffffffu, m[f][0], o));
+            m[f][1] = fmaxf(m[f][1], __shfl_xor_sync(0xffffffffu, m[f][1], o));
+        }
     }
 }
 
@@ -327,26 +353,35 @@ __device__ __forceinline__ void score_page_fp8(uint32_t stage, const float *scl,
     }
 }
 
-// The query fragment of request b for the page scorer of format F.
-// bf16: the B fragment of m16n8k16 (heads in columns 0-3, 4-7 zero).
-// fp8: f16 pairs in the byte-to-column map of score_page_fp8, scaled by 2^e
-// per head so the largest |q| lands in [2^13, 2^14); inv_lo / inv_hi receive
-// 2^-e of heads 2t and 2t+1 (t = lane % 4).
-template <class F>
+// The query fragments of request b for the page scorer of format F.
+// bf16: the B fragments of m16n8k16: column c = 8f + g of fragment f is q row
+// b * kCols + c (position c / 4, head c % 4); columns past kCols are zero.
+// fp8 (one position): f16 pairs in the byte-to-column map of score_page_fp8,
+// scaled by 2^e per head so the largest |q| lands in [2^13, 2^14); inv_lo /
+// inv_hi receive 2^-e of heads 2t and 2t+1 (t = lane % 4).
+template <class F, int NQ>
 __device__ __forceinline__ void load_query(const ScoreParams &p, int b, int lane,
-                                           uint32_t (&bq)[8][2], float &inv_lo, float &inv_hi)
+                                           uint32_t (&bq)[Cols<NQ>::kFrags][8][2], float &inv_lo,
+                                           float &inv_hi)
 {
+    constexpr int NC = Cols<NQ>::kCols;
     const int g = lane >> 2, t = lane & 3;
-    const uint16_t *qrow = p.q + (static_cast<size_t>(b) * kHeads + (g & 3)) * kDim;
     if constexpr (!F::kFp8) {
-        const uint32_t *qw = reinterpret_cast<const uint32_t *>(qrow);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            bq[ks][0] = g < kHeads ? __ldg(qw + 8 * ks + t) : 0u;
-            bq[ks][1] = g < kHeads ? __ldg(qw + 8 * ks + 4 + t) : 0u;
+        for (int f = 0; f < Cols<NQ>::kFrags; ++f) {
+            const int c = 8 * f + g;
+            const uint32_t *qw = reinterpret_cast<const uint32_t *>(
+                p.q + (static_cast<size_t>(b) * NC + (c < NC ? c : 0)) * kDim);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                bq[f][ks][0] = c < NC ? __ldg(qw + 8 * ks + t) : 0u;
+                bq[f][ks][1] = c < NC ? __ldg(qw + 8 * ks + 4 + t) : 0u;
+            }
         }
         inv_lo = inv_hi = 1.0f;
     } else {
+        static_assert(NQ == 1, "the fp8 path scores one position");
+        const uint16_t *qrow = p.q + (static_cast<size_t>(b) * kHeads + (g & 3)) * kDim;
         const uint2 *q8 = reinterpret_cast<const uint2 *>(qrow);  // 4 bf16 per load
         float v[8][4];
         float amax = 0.0f;
@@ -370,25 +405,29 @@ __device__ __forceinline__ void load_query(const ScoreParams &p, int b, int lane
         const float up = __int_as_float((127 + sh) << 23), down = __int_as_float((127 - sh) << 23);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            bq[ks][0] = f32x2_to_f16x2(v[ks][0] * up, v[ks][1] * up);
-            bq[ks][1] = f32x2_to_f16x2(v[ks][2] * up, v[ks][3] * up);
+            bq[0][ks][0] = f32x2_to_f16x2(v[ks][0] * up, v[ks][1] * up);
+            bq[0][ks][1] = f32x2_to_f16x2(v[ks][2] * up, v[ks][3] * up);
         }
         inv_lo = __shfl_sync(0xffffffffu, down, (8 * t) & 31);
         inv_hi = __shfl_sync(0xffffffffu, down, (8 * t + 4) & 31);
     }
 }
 
-template <int KMAX, class F>
+template <int KMAX, class F, int NQ>
 __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_t *smem,
                              SmemCtl<F> *ctl, const int *prefix, WorkspaceHeader *hdr,
                              uint64_t *g_slots)
 {
     using P = Pipe<F>;
+    using CL = SmemLayout<KMAX, F, NQ>;
     constexpr int C = P::kConsumers;
-    constexpr int NR = KMAX / 8;  // list registers per lane: 4 heads x KMAX / 32 lanes
+    constexpr int NC = Cols<NQ>::kCols;    // query columns: NQ positions x 4 heads
+    constexpr int NF = Cols<NQ>::kFrags;   // n8 fragments
+    constexpr int NR = NC * KMAX / 32;     // list registers per lane
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int t = lane & 3;
     const float neg_inf = -__int_as_float(0x7f800000);
-    uint64_t *listbuf = reinterpret_cast<uint64_t *>(smem + SmemLayout<KMAX, F>::lists);
+    uint64_t *listbuf = reinterpret_cast<uint64_t *>(smem + CL::lists);
 
     // ldmatrix lane geometry (bf16): matrix mi = lane / 8 (rows +8 for odd,
     // dims +8 for mi >= 2), row-in-matrix r = lane % 8.
@@ -398,10 +437,15 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4)
         xo[c4] = static_cast<uint32_t>((((c4 * 2 + (mi >> 1)) ^ rr) & 7) << 4);
+    // position of this lane's columns 8f + 2t, 8f + 2t + 1 (clamped for padding columns)
+    int lane_pos[NF];
+#pragma unroll
+    for (int f = 0; f < NF; ++f)
+        lane_pos[f] = min((8 * f + 2 * t) >> 2, NQ - 1);
 
-    const uint32_t stage0 = smem_addr(smem + SmemLayout<KMAX, F>::stages);
-    const float *scales = reinterpret_cast<const float *>(smem + SmemLayout<KMAX, F>::scales);
-    uint32_t bq[8][2];
+    const uint32_t stage0 = smem_addr(smem + CL::stages);
+    const float *scales = reinterpret_cast<const float *>(smem + CL::scales);
+    uint32_t bq[NF][8][2];
     float inv_lo = 1.0f, inv_hi = 1.0f;
     int q_row = -1;
     uint32_t it = 0;       // pages of this CTA so far (same count as the producer's)
@@ -424,8 +468,15 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
         while (pg < p1) {
             const int b = find_row(prefix, p.batch, pg);
             const int row_first = prefix[b], row_end = prefix[b + 1];
-            const int nb = row_end - row_first;
             const int seg_end = min(p1, row_end);
+            // position i sees the first seq_len - (NQ - 1 - i) tokens
+            const int seq_len = p.seq_lens[b];
+            int nb_pos[NQ];
+#pragma unroll
+            for (int i = 0; i < NQ; ++i) {
+                const int len = seq_len - (NQ - 1 - i);
+                nb_pos[i] = len > 0 ? (len + kPage - 1) / kPage : 0;
+            }
             uint64_t lst[NR];
 #pragma unroll
             for (int r = 0; r < NR; ++r)
@@ -438,53 +489,61 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
                 const int j = x - row_first;
 
                 if (b != q_row) {  // issue the query loads before waiting on the page
-                    load_query<F>(p, b, lane, bq, inv_lo, inv_hi);
+                    load_query<F, NQ>(p, b, lane, bq, inv_lo, inv_hi);
                     q_row = b;
                 }
 
                 const bool ready = warp_wait(ctl, hdr, smem_addr(&ctl->full[s]), P::use_of(my) & 1u);
                 const int2 meta = ctl->meta[s];
-                float sc[4] = {neg_inf, neg_inf, neg_inf, neg_inf};
+                float sc[NC];
+#pragma unroll
+                for (int cc = 0; cc < NC; ++cc)
+                    sc[cc] = neg_inf;
                 const bool ok = ready && meta.y != 0;
                 if (ok) {
-                    float m0, m1;
+                    float m[NF][2];
                     if constexpr (F::kFp8) {
-                        score_page_fp8(stage0 + s * F::kDataBytes, scales + s * kPage, bq, meta.x,
-                                       lane, m0, m1);
-                        m0 *= inv_lo;
-                        m1 *= inv_hi;
+                        score_page_fp8(stage0 + s * F::kDataBytes, scales + s * kPage, bq[0], meta.x,
+                                       lane, m[0][0], m[0][1]);
+                        m[0][0] *= inv_lo;
+                        m[0][1] *= inv_hi;
                     } else {
-                        score_page(stage0 + s * F::kDataBytes, bq, meta.x, lane_off, xo, lane, m0, m1);
+                        const int rem = seq_len - j * kPage;  // tokens of the last position in this block on
+                        int vrows[NF];
+#pragma unroll
+                        for (int f = 0; f < NF; ++f)
+                            vrows[f] = min(kPage, rem - (NQ - 1 - lane_pos[f]));
+                        score_page<NQ>(stage0 + s * F::kDataBytes, bq, vrows, lane_off, xo, lane, m);
                     }
-                    sc[0] = __shfl_sync(0xffffffffu, m0, 0);
-                    sc[1] = __shfl_sync(0xffffffffu, m1, 0);
-                    sc[2] = __shfl_sync(0xffffffffu, m0, 1);
-                    sc[3] = __shfl_sync(0xffffffffu, m1, 1);
+#pragma unroll
+                    for (int cc = 0; cc < NC; ++cc)
+                        sc[cc] = __shfl_sync(0xffffffffu, m[cc >> 3][cc & 1], (cc & 7) >> 1);
                 }
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&ctl->empty[s]));
 
-                if (p.out_block_scores != nullptr && lane < kHeads) {
+                if (p.out_block_scores != nullptr && lane < NC) {
                     float v = sc[0];
-                    v = lane == 1 ? sc[1] : v;
-                    v = lane == 2 ? sc[2] : v;
-                    v = lane == 3 ? sc[3] : v;
-                    p.out_block_scores[(static_cast<size_t>(b) * kHeads + lane) * p.bt_stride + j] = v;
+#pragma unroll
+                    for (int cc = 1; cc < NC; ++cc)
+                        v = lane == cc ? sc[cc] : v;
+                    p.out_block_scores[(static_cast<size_t>(b) * NC + lane) * p.bt_stride + j] = v;
                 }
 
-                const bool pinned = j < p.n_sink || j >= nb - p.n_window;
-                uint64_t key[4];
+                uint64_t key[NC];
 #pragma unroll
-                for (int h = 0; h < kHeads; ++h)
-                    key[h] = ok ? pack_key(sc[h], j, pinned) : 0ull;
-                if constexpr (KMAX == 16) {
-                    lst[0] = insert_desc<16>(lst[0], lane < 16 ? key[0] : key[1], lane);
-                    lst[1] = insert_desc<16>(lst[1], lane < 16 ? key[2] : key[3], lane);
-                } else {
+                for (int cc = 0; cc < NC; ++cc) {
+                    const int nbp = nb_pos[cc >> 2];
+                    const bool pinned = j < p.n_sink || j >= nbp - p.n_window;
+                    key[cc] = (ok && j < nbp) ? pack_key(sc[cc], j, pinned) : 0ull;
+                }
 #pragma unroll
-                    for (int h = 0; h < kHeads; ++h)
-                        lst[h] = insert_desc<32>(lst[h], key[h], lane);
+                for (int r = 0; r < NR; ++r) {
+                    if constexpr (KMAX == 16)
+                        lst[r] = insert_desc<16>(lst[r], lane < 16 ? key[2 * r] : key[2 * r + 1], lane);
+                    else
+                        lst[r] = insert_desc<32>(lst[r], key[r], lane);
                 }
             }
             it += static_cast<uint32_t>(seg_end - pg);
@@ -496,11 +555,11 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
             // passed the next segment's barrier (and so has finished reading
             // this one).
             const int buf = static_cast<int>(segments & 1u);
-            uint64_t *lb = listbuf + static_cast<size_t>(buf) * C * kHeads * KMAX;
+            uint64_t *lb = listbuf + static_cast<size_t>(buf) * C * NC * KMAX;
 #pragma unroll
             for (int r = 0; r < NR; ++r) {
-                const int head = r * (32 / KMAX) + lane / KMAX;
-                lb[(w * kHeads + head) * KMAX + lane % KMAX] = lst[r];
+                const int col = r * (32 / KMAX) + lane / KMAX;
+                lb[(w * NC + col) * KMAX + lane % KMAX] = lst[r];
             }
             mbar_arrive(smem_addr(&ctl->list_bar[buf]));  // every consumer thread
             const bool lists_ready =
@@ -514,33 +573,45 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
                     atomicOr(&hdr->fault, MSA_FAULT_SLOTS);
                 continue;
             }
-            auto L = [&](int src, int h, int rank) { return lb[(src * kHeads + h) * KMAX + rank]; };
-            auto store = [&](int h, int rank, uint64_t v) {
-                g_slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + rank] = v;
+            auto L = [&](int src, int col, int rank) { return lb[(src * NC + col) * KMAX + rank]; };
+            auto store = [&](int col, int rank, uint64_t v) {
+                g_slots[(static_cast<size_t>(slot) * NC + col) * KMAX + rank] = v;
             };
+            constexpr int kPerWarp = NC / C;  // columns each warp merges
             if constexpr (C == 2 && KMAX == 16) {
-                // lanes 0-15: head 2w, lanes 16-31: head 2w+1
-                const int h = 2 * w + (lane >> 4), r = lane & 15;
-                store(h, r, merge_top<16>(L(0, h, r), L(1, h, 15 - r), lane));
+                // two columns per pass: lanes 0-15 and 16-31
+#pragma unroll
+                for (int pp = 0; pp < kPerWarp / 2; ++pp) {
+                    const int col = w * kPerWarp + 2 * pp + (lane >> 4), r = lane & 15;
+                    store(col, r, merge_top<16>(L(0, col, r), L(1, col, 15 - r), lane));
+                }
             } else if constexpr (C == 2) {
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int h = 2 * w + hh;
-                    store(h, lane, merge_top<32>(L(0, h, lane), L(1, h, 31 - lane), lane));
+                for (int pp = 0; pp < kPerWarp; ++pp) {
+                    const int col = w * kPerWarp + pp;
+                    store(col, lane, merge_top<32>(L(0, col, lane), L(1, col, 31 - lane), lane));
                 }
             } else if constexpr (C == 4 && KMAX == 16) {
-                // head w: lanes 0-15 merge lists 0,1, lanes 16-31 lists 2,3, then the halves
-                const int half = lane >> 4, r = lane & 15;
-                uint64_t v = merge_top<16>(L(2 * half, w, r), L(2 * half + 1, w, 15 - r), lane);
-                v = merge_top<16>(v, __shfl_sync(0xffffffffu, v, 31 - lane), lane);
-                if (lane < 16)
-                    store(w, r, v);
+                // per column: lanes 0-15 merge lists 0,1, lanes 16-31 lists 2,3, then the halves
+#pragma unroll
+                for (int pp = 0; pp < kPerWarp; ++pp) {
+                    const int col = w * kPerWarp + pp;
+                    const int half = lane >> 4, r = lane & 15;
+                    uint64_t v = merge_top<16>(L(2 * half, col, r), L(2 * half + 1, col, 15 - r), lane);
+                    v = merge_top<16>(v, __shfl_sync(0xffffffffu, v, 31 - lane), lane);
+                    if (lane < 16)
+                        store(col, r, v);
+                }
             } else {
                 static_assert(C == 4, "two or four consumer warps");
-                uint64_t v = merge_top<32>(L(0, w, lane), L(1, w, 31 - lane), lane);
-                const uint64_t u = merge_top<32>(L(2, w, lane), L(3, w, 31 - lane), lane);
-                v = merge_top<32>(v, __shfl_sync(0xffffffffu, u, 31 - lane), lane);
-                store(w, lane, v);
+#pragma unroll
+                for (int pp = 0; pp < kPerWarp; ++pp) {
+                    const int col = w * kPerWarp + pp;
+                    uint64_t v = merge_top<32>(L(0, col, lane), L(1, col, 31 - lane), lane);
+                    const uint64_t u = merge_top<32>(L(2, col, lane), L(3, col, 31 - lane), lane);
+                    v = merge_top<32>(v, __shfl_sync(0xffffffffu, u, 31 - lane), lane);
+                    store(col, lane, v);
+                }
             }
         }
     }
@@ -587,14 +658,14 @@ __device__ __forceinline__ int resolve_ticket(const Partition &part, WorkspaceHe
     return c;
 }
 
-template <int KMAX, class F>
+template <int KMAX, class F, int NQ>
 __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_t *smem,
                              SmemCtl<F> *ctl, const int *prefix, WorkspaceHeader *hdr)
 {
     using P = Pipe<F>;
     const int lane = threadIdx.x & 31;
-    const uint32_t stage0 = smem_addr(smem + SmemLayout<KMAX, F>::stages);
-    const uint32_t scale0 = smem_addr(smem + SmemLayout<KMAX, F>::scales);
+    const uint32_t stage0 = smem_addr(smem + SmemLayout<KMAX, F, NQ>::stages);
+    const uint32_t scale0 = smem_addr(smem + SmemLayout<KMAX, F, NQ>::scales);
     uint32_t it = 0;  // pages issued
     uint32_t n = 0;   // chunk ids posted
     const uint64_t stream_policy = l2_evict_first_policy();  // K is read once per pass
@@ -699,7 +770,7 @@ __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_
     }
 }
 
-template <int KMAX, class F>
+template <int KMAX, class F, int NQ>
 __global__ void __launch_bounds__(Pipe<F>::kThreads, 1)
     score_kernel(const __grid_constant__ ScoreParams p)
 {
@@ -707,8 +778,8 @@ __global__ void __launch_bounds__(Pipe<F>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
-    SmemCtl<F> *ctl = reinterpret_cast<SmemCtl<F> *>(smem + SmemLayout<KMAX, F>::ctl);
-    int *prefix = reinterpret_cast<int *>(smem + SmemLayout<KMAX, F>::prefix);
+    SmemCtl<F> *ctl = reinterpret_cast<SmemCtl<F> *>(smem + SmemLayout<KMAX, F, NQ>::ctl);
+    int *prefix = reinterpret_cast<int *>(smem + SmemLayout<KMAX, F, NQ>::prefix);
     WorkspaceHeader *hdr = reinterpret_cast<WorkspaceHeader *>(p.ws);
     uint64_t *g_slots = reinterpret_cast<uint64_t *>(p.ws + slots_offset(p.batch));
     const int warp = threadIdx.x >> 5;
@@ -753,12 +824,12 @@ __global__ void __launch_bounds__(Pipe<F>::kThreads, 1)
     }
 
     if (warp == P::kProducerWarp)
-        run_producer<KMAX, F>(p, part, smem, ctl, prefix, hdr);
+        run_producer<KMAX, F, NQ>(p, part, smem, ctl, prefix, hdr);
     else
-        run_consumer<KMAX, F>(p, part, smem, ctl, prefix, hdr, g_slots);
+        run_consumer<KMAX, F, NQ>(p, part, smem, ctl, prefix, hdr, g_slots);
 }
 
-// a7: one CTA per (head, request).  The request's chunk lists are staged in
+// a7: one CTA per (query column, request): column = 4 * position + head.  The request's chunk lists are staged in
 // shared memory a tile at a time (all loads in flight together), each group of
 // KMAX lanes folds every kGroups-th list of the tile into a running top-KMAX,
 // and a tree over the groups yields the request's top-KMAX for the head.
@@ -767,8 +838,8 @@ constexpr int kMergeTileKeys = 2048;  // 16 KiB of keys staged per pass
 
 template <int KMAX>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const uint8_t *ws, int batch, int k,
-                                                              int slot_capacity, int32_t *out_ids,
-                                                              float *out_scores)
+                                                              int cols, int slot_capacity,
+                                                              int32_t *out_ids, float *out_scores)
 {
     constexpr int kGroups = kMergeThreads / KMAX;
     constexpr int kTileLists = kMergeTileKeys / KMAX;
@@ -799,7 +870,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const uint8_t *ws,
             const int li = e / KMAX, r = e % KMAX;
             const int slot = c_first + t0 + li + b;
             tile[e] = slot < slot_capacity
-                          ? slots[(static_cast<size_t>(slot) * kHeads + h) * KMAX + r]
+                          ? slots[(static_cast<size_t>(slot) * cols + h) * KMAX + r]
                           : 0ull;
         }
         __syncthreads();
@@ -828,7 +899,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const uint8_t *ws,
         int id;
         float score;
         unpack_key(run, id, score);
-        const size_t o = (static_cast<size_t>(b) * kHeads + h) * k + rank;
+        const size_t o = (static_cast<size_t>(b) * cols + h) * k + rank;
         out_ids[o] = id;
         out_scores[o] = score;
     }
@@ -947,14 +1018,14 @@ static int device_sms(int dev)
     return v;
 }
 
-template <int KMAX, class F>
+template <int KMAX, class F, int NQ>
 static bool ensure_smem_attr(int dev)
 {
     static std::atomic<bool> done[kMaxDevices];
     if (dev >= 0 && dev < kMaxDevices && done[dev].load(std::memory_order_acquire))
         return true;
-    const size_t bytes = SmemLayout<KMAX, F>::bytes(MSA_MAX_BATCH);
-    if (cudaFuncSetAttribute(score_kernel<KMAX, F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t bytes = SmemLayout<KMAX, F, NQ>::bytes(MSA_MAX_BATCH);
+    if (cudaFuncSetAttribute(score_kernel<KMAX, F, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(bytes)) != cudaSuccess)
         return false;
     if (dev >= 0 && dev < kMaxDevices)
@@ -1041,7 +1112,7 @@ static bool make_pool_map(CUtensorMap *map, const void *pool, int64_t num_pages)
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int KMAX, class F>
+template <int KMAX, class F, int NQ>
 static msa_status launch_score(const void *q, const void *kcache_pool, const float *kscale,
                                int64_t num_pages, const int32_t *block_table, int64_t bt_stride,
                                const int32_t *seq_lens, int batch, int max_model_len, int n_sink,
@@ -1068,12 +1139,12 @@ static msa_status launch_score(const void *q, const void *kcache_pool, const flo
     p.n_window = n_window;
     p.split_blocks = split_blocks;
     p.slot_capacity = slot_capacity;
-    if (!ensure_smem_attr<KMAX, F>(dev))
+    if (!ensure_smem_attr<KMAX, F, NQ>(dev))
         return MSA_ERR_CUDA;
-    const size_t smem = SmemLayout<KMAX, F>::bytes(batch);
+    const size_t smem = SmemLayout<KMAX, F, NQ>::bytes(batch);
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(Pipe<F>::kThreads), smem, st, attr);
-    return cudaLaunchKernelEx(&cfg, score_kernel<KMAX, F>, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, score_kernel<KMAX, F, NQ>, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 struct Plan {
@@ -1083,7 +1154,7 @@ struct Plan {
 };
 
 static msa_status plan(int batch, int max_batch, int max_model_len, int k, int split_blocks,
-                       size_t workspace_bytes, Plan &out)
+                       size_t workspace_bytes, Plan &out, int nq = 1)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
@@ -1098,7 +1169,7 @@ static msa_status plan(int batch, int max_batch, int max_model_len, int k, int s
     const int64_t need_slots = chunk_bound(batch, max_blocks, split_blocks, grid) + batch;
     if (workspace_bytes < off)
         return MSA_ERR_WORKSPACE_TOO_SMALL;
-    const int64_t cap = static_cast<int64_t>((workspace_bytes - off) / slot_bytes(kmax));
+    const int64_t cap = static_cast<int64_t>((workspace_bytes - off) / (slot_bytes(kmax) * nq));
     if (cap < need_slots)
         return MSA_ERR_WORKSPACE_TOO_SMALL;
     out.grid = grid;
@@ -1108,7 +1179,7 @@ static msa_status plan(int batch, int max_batch, int max_model_len, int k, int s
     return MSA_OK;
 }
 
-template <class F>
+template <class F, int NQ = 1>
 static msa_status score_entry(const void *q, const void *kcache_pool, const float *kscale,
                               int64_t num_pages, const int32_t *block_table, int64_t bt_stride,
                               const int32_t *seq_lens, int batch, int max_batch, int max_model_len,
@@ -1125,32 +1196,41 @@ static msa_status score_entry(const void *q, const void *kcache_pool, const floa
     if (batch == 0)
         return MSA_OK;
     Plan pl;
-    st = plan(batch, max_batch, max_model_len, k, split_blocks, workspace_bytes, pl);
+    st = plan(batch, max_batch, max_model_len, k, split_blocks, workspace_bytes, pl, NQ);
     if (st != MSA_OK)
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (kmax_for(k) == 16)
-        return launch_score<16, F>(q, kcache_pool, kscale, num_pages, block_table, bt_stride,
+        return launch_score<16, F, NQ>(q, kcache_pool, kscale, num_pages, block_table, bt_stride,
+                                       seq_lens, batch, max_model_len, n_sink, n_window,
+                                       out_block_scores, workspace, pl.slot_capacity, pl.grid,
+                                       split_blocks, s, pl.dev);
+    return launch_score<32, F, NQ>(q, kcache_pool, kscale, num_pages, block_table, bt_stride,
                                    seq_lens, batch, max_model_len, n_sink, n_window,
                                    out_block_scores, workspace, pl.slot_capacity, pl.grid,
                                    split_blocks, s, pl.dev);
-    return launch_score<32, F>(q, kcache_pool, kscale, num_pages, block_table, bt_stride, seq_lens,
-                               batch, max_model_len, n_sink, n_window, out_block_scores, workspace,
-                               pl.slot_capacity, pl.grid, split_blocks, s, pl.dev);
 }
 
 }  // namespace msa
 
 using namespace msa;
 
-extern "C" size_t msa_indexer_workspace_bytes(int max_batch, int max_model_len, int k,
-                                              int split_blocks)
+extern "C" size_t msa_indexer_workspace_bytes_mq(int max_batch, int max_model_len, int k,
+                                                 int split_blocks, int q_len)
 {
     if (!bounds_ok(max_batch, max_model_len, k, split_blocks))
         return 0;
+    if (q_len != 1 && q_len != 2 && q_len != 4)
+        return 0;
     const int64_t chunks = chunk_bound(max_batch, blocks_for(max_model_len), split_blocks, MSA_MAX_GRID);
     return slots_offset(max_batch) +
-           static_cast<size_t>(chunks + max_batch) * slot_bytes(kmax_for(k));
+           static_cast<size_t>(chunks + max_batch) * slot_bytes(kmax_for(k)) * q_len;
+}
+
+extern "C" size_t msa_indexer_workspace_bytes(int max_batch, int max_model_len, int k,
+                                              int split_blocks)
+{
+    return msa_indexer_workspace_bytes_mq(max_batch, max_model_len, k, split_blocks, 1);
 }
 
 
@@ -1179,9 +1259,8 @@ extern "C" msa_status msa_indexer_score_fp8(const void *q, const void *kcache_fp
                                out_block_scores, workspace, workspace_bytes, split_blocks, stream);
 }
 
-extern "C" msa_status msa_indexer_merge(int batch, int k, int32_t *out_ids, float *out_scores,
-                                        const void *workspace, size_t workspace_bytes,
-                                        void *stream)
+static msa_status merge_entry(int batch, int k, int cols, int32_t *out_ids, float *out_scores,
+                              const void *workspace, size_t workspace_bytes, void *stream)
 {
     if (!out_ids || !out_scores || !workspace || batch < 0 || batch > MSA_MAX_BATCH)
         return MSA_ERR_INVALID_ARG;
@@ -1195,21 +1274,29 @@ extern "C" msa_status msa_indexer_merge(int batch, int k, int32_t *out_ids, floa
         return MSA_OK;
     const int kmax = kmax_for(k);
     const size_t off = slots_offset(batch);
-    if (workspace_bytes < off + slot_bytes(kmax))
+    const size_t per_slot = slot_bytes(kmax) / kHeads * cols;
+    if (workspace_bytes < off + per_slot)
         return MSA_ERR_WORKSPACE_TOO_SMALL;
-    const int64_t cap = static_cast<int64_t>((workspace_bytes - off) / slot_bytes(kmax));
+    const int64_t cap = static_cast<int64_t>((workspace_bytes - off) / per_slot);
     const int capacity = static_cast<int>(cap > (int64_t{1} << 30) ? (int64_t{1} << 30) : cap);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint8_t *ws = static_cast<const uint8_t *>(workspace);
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(kHeads, static_cast<unsigned>(batch)),
+    cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(cols), static_cast<unsigned>(batch)),
                                         dim3(kMergeThreads), 0, s, attr);
     cudaError_t e = kmax == 16
-                        ? cudaLaunchKernelEx(&cfg, merge_kernel<16>, ws, batch, k, capacity,
+                        ? cudaLaunchKernelEx(&cfg, merge_kernel<16>, ws, batch, k, cols, capacity,
                                              out_ids, out_scores)
-                        : cudaLaunchKernelEx(&cfg, merge_kernel<32>, ws, batch, k, capacity,
+                        : cudaLaunchKernelEx(&cfg, merge_kernel<32>, ws, batch, k, cols, capacity,
                                              out_ids, out_scores);
     return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+extern "C" msa_status msa_indexer_merge(int batch, int k, int32_t *out_ids, float *out_scores,
+                                        const void *workspace, size_t workspace_bytes,
+                                        void *stream)
+{
+    return merge_entry(batch, k, kHeads, out_ids, out_scores, workspace, workspace_bytes, stream);
 }
 
 extern "C" msa_status msa_indexer_decode(const void *q, const void *kcache_pool, int64_t num_pages,
@@ -1327,6 +1414,42 @@ extern "C" msa_status msa_indexer_expand_pages(const int32_t *ids, int batch, in
         cudaLaunchKernelEx(&cfg, expand_pages_kernel, ids, k, seq_lens, kv_block_table,
                            kv_bt_stride, kPage / page_tokens, page_tokens, out_pages, out_num_pages);
     return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+extern "C" msa_status msa_indexer_decode_mq(const void *q, int q_len, const void *kcache_pool,
+                                            int64_t num_pages, const int32_t *block_table,
+                                            int64_t bt_stride, const int32_t *seq_lens, int batch,
+                                            int max_batch, int max_model_len, int k, int n_sink,
+                                            int n_window, int32_t *out_ids, float *out_scores,
+                                            float *out_block_scores, void *workspace,
+                                            size_t workspace_bytes, int split_blocks, void *stream)
+{
+    if (!out_ids || !out_scores)
+        return MSA_ERR_INVALID_ARG;
+    if (q_len < 1)
+        return MSA_ERR_INVALID_ARG;
+    if (q_len != 1 && q_len != 2 && q_len != 4)
+        return MSA_ERR_UNSUPPORTED;
+    msa_status st;
+    if (q_len == 1)
+        st = score_entry<Bf16Fmt, 1>(q, kcache_pool, nullptr, num_pages, block_table, bt_stride,
+                                     seq_lens, batch, max_batch, max_model_len, k, n_sink, n_window,
+                                     out_block_scores, workspace, workspace_bytes, split_blocks,
+                                     stream);
+    else if (q_len == 2)
+        st = score_entry<Bf16Fmt, 2>(q, kcache_pool, nullptr, num_pages, block_table, bt_stride,
+                                     seq_lens, batch, max_batch, max_model_len, k, n_sink, n_window,
+                                     out_block_scores, workspace, workspace_bytes, split_blocks,
+                                     stream);
+    else
+        st = score_entry<Bf16Fmt, 4>(q, kcache_pool, nullptr, num_pages, block_table, bt_stride,
+                                     seq_lens, batch, max_batch, max_model_len, k, n_sink, n_window,
+                                     out_block_scores, workspace, workspace_bytes, split_blocks,
+                                     stream);
+    if (st != MSA_OK || batch == 0)
+        return st;
+    return merge_entry(batch, k, kHeads * q_len, out_ids, out_scores, workspace, workspace_bytes,
+                       stream);
 }
 
 extern "C" msa_status msa_indexer_decode_fp8(const void *q, const void *kcache_fp8,
