@@ -193,6 +193,35 @@ class Oracle:
         return (s.reshape(B, Q, HEADS, stride), ids.reshape(B, Q, HEADS, k),
                 sel.reshape(B, Q, HEADS, k), lens)
 
+    def run_prefill(self, q: np.ndarray, cu_seqlens_q: np.ndarray, pool: np.ndarray,
+                    block_table: np.ndarray, seq_lens: np.ndarray, k: int, n_sink: int,
+                    n_window: int):
+        """Prefill: the new tokens of every request, each over its own causal prefix.
+
+        q is [total_q, 4, 128]; request b's new tokens are rows
+        [cu_seqlens_q[b], cu_seqlens_q[b+1]) and are its last n_b tokens
+        (vLLM PR #57832, "Question ... mixed batches": the prefill branch
+        scores iq[nd:] with cu_seqlens_q).  New token t of request b sits at
+        position seq_len - n_b + t and sees the first seq_len - n_b + t + 1
+        tokens, so each row is one decode query over that length.
+        Returns (scores [total_q,4,stride], ids [total_q,4,k], sel, lens [total_q]).
+        """
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+        seq = np.asarray(seq_lens, dtype=np.int64)
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        rows_bt, lens = [], []
+        for b in range(seq.shape[0]):
+            n = int(cu[b + 1] - cu[b])
+            for t in range(n):
+                rows_bt.append(bt[b])
+                lens.append(max(0, int(seq[b]) - n + t + 1))
+        lens = np.asarray(lens, dtype=np.int32)
+        rows_bt = np.asarray(rows_bt, dtype=np.int32).reshape(-1, bt.shape[1])
+        s = self.block_scores(q, pool, rows_bt, lens)
+        ids, sel = self.select(s, lens, k, n_sink, n_window)
+        return s, ids, sel, lens
+
     def run(self, w, k: Optional[int] = None, n_sink: Optional[int] = None,
             n_window: Optional[int] = None):
         """Block scores and selection for a `workloads.Workload` (bf16 or fp8 cache)."""

@@ -357,6 +357,26 @@ def check_multi_query_one_position_is_decode(orc) -> None:
     np.testing.assert_array_equal(s[:, 0], s1)
 
 
+def check_prefill_matches_multi_query_fixture(orc) -> None:
+    """Four new tokens at the end of a 130-token request are the four draft
+    positions of the multi-position fixture: the same ids and scores."""
+    with open(os.path.join(GOLDEN_DIR, "multi_query_causal.json")) as f:
+        fx = json.load(f)
+    L, Q = int(fx["seq_len"]), int(fx["q_len"])
+    pool = np.zeros((2, PAGE, DIM), dtype=np.float32)
+    for tok, v in fx["planted_dim0"].items():
+        pool[int(tok) // PAGE, int(tok) % PAGE, 0] = v
+    q = np.zeros((Q, HEADS, DIM), dtype=np.float32)
+    q[:, :, 0] = np.asarray(fx["alpha"], dtype=np.float32)[None, :]
+    s, ids, sel, lens = orc.run_prefill(wl.f32_to_bf16_bits(q), np.array([0, Q]),
+                                        wl.f32_to_bf16_bits(pool), np.array([[0, 1]], dtype=np.int32),
+                                        np.array([L], dtype=np.int32), int(fx["k"]),
+                                        int(fx["n_sink"]), int(fx["n_window"]))
+    assert list(lens) == [127, 128, 129, 130]
+    np.testing.assert_array_equal(ids, np.asarray(fx["expected_ids"], dtype=np.int32)[0])
+
+
 ALL_CHECKS = (check_golden, check_scores_vs_numpy, check_select_vs_rank_count, check_invariants,
               check_expand_golden, check_expand_invariants, check_e4m3_codes, check_fp8_golden,
-              check_fp8_vs_numpy, check_multi_query_golden, check_multi_query_one_position_is_decode)
+              check_fp8_vs_numpy, check_multi_query_golden, check_multi_query_one_position_is_decode,
+              check_prefill_matches_multi_query_fixture)
