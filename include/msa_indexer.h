@@ -256,6 +256,39 @@ msa_status msa_indexer_expand_pages(const int32_t *ids, int batch, int k, const 
                                     void *stream);
 
 /*
+ * Prefill scoring: every new token of every request selects blocks over its
+ * own causal prefix (vLLM PR #57832: the prefill branch scores iq[nd:] with
+ * cu_seqlens_q and takes the per-token top-k).  Request b's new tokens are
+ * its last n_b = cu_seqlens_q[b+1] - cu_seqlens_q[b] tokens; new token t
+ * sits at position seq_lens[b] - n_b + t and sees tokens [0, position].
+ * Pins and top-k are per (token, head), over that token's block count.
+ *
+ *   q             bf16 [total_q, 4, 128]: rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
+ *                 are request b's new tokens in order.
+ *   cu_seqlens_q  int32 [batch + 1], non-decreasing, cu_seqlens_q[batch] <= total_q.
+ *   seq_lens      int32 [batch]: tokens of request b including its new ones.
+ *   out_ids / out_scores  [total_q, 4, k].
+ *   out_block_scores      optional fp32 [total_q, 4, ceil(max_model_len/128)]:
+ *                 block scores of each token's visible blocks (others untouched).
+ *   workspace     >= msa_indexer_prefill_workspace_bytes(total_q, max_model_len)
+ *                 bytes (256 when out_block_scores is given), 256-byte aligned,
+ *                 zero-filled before first use.
+ *
+ * Requests with inconsistent rows or lengths produce -1 / -inf and set
+ * MSA_FAULT_SEQ_LEN; bad pages set MSA_FAULT_PAGE_ID (read with
+ * msa_indexer_get_error on this workspace).  bf16 cache; two kernels.
+ */
+size_t msa_indexer_prefill_workspace_bytes(int max_total_q, int max_model_len);
+
+msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqlens_q, int total_q,
+                               const void *kcache_pool, int64_t num_pages,
+                               const int32_t *block_table, int64_t bt_stride,
+                               const int32_t *seq_lens, int batch, int max_model_len, int k,
+                               int n_sink, int n_window, int32_t *out_ids, float *out_scores,
+                               float *out_block_scores, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/*
  * Reads the workspace fault word (MSA_FAULT_* bits) into *flags and clears
  * it.  Synchronises `stream`.  Returns MSA_ERR_INVALID_ARG for null
  * pointers, MSA_ERR_CUDA if a CUDA call fails.

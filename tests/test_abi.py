@@ -85,3 +85,32 @@ def test_bad_sizes_are_rejected_before_any_gpu_work(lib):
     assert lib.msa_indexer_decode(*args(pages=0)) == 1
     assert lib.msa_indexer_decode(*args(pages=1 << 25)) == 2
     assert lib.msa_indexer_decode(*args(maxB=5000, B=5000)) == 2
+
+
+def test_prefill_workspace_and_argument_checks(lib):
+    import sparse_attention_decode_gb300 as msa
+    # header + total_q x 4 heads x blocks x fp32
+    assert msa.msa_indexer_prefill_workspace_bytes(100, 8192) == 256 + 100 * 4 * 64 * 4
+    assert msa.msa_indexer_prefill_workspace_bytes(0, 8192) == 256
+    assert msa.msa_indexer_prefill_workspace_bytes(-1, 8192) == 0
+    assert msa.msa_indexer_prefill_workspace_bytes(4, 0) == 0
+    st = lib.msa_indexer_prefill(None, None, 4, None, 8, None, 8, None, 1, 1024, 16, 1, 2, None,
+                                 None, None, None, 0, None)
+    assert st == 1
+
+
+def test_prefill_bad_sizes_are_rejected_before_any_gpu_work(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-only check: never hand placeholder pointers to a process with a GPU")
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+    args = lambda **kw: [fake, fake, kw.get("tq", 64), fake, kw.get("pages", 10), fake, 8, fake,
+                         kw.get("B", 2), 1024, kw.get("k", 16), kw.get("sink", 1), kw.get("win", 2),
+                         fake, fake, None, fake, kw.get("wsb", 1 << 20), None]
+    assert lib.msa_indexer_prefill(*args(sink=9, win=8)) == 1  # pins exceed k
+    assert lib.msa_indexer_prefill(*args(k=33)) == 2
+    assert lib.msa_indexer_prefill(*args(B=0)) == 1
+    assert lib.msa_indexer_prefill(*args(B=5000)) == 2
+    assert lib.msa_indexer_prefill(*args(tq=-1)) == 1
+    assert lib.msa_indexer_prefill(*args(pages=0)) == 1
+    assert lib.msa_indexer_prefill(*args(wsb=256 + 64 * 4 * 8 * 4 - 4)) == 3
