@@ -107,9 +107,15 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
 
 
+# The files the decode kernels are compiled from (the prefill unit is separate).
+DECODE_SOURCES = ("host_util.cuh", "keys.cuh", "layout.cuh", "msa_indexer.cu", "ptx.cuh",
+                  os.path.join("..", "..", "include", "msa_indexer.h"))
+
+
 def kernel_source_hash() -> str:
+    """Hash of the decode kernels' sources: a profile taken at another hash is stale."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
+    for name in DECODE_SOURCES:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())

@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIBRARY = os.path.join(LIB_DIR, "libmsa_indexer.so")
-MAIN_SOURCE = os.path.join(CSRC, "msa_indexer.cu")
+UNITS = ("msa_indexer.cu", "prefill.cu")  # translation units, compiled in parallel
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -38,14 +38,21 @@ def needs_build(out: str = LIBRARY) -> bool:
     return any(os.path.getmtime(s) > t for s in sources())
 
 
-def command(out: str = LIBRARY, verbose_ptxas: bool = False):
-    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(_nvcc())), "lib64")
-    cmd = [_nvcc(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-           "-shared", "-cudart", "shared", f"-I{INCLUDE}", "-Xlinker", f"-rpath={cuda_lib}",
-           "-o", out, MAIN_SOURCE]
+def _common_flags():
+    return [*ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{INCLUDE}"]
+
+
+def compile_command(unit: str, obj: str, verbose_ptxas: bool = False):
+    cmd = [_nvcc(), *_common_flags(), "-c", "-o", obj, os.path.join(CSRC, unit)]
     if verbose_ptxas:
         cmd.insert(1, "-Xptxas=-v")
     return cmd
+
+
+def link_command(objs, out: str):
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(_nvcc())), "lib64")
+    return [_nvcc(), *ARCH_FLAGS, "-shared", "-cudart", "shared", "-Xlinker", f"-rpath={cuda_lib}",
+            "-o", out, *objs]
 
 
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
@@ -53,9 +60,23 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if not force and not needs_build():
         return LIBRARY
     os.makedirs(LIB_DIR, exist_ok=True)
-    tmp = LIBRARY + f".tmp{os.getpid()}"
-    subprocess.run(command(tmp, verbose_ptxas), check=True)
-    os.replace(tmp, LIBRARY)
+    from concurrent.futures import ThreadPoolExecutor
+    tag = f".tmp{os.getpid()}"
+    objs = [os.path.join(LIB_DIR, os.path.splitext(u)[0] + tag + ".o") for u in UNITS]
+    try:
+        with ThreadPoolExecutor(len(UNITS)) as ex:
+            runs = list(ex.map(lambda uo: subprocess.run(compile_command(uo[0], uo[1], verbose_ptxas)),
+                               zip(UNITS, objs)))
+        for u, r in zip(UNITS, runs):
+            if r.returncode != 0:
+                raise subprocess.CalledProcessError(r.returncode, f"nvcc {u}")
+        tmp = LIBRARY + tag
+        subprocess.run(link_command(objs, tmp), check=True)
+        os.replace(tmp, LIBRARY)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIBRARY
 
 

@@ -37,6 +37,7 @@
 #include "keys.cuh"
 #include "layout.cuh"
 #include "ptx.cuh"
+#include "host_util.cuh"
 
 namespace msa {
 
@@ -303,7 +304,7 @@ __device__ __forceinline__ void score_page_fp8(uint32_t stage, const float *scl,
                                                float &m0, float &m1)
 {
     const float neg_inf = -__int_as_float(0x7f800000);
-    const int g = lane >> 2, t = lane & 3;
+    const int g = lane >> 2;
     m0 = neg_inf;
     m1 = neg_inf;
 #pragma unroll
@@ -905,12 +906,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const uint8_t *ws,
     }
 }
 
-}  // namespace msa
-
-#include "prefill.cuh"
-
-namespace msa {
-
 // Selected blocks -> small KV pages.  One warp per (request, head): the
 // <= 32 selected ids are sorted ascending across the lanes (bitonic), each
 // lane counts the small pages of its block, a lane prefix gives the output
@@ -970,60 +965,6 @@ __global__ void __launch_bounds__(128) expand_pages_kernel(const int32_t *ids, i
 // host side
 // ---------------------------------------------------------------------------
 
-// Launch configuration with programmatic dependent launch: the grid may be
-// scheduled while the previous kernel on the stream is still running; it
-// calls griddep_wait() before touching global memory, so it observes all of
-// that kernel's writes (and the previous kernel cannot see any of its own).
-static cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                                     cudaLaunchAttribute (&attr)[1])
-{
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cfg;
-}
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_tiled()
-{
-    static EncodeTiledFn fn = [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return static_cast<EncodeTiledFn>(nullptr);
-        return reinterpret_cast<EncodeTiledFn>(f);
-    }();
-    return fn;
-}
-
-constexpr int kMaxDevices = 64;
-
-static int device_sms(int dev)
-{
-    static std::atomic<int> cache[kMaxDevices];
-    int v = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load(std::memory_order_relaxed) : 0;
-    if (v > 0)
-        return v;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
-        return 0;
-    if (dev >= 0 && dev < kMaxDevices)
-        cache[dev].store(v, std::memory_order_relaxed);
-    return v;
-}
-
 template <int KMAX, class F, int NQ>
 static bool ensure_smem_attr(int dev)
 {
@@ -1038,8 +979,6 @@ static bool ensure_smem_attr(int dev)
         done[dev].store(true, std::memory_order_release);
     return true;
 }
-
-static int64_t blocks_for(int max_model_len) { return (static_cast<int64_t>(max_model_len) + kPage - 1) / kPage; }
 
 static bool bounds_ok(int max_batch, int max_model_len, int k, int split_blocks)
 {
@@ -1477,92 +1416,6 @@ extern "C" msa_status msa_indexer_decode_fp8(const void *q, const void *kcache_f
     if (st != MSA_OK || batch == 0)
         return st;
     return msa_indexer_merge(batch, k, out_ids, out_scores, workspace, workspace_bytes, stream);
-}
-
-extern "C" size_t msa_indexer_prefill_workspace_bytes(int max_total_q, int max_model_len)
-{
-    if (max_total_q < 0 || max_model_len < 1)
-        return 0;
-    return kHeaderBytes + static_cast<size_t>(max_total_q) * kHeads *
-                              static_cast<size_t>(blocks_for(max_model_len)) * sizeof(float);
-}
-
-extern "C" msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqlens_q, int total_q,
-                                          const void *kcache_pool, int64_t num_pages,
-                                          const int32_t *block_table, int64_t bt_stride,
-                                          const int32_t *seq_lens, int batch, int max_model_len,
-                                          int k, int n_sink, int n_window, int32_t *out_ids,
-                                          float *out_scores, float *out_block_scores,
-                                          void *workspace, size_t workspace_bytes, void *stream)
-{
-    if (!q || !cu_seqlens_q || !kcache_pool || !block_table || !seq_lens || !out_ids ||
-        !out_scores || !workspace)
-        return MSA_ERR_INVALID_ARG;
-    if (total_q < 0 || batch < 1 || max_model_len < 1 || k < 1 || n_sink < 0 || n_window < 0 ||
-        num_pages < 1 || bt_stride < 1)
-        return MSA_ERR_INVALID_ARG;
-    if (k > MSA_MAX_TOPK || batch > MSA_MAX_BATCH || num_pages > (int64_t{1} << 24))
-        return MSA_ERR_UNSUPPORTED;
-    if (static_cast<int64_t>(n_sink) + n_window > k)
-        return MSA_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(kcache_pool) & 15) ||
-        (reinterpret_cast<uintptr_t>(workspace) & 255))
-        return MSA_ERR_INVALID_ARG;
-    const int64_t bs_stride = blocks_for(max_model_len);
-    const size_t scores_bytes = static_cast<size_t>(total_q) * kHeads * bs_stride * sizeof(float);
-    const size_t need = kHeaderBytes + (out_block_scores ? 0 : scores_bytes);
-    if (workspace_bytes < need)
-        return MSA_ERR_WORKSPACE_TOO_SMALL;
-    if (total_q == 0)
-        return MSA_OK;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return MSA_ERR_CUDA;
-    static std::atomic<bool> attr_done[kMaxDevices];
-    if (dev >= 0 && dev < kMaxDevices && !attr_done[dev].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(prefill_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kPfSmemBytes)) != cudaSuccess)
-            return MSA_ERR_CUDA;
-        attr_done[dev].store(true, std::memory_order_release);
-    }
-    PrefillParams p;
-    std::memset(&p, 0, sizeof p);
-    if (!make_pool_map<Bf16Fmt>(&p.tmap, kcache_pool, num_pages))
-        return MSA_ERR_CUDA;
-    WorkspaceHeader *hdr = static_cast<WorkspaceHeader *>(workspace);
-    p.q = static_cast<const uint16_t *>(q);
-    p.cu_q = cu_seqlens_q;
-    p.block_table = block_table;
-    p.seq_lens = seq_lens;
-    p.scores = out_block_scores ? out_block_scores
-                                : reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kHeaderBytes);
-    p.fault = &hdr->fault;
-    p.bt_stride = bt_stride;
-    p.bs_stride = bs_stride;
-    p.num_pages = num_pages;
-    p.batch = batch;
-    p.seq_limit = static_cast<int>(bt_stride * kPage < max_model_len ? bt_stride * kPage : max_model_len);
-    p.total_q = total_q;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // tiles of 32 new tokens: at most ceil(total_q / 32) + batch (one partial tile per request)
-    const int64_t grid = (static_cast<int64_t>(total_q) + kPfTokens - 1) / kPfTokens + batch;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(grid)), dim3(kPfThreads),
-                                        kPfSmemBytes, st, attr);
-    if (cudaLaunchKernelEx(&cfg, prefill_score_kernel, p) != cudaSuccess)
-        return MSA_ERR_CUDA;
-    const int64_t rows = static_cast<int64_t>(total_q) * kHeads;
-    cudaLaunchAttribute attr2[1];
-    cudaLaunchConfig_t cfg2 = pdl_config(dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), 0,
-                                         st, attr2);
-    cudaError_t e = kmax_for(k) == 16
-                        ? cudaLaunchKernelEx(&cfg2, rows_topk_kernel<16>, static_cast<const float *>(p.scores),
-                                             bs_stride, cu_seqlens_q, seq_lens, batch, total_q,
-                                             p.seq_limit, k, n_sink, n_window, out_ids, out_scores)
-                        : cudaLaunchKernelEx(&cfg2, rows_topk_kernel<32>, static_cast<const float *>(p.scores),
-                                             bs_stride, cu_seqlens_q, seq_lens, batch, total_q,
-                                             p.seq_limit, k, n_sink, n_window, out_ids, out_scores);
-    return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 extern "C" msa_status msa_indexer_get_error(void *workspace, void *stream, uint32_t *flags)

@@ -1,0 +1,689 @@
+// Prefill scoring for the MSA lightning indexer on GB300 (sm_103a).
+//
+// Every new token of every request scores the blocks of its own causal prefix
+// (vLLM PR #57832, reply to "Will this re-run the decode part when in mixed
+// batches?": the prefill branch scores the prefill query rows over the block
+// table, then takes a per-token top-k over cu_seqlens_q; prefill amortises
+// each index-cache read over many query tokens).  Request b has n_b new
+// tokens, its last ones: new token t sits at position seq_len_b - n_b + t and
+// sees tokens [0, position].
+//
+// tc_prefill_score_kernel (persistent, one CTA per SM): the product of the
+// new tokens' query rows (token x head) with the keys is a dense contraction,
+// run on the 5th-generation tensor cores.  Work unit = (tile of 64 new tokens
+// of one request, one visible page of that tile); the units of the whole
+// batch, in order, are cut into one equal range per CTA (the page counts
+// have a closed form), which balances the causal triangle.  Per CTA:
+//   warp 0     TMA producer: the tile's 256 query rows (64 KiB, 128B swizzle)
+//              and the pages (32 KiB each) through a 4-stage ring;
+//   warp 1     owns the TMEM allocation; one thread issues tcgen05.mma
+//              (M = 128 rows, N = 128 keys, K = 16) for both 128-row halves
+//              of the tile against each page, fp32 accumulators in TMEM,
+//              double-buffered across pages (2 x 2 x 128 = 512 columns);
+//   warps 2-9  read their rows' 128 accumulators per page from TMEM and
+//              write the masked block max (keys <= the row's position).
+//
+// rows_topk_kernel: one warp per (token, head) row: pins and top-k over the
+// row's block scores (32 keys sorted at a time, merged into a running list).
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/msa_indexer.h"
+#include "host_util.cuh"
+#include "keys.cuh"
+#include "layout.cuh"
+#include "ptx.cuh"
+#include "tcgen05.cuh"
+
+namespace msa {
+
+constexpr int kTileTokens = 64;                       // new tokens per work tile
+constexpr int kMRows = 128;                           // rows per MMA: 32 tokens x 4 heads
+constexpr int kMTiles = kTileTokens * kHeads / kMRows;  // 2
+constexpr int kTcStages = 4;
+constexpr int kEpiWarps = 4 * kMTiles;                // one per (TMEM lane quarter, M tile)
+constexpr int kTcThreads = 32 * (2 + kEpiWarps);
+constexpr uint32_t kTmemCols = 2 * kMTiles * kPage;   // 512
+constexpr int kQTileBytes = kMRows * kDim * 2;        // 32 KiB per M tile
+constexpr uint32_t kQBytes = kMTiles * kQTileBytes;
+constexpr uint32_t kIdesc = umma_idesc_bf16_f32(kMRows, kPage);
+
+struct TcParams {
+    CUtensorMap kmap;  // pool as [num_pages*128][128] bf16, 64x128 boxes, 128B swizzle
+    CUtensorMap qmap;  // q as [total_q*4][128] bf16, 64x128 boxes, 128B swizzle
+    const int32_t *cu_q;
+    const int32_t *block_table;
+    const int32_t *seq_lens;
+    float *scores;  // [total_q, 4, bs_stride]
+    uint32_t *fault;
+    int64_t bt_stride;
+    int64_t bs_stride;
+    int64_t num_pages;
+    int batch;
+    int seq_limit;
+    int total_q;
+};
+
+struct TcSmem {
+    uint64_t k_full[kTcStages];
+    uint64_t k_empty[kTcStages];
+    uint64_t q_full;
+    uint64_t q_empty;
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+    int b0, t0, j0;
+    long long units;
+};
+
+constexpr size_t kTcSmemBytes = 1024 /* alignment slack */ + kQBytes +
+                                static_cast<size_t>(kTcStages) * kPageBytes + sizeof(TcSmem);
+
+// One request as the kernels see it.  ok = false for a request they refuse:
+// rows outside [0, total_q) or out of order, a length past the limit or
+// negative, or more new tokens than tokens.
+struct Req {
+    int n, len, c0;
+    bool ok;
+};
+
+__device__ __forceinline__ Req req_info(const int32_t *cu_q, const int32_t *seq_lens, int total_q,
+                                        int seq_limit, int b)
+{
+    Req r;
+    r.c0 = cu_q[b];
+    const int c1 = cu_q[b + 1];
+    r.n = c1 - r.c0;
+    r.len = seq_lens[b];
+    r.ok = r.c0 >= 0 && c1 <= total_q && r.n >= 0 && r.len >= 0 && r.len <= seq_limit && r.n <= r.len;
+    return r;
+}
+
+__device__ __forceinline__ int tiles_of(const Req &r) { return (r.n + kTileTokens - 1) / kTileTokens; }
+
+// Pages tile t sees: those up to its last token's position.
+__device__ __forceinline__ int tile_pages(const Req &r, int t)
+{
+    const int last = min(r.n, kTileTokens * (t + 1)) - 1;
+    return (r.len - r.n + last) / kPage + 1;
+}
+
+// Pages of tiles [0, t) for t <= tiles - 1 (all full tiles).  Full tile t'
+// ends at position c + 64 t' with c = len - n + 63 and sees
+// floor((c + 64 t') / 128) + 1 pages; even t' = 2m gives m + floor(c / 128),
+// odd t' = 2m + 1 gives m + floor((c + 64) / 128).
+__device__ __forceinline__ long long pages_before(const Req &r, int t)
+{
+    const long long c = static_cast<long long>(r.len) - r.n + kTileTokens - 1;
+    const long long e = (t + 1) / 2, o = t / 2;
+    return t + e * (c / kPage) + e * (e - 1) / 2 + o * ((c + kTileTokens) / kPage) + o * (o - 1) / 2;
+}
+
+__device__ __forceinline__ long long req_units(const Req &r)
+{
+    if (!r.ok || r.n == 0)
+        return 0;
+    const int T = tiles_of(r);
+    return pages_before(r, T - 1) + tile_pages(r, T - 1);
+}
+
+__device__ __forceinline__ long long warp_sum64(long long v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ long long warp_incl_scan64(long long v, int lane)
+{
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o)
+            v += u;
+    }
+    return v;
+}
+
+// Walks the work tiles of the batch in order, from a given (request, tile).
+struct Cursor {
+    int b, t, j, T;
+    Req r;
+
+    __device__ __forceinline__ void load(const TcParams &p, int b_, int t_, int j_)
+    {
+        b = b_;
+        t = t_;
+        j = j_;
+        r = req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, b);
+        T = tiles_of(r);
+    }
+
+    // Moves to the next tile; false past the last request.
+    __device__ __forceinline__ bool next(const TcParams &p)
+    {
+        j = 0;
+        if (++t < T)
+            return true;
+        t = 0;
+        for (++b; b < p.batch; ++b) {
+            r = req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, b);
+            if (r.ok && r.n > 0) {
+                T = tiles_of(r);
+                return true;
+            }
+        }
+        return false;
+    }
+};
+
+// This CTA's range of work units: [W*g/G, W*(g+1)/G) of the batch's
+// (tile, page) units in order.  Run by one warp; writes the start and count.
+__device__ void plan_range(const TcParams &p, TcSmem *ctl, int lane)
+{
+    long long W = 0;
+    for (int b0 = 0; b0 < p.batch; b0 += 32) {
+        long long v = 0;
+        if (b0 + lane < p.batch) {
+            const Req r = req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, b0 + lane);
+            if (!r.ok && blockIdx.x == 0)
+                atomicOr(p.fault, MSA_FAULT_SEQ_LEN);
+            v = req_units(r);
+        }
+        W += warp_sum64(v);
+    }
+    const long long G = gridDim.x, g = blockIdx.x;
+    const long long u0 = W * g / G, u1 = W * (g + 1) / G;
+    int fb = -1;
+    long long base = 0;
+    if (u1 > u0) {
+        long long cum = 0;
+        for (int b0 = 0; b0 < p.batch && fb < 0; b0 += 32) {
+            long long v = 0;
+            if (b0 + lane < p.batch)
+                v = req_units(req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, b0 + lane));
+            const long long incl = warp_incl_scan64(v, lane);
+            const long long total = __shfl_sync(0xffffffffu, incl, 31);
+            if (cum + total > u0) {
+                const unsigned m = __ballot_sync(0xffffffffu, cum + incl > u0);
+                const int l = __ffs(m) - 1;
+                fb = b0 + l;
+                base = cum + __shfl_sync(0xffffffffu, incl - v, l);
+            } else {
+                cum += total;
+            }
+        }
+    }
+    if (lane == 0) {
+        if (fb < 0) {
+            ctl->units = 0;
+        } else {
+            const Req r = req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, fb);
+            const long long rel = u0 - base;
+            // the last tile t with pages_before(t) <= rel
+            int lo = 0, hi = tiles_of(r) - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (pages_before(r, mid) <= rel)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            ctl->b0 = fb;
+            ctl->t0 = lo;
+            ctl->j0 = static_cast<int>(rel - pages_before(r, lo));
+            ctl->units = u1 - u0;
+        }
+    }
+}
+
+__device__ __forceinline__ bool aborted(const TcSmem *ctl)
+{
+    return *reinterpret_cast<const volatile int *>(&ctl->abort) != 0;
+}
+
+__device__ __forceinline__ void give_up(const TcParams &p, TcSmem *ctl)
+{
+    atomicOr(p.fault, MSA_FAULT_TIMEOUT);
+    *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const __grid_constant__ TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t q_smem = smem_addr(smem);
+    const uint32_t k_smem = q_smem + kQBytes;
+    TcSmem *ctl = reinterpret_cast<TcSmem *>(smem + kQBytes + kTcStages * kPageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(smem_addr(&ctl->k_full[s]), 1);
+            mbar_init(smem_addr(&ctl->k_empty[s]), 1);
+        }
+        mbar_init(smem_addr(&ctl->q_full), 1);
+        mbar_init(smem_addr(&ctl->q_empty), 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_addr(&ctl->acc_full[a]), 1);
+            mbar_init(smem_addr(&ctl->acc_empty[a]), kEpiWarps);
+        }
+        mbar_init(smem_addr(&ctl->mma_done), 1);
+        ctl->abort = 0;
+        fence_barrier_init();
+    }
+    griddep_wait();
+    griddep_launch_dependents();
+    if (warp == 0)
+        plan_range(p, ctl, lane);
+    __syncthreads();
+    const long long units = ctl->units;
+    if (units <= 0)
+        return;  // uniform: no TMEM taken yet
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish_alloc_permit();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = ctl->tmem_base;
+    const int sb = ctl->b0, st = ctl->t0, sj = ctl->j0;
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        Cursor c;
+        c.load(p, sb, st, sj);
+        long long left = units;
+        uint32_t kc = 0, seg = 0;
+        bool ok_run = true;
+        while (left > 0 && ok_run) {
+            const int nb = tile_pages(c.r, c.t);
+            const int je = static_cast<int>(min(static_cast<long long>(nb), c.j + left));
+            if (lane == 0) {
+                if (seg > 0 && !mbar_wait(smem_addr(&ctl->q_empty), (seg - 1) & 1u)) {
+                    give_up(p, ctl);
+                    ok_run = false;
+                } else {
+                    const uint32_t qf = smem_addr(&ctl->q_full);
+                    const int row0 = (c.r.c0 + kTileTokens * c.t) * kHeads;
+                    mbar_arrive_expect_tx(qf, kQBytes);
+#pragma unroll
+                    for (int mt = 0; mt < kMTiles; ++mt)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_2d(q_smem + mt * kQTileBytes + h * kHalfPageBytes, &p.qmap, 64 * h,
+                                        row0 + mt * kMRows, qf);
+                }
+            }
+            ok_run = __shfl_sync(0xffffffffu, ok_run ? 1 : 0, 0) != 0;
+            for (int jb = c.j; jb < je && ok_run; jb += 32) {
+                const int jl = jb + lane;
+                int page = 0, ok = 0;
+                if (jl < je) {
+                    page = p.block_table[static_cast<int64_t>(c.b) * p.bt_stride + jl];
+                    ok = (page >= 0 && page < p.num_pages) ? 1 : 0;
+                    if (!ok)
+                        atomicOr(p.fault, MSA_FAULT_PAGE_ID);
+                }
+                const int cnt = min(32, je - jb);
+                for (int i = 0; i < cnt; ++i) {
+                    const int pg = __shfl_sync(0xffffffffu, page, i);
+                    const int pok = __shfl_sync(0xffffffffu, ok, i);
+                    int good = 1;
+                    if (lane == 0) {
+                        const int s = static_cast<int>(kc % kTcStages);
+                        const uint32_t full = smem_addr(&ctl->k_full[s]);
+                        if (aborted(ctl) ||
+                            (kc >= kTcStages &&
+                             !mbar_wait(smem_addr(&ctl->k_empty[s]), ((kc / kTcStages) - 1) & 1u))) {
+                            give_up(p, ctl);
+                            good = 0;
+                        } else if (pok) {
+                            const uint32_t dst = k_smem + s * kPageBytes;
+                            mbar_arrive_expect_tx(full, kPageBytes);
+                            tma_load_2d(dst, &p.kmap, 0, pg * kPage, full);
+                            tma_load_2d(dst + kHalfPageBytes, &p.kmap, 64, pg * kPage, full);
+                        } else {
+                            mbar_arrive(full);  // nothing to load; the epilogue writes -inf
+                        }
+                    }
+                    if (__shfl_sync(0xffffffffu, good, 0) == 0) {
+                        ok_run = false;
+                        break;
+                    }
+                    ++kc;
+                }
+            }
+            ++seg;
+            left -= je - c.j;
+            if (left > 0 && !c.next(p))
+                break;
+        }
+        if (lane == 0) {  // drain: no copy may land after the CTA exits
+            for (uint32_t i = kc > kTcStages ? kc - kTcStages : 0; i < kc; ++i)
+                if (!mbar_wait(smem_addr(&ctl->k_full[i % kTcStages]), (i / kTcStages) & 1u))
+                    give_up(p, ctl);
+            if (seg > 0 && !mbar_wait(smem_addr(&ctl->q_full), (seg - 1) & 1u))
+                give_up(p, ctl);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issue (one thread) ----------------
+        if (lane == 0) {
+            Cursor c;
+            c.load(p, sb, st, sj);
+            long long left = units;
+            uint32_t kc = 0, ac = 0, seg = 0;
+            bool ok_run = true;
+            while (left > 0 && ok_run) {
+                const int nb = tile_pages(c.r, c.t);
+                const int je = static_cast<int>(min(static_cast<long long>(nb), c.j + left));
+                if (!mbar_wait(smem_addr(&ctl->q_full), seg & 1u)) {
+                    give_up(p, ctl);
+                    break;
+                }
+                tc_fence_after_sync();
+                for (int j = c.j; j < je; ++j) {
+                    const int s = static_cast<int>(kc % kTcStages);
+                    const int a = static_cast<int>(ac & 1u);
+                    if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->k_full[s]), (kc / kTcStages) & 1u) ||
+                        (ac >= 2 && !mbar_wait(smem_addr(&ctl->acc_empty[a]), ((ac >> 1) - 1) & 1u))) {
+                        give_up(p, ctl);
+                        ok_run = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t kst = k_smem + s * kPageBytes;
+#pragma unroll
+                    for (int mt = 0; mt < kMTiles; ++mt) {
+                        const uint32_t d = tmem + static_cast<uint32_t>(a * kMTiles * kPage + mt * kPage);
+#pragma unroll
+                        for (int ks = 0; ks < kDim / 16; ++ks) {
+                            const uint32_t off = (ks >> 2) * kHalfPageBytes + (ks & 3) * 32;
+                            umma_bf16(d, umma_desc_sw128(q_smem + mt * kQTileBytes + off),
+                                      umma_desc_sw128(kst + off), kIdesc, ks > 0 ? 1u : 0u);
+                        }
+                    }
+                    umma_commit(smem_addr(&ctl->k_empty[s]));
+                    umma_commit(smem_addr(&ctl->acc_full[a]));
+                    ++kc;
+                    ++ac;
+                }
+                umma_commit(smem_addr(&ctl->q_empty));
+                ++seg;
+                left -= je - c.j;
+                if (left > 0 && !c.next(p))
+                    break;
+            }
+            // every MMA issued has completed before TMEM is freed
+            umma_commit(smem_addr(&ctl->mma_done));
+            if (!mbar_wait(smem_addr(&ctl->mma_done), 0))
+                give_up(p, ctl);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: TMEM -> block scores ----------------
+        const int e = warp - 2;
+        const int quarter = warp & 3;        // TMEM lanes this warp may read
+        const int mt = e >> 2;               // M tile of this warp
+        const int row_in_tile = mt * kMRows + 32 * quarter + lane;  // 0..255
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16) +
+                                   static_cast<uint32_t>(mt * kPage);
+        const float neg_inf = -__int_as_float(0x7f800000);
+        Cursor c;
+        c.load(p, sb, st, sj);
+        long long left = units;
+        uint32_t ac = 0;
+        bool ok_run = true;
+        while (left > 0 && ok_run) {
+            const int nb = tile_pages(c.r, c.t);
+            const int je = static_cast<int>(min(static_cast<long long>(nb), c.j + left));
+            const int tl = kTileTokens * c.t + (row_in_tile >> 2);  // token within the request's new ones
+            const int head = row_in_tile & 3;
+            const bool live = tl < c.r.n;
+            const int pos = c.r.len - c.r.n + tl;
+            float *out = p.scores + (static_cast<int64_t>(c.r.c0 + tl) * kHeads + head) * p.bs_stride;
+            for (int j = c.j; j < je; ++j) {
+                const int a = static_cast<int>(ac & 1u);
+                bool ready = !aborted(ctl) && mbar_wait(smem_addr(&ctl->acc_full[a]), (ac >> 1) & 1u);
+                ready = __all_sync(0xffffffffu, ready);
+                if (!ready) {
+                    if (lane == 0)
+                        give_up(p, ctl);
+                    ok_run = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const int page = p.block_table[static_cast<int64_t>(c.b) * p.bt_stride + j];
+                const bool page_ok = page >= 0 && page < p.num_pages;
+                const int first_key = j * kPage;
+                const bool want = live && first_key <= pos;
+                if (page_ok && __any_sync(0xffffffffu, want)) {
+                    float mx = neg_inf;
+#pragma unroll
+                    for (int q4 = 0; q4 < kPage / 32; ++q4) {
+                        uint32_t r[32];
+                        tmem_ld32(lane_addr + static_cast<uint32_t>(a * kMTiles * kPage + 32 * q4), r);
+                        tmem_wait_ld(r);
+                        const int lim = pos - (first_key + 32 * q4);  // keys i <= lim are visible
+                        if (lim >= 31) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                mx = fmaxf(mx, __uint_as_float(r[i]));
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                mx = fmaxf(mx, i <= lim ? __uint_as_float(r[i]) : neg_inf);
+                        }
+                    }
+                    if (want)
+                        out[j] = mx;
+                } else if (!page_ok && want) {
+                    out[j] = neg_inf;
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(&ctl->acc_empty[a]));
+                ++ac;
+            }
+            left -= je - c.j;
+            if (left > 0 && !c.next(p))
+                break;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Sorts 32 keys (one per lane) into descending order across the warp.
+__device__ __forceinline__ uint64_t sort32_desc(uint64_t v, int lane)
+{
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int j = size >> 1; j > 0; j >>= 1) {
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
+            const bool desc = (lane & size) == 0;  // always true at size 32
+            const bool low = (lane & j) == 0;
+            v = (low == desc) ? umax64(v, o) : umin64(v, o);
+        }
+    }
+    return v;
+}
+
+// One warp per (token, head) row of the prefill: pins and top-k of its blocks.
+template <int KMAX>
+__global__ void __launch_bounds__(256) rows_topk_kernel(const float *scores, int64_t bs_stride,
+                                                        const int32_t *cu_q, const int32_t *seq_lens,
+                                                        int batch, int total_q, int seq_limit, int k,
+                                                        int n_sink, int n_window, int32_t *out_ids,
+                                                        float *out_scores)
+{
+    griddep_wait();
+    griddep_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // (token, head)
+    if (row >= static_cast<int64_t>(total_q) * kHeads)
+        return;
+    const int tok = static_cast<int>(row / kHeads);
+    // the request of this token: the last b with cu_q[b] <= tok
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cu_q[mid] <= tok)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const Req r = req_info(cu_q, seq_lens, total_q, seq_limit, lo);
+    int nb = 0;
+    if (r.ok && r.c0 <= tok && tok < r.c0 + r.n)
+        nb = (r.len - r.n + (tok - r.c0)) / kPage + 1;
+    const float *srow = scores + row * bs_stride;
+    uint64_t run = 0;
+    for (int c0 = 0; c0 < nb; c0 += 32) {
+        const int j = c0 + lane;
+        uint64_t key = 0;
+        if (j < nb) {
+            const float s = srow[j];
+            // -inf marks a block whose page was out of range: never selected
+            if (s != -__int_as_float(0x7f800000))
+                key = pack_key(s, j, j < n_sink || j >= nb - n_window);
+        }
+        const uint64_t sorted = sort32_desc(key, lane);
+        if constexpr (KMAX == 16)
+            run = merge_top<16>(run, __shfl_sync(0xffffffffu, sorted, (15 - lane) & 31), lane);
+        else
+            run = merge_top<32>(run, __shfl_sync(0xffffffffu, sorted, 31 - lane), lane);
+    }
+    if (lane < k) {
+        int id;
+        float score;
+        unpack_key(run, id, score);
+        out_ids[row * k + lane] = id;
+        out_scores[row * k + lane] = score;
+    }
+}
+
+// 2-D bf16 tensor map over `rows` rows of 128 elements (256 B), 64x128 boxes,
+// 128-byte swizzle: two boxes fill one 128x128 operand tile.
+static bool make_rows_map(CUtensorMap *map, const void *base, int64_t rows)
+{
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * 2};
+    const cuuint32_t box[2] = {64u, 128u};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" size_t msa_indexer_prefill_workspace_bytes(int max_total_q, int max_model_len)
+{
+    if (max_total_q < 0 || max_model_len < 1)
+        return 0;
+    return kHeaderBytes + static_cast<size_t>(max_total_q) * kHeads *
+                              static_cast<size_t>(blocks_for(max_model_len)) * sizeof(float);
+}
+
+extern "C" msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqlens_q, int total_q,
+                                          const void *kcache_pool, int64_t num_pages,
+                                          const int32_t *block_table, int64_t bt_stride,
+                                          const int32_t *seq_lens, int batch, int max_model_len,
+                                          int k, int n_sink, int n_window, int32_t *out_ids,
+                                          float *out_scores, float *out_block_scores,
+                                          void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!q || !cu_seqlens_q || !kcache_pool || !block_table || !seq_lens || !out_ids ||
+        !out_scores || !workspace)
+        return MSA_ERR_INVALID_ARG;
+    if (total_q < 0 || batch < 1 || max_model_len < 1 || k < 1 || n_sink < 0 || n_window < 0 ||
+        num_pages < 1 || bt_stride < 1)
+        return MSA_ERR_INVALID_ARG;
+    if (k > MSA_MAX_TOPK || batch > MSA_MAX_BATCH || num_pages > (int64_t{1} << 24) ||
+        total_q > (1 << 28))
+        return MSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(n_sink) + n_window > k)
+        return MSA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(kcache_pool) & 15) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255))
+        return MSA_ERR_INVALID_ARG;
+    const int64_t bs_stride = blocks_for(max_model_len);
+    const size_t scores_bytes = static_cast<size_t>(total_q) * kHeads * bs_stride * sizeof(float);
+    const size_t need = kHeaderBytes + (out_block_scores ? 0 : scores_bytes);
+    if (workspace_bytes < need)
+        return MSA_ERR_WORKSPACE_TOO_SMALL;
+    if (total_q == 0)
+        return MSA_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return MSA_ERR_CUDA;
+    const int sms = device_sms(dev);
+    if (sms <= 0)
+        return MSA_ERR_CUDA;
+    static std::atomic<bool> attr_done[kMaxDevices];
+    if (dev >= 0 && dev < kMaxDevices && !attr_done[dev].load(std::memory_order_acquire)) {
+        if (cudaFuncSetAttribute(tc_prefill_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kTcSmemBytes)) != cudaSuccess)
+            return MSA_ERR_CUDA;
+        attr_done[dev].store(true, std::memory_order_release);
+    }
+    TcParams p;
+    std::memset(&p, 0, sizeof p);
+    if (!make_rows_map(&p.kmap, kcache_pool, num_pages * kPage) ||
+        !make_rows_map(&p.qmap, q, static_cast<int64_t>(total_q) * kHeads))
+        return MSA_ERR_CUDA;
+    WorkspaceHeader *hdr = static_cast<WorkspaceHeader *>(workspace);
+    p.cu_q = cu_seqlens_q;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.scores = out_block_scores ? out_block_scores
+                                : reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kHeaderBytes);
+    p.fault = &hdr->fault;
+    p.bt_stride = bt_stride;
+    p.bs_stride = bs_stride;
+    p.num_pages = num_pages;
+    p.batch = batch;
+    p.seq_limit = static_cast<int>(bt_stride * kPage < max_model_len ? bt_stride * kPage : max_model_len);
+    p.total_q = total_q;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(sms)), dim3(kTcThreads),
+                                        kTcSmemBytes, st, attr);
+    if (cudaLaunchKernelEx(&cfg, tc_prefill_score_kernel, p) != cudaSuccess)
+        return MSA_ERR_CUDA;
+    const int64_t rows = static_cast<int64_t>(total_q) * kHeads;
+    cudaLaunchAttribute attr2[1];
+    cudaLaunchConfig_t cfg2 = pdl_config(dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), 0,
+                                         st, attr2);
+    cudaError_t e = kmax_for(k) == 16
+                        ? cudaLaunchKernelEx(&cfg2, rows_topk_kernel<16>, static_cast<const float *>(p.scores),
+                                             bs_stride, cu_seqlens_q, seq_lens, batch, total_q,
+                                             p.seq_limit, k, n_sink, n_window, out_ids, out_scores)
+                        : cudaLaunchKernelEx(&cfg2, rows_topk_kernel<32>, static_cast<const float *>(p.scores),
+                                             bs_stride, cu_seqlens_q, seq_lens, batch, total_q,
+                                             p.seq_limit, k, n_sink, n_window, out_ids, out_scores);
+    return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
