@@ -7,6 +7,7 @@ shuffled index-K pool.  The metric is index-K GB/s (algorithmic bytes: every
 valid token's 128 bf16 values once) with us/call beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --path prefill   # prefill scoring (tensor cores), its own line
 
 Under torchrun (N > 1) every rank runs its own replica of the batch on its
 own GPU; there is no data-path collective (weak scaling), only a barrier and
@@ -34,7 +35,10 @@ METRIC = "indexer decode µs/call and index-K HBM GB/s (B=32, 128K ctx) vs GB300
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = {"bf16": os.path.join(ROOT, "profiles", "score_kernel_long_context.md"),
-                   "fp8": os.path.join(ROOT, "profiles", "score_kernel_fp8_long_context.md")}
+                   "fp8": os.path.join(ROOT, "profiles", "score_kernel_fp8_long_context.md"),
+                   "prefill": os.path.join(ROOT, "profiles", "prefill_kernel_chunked_128k.md")}
+PREFILL_METRIC = "prefill index-score TFLOP/s (4 x 2048 new tokens at 128K ctx) vs GB300 bf16 peak"
+PREFILL_PAIRS = [(2048, 131072)] * 4  # (new tokens, tokens) per request
 CSRC = os.path.join(ROOT, "sparse_attention_decode_gb300", "csrc")
 
 
@@ -48,6 +52,8 @@ def parse_args(argv=None):
                     help="requests per step (32 is the headline workload; smaller only for profiling)")
     ap.add_argument("--cache", choices=["bf16", "fp8"], default="bf16",
                     help="index-K cache format (bf16 is the headline; fp8 = E4M3 + per-token scale)")
+    ap.add_argument("--path", choices=["decode", "prefill"], default="decode",
+                    help="decode (the headline) or prefill scoring (4 x 2048 new tokens at 128K)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args(argv)
@@ -97,6 +103,16 @@ def max_over_ranks(dist, value: float, device=None) -> float:
 # helpers
 # ----------------------------------------------------------------------------
 
+def measured_bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        return v, "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
+    except Exception:
+        return 1900.0, "fallback (no MEASURED_PEAKS.json)"
+
+
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -112,10 +128,14 @@ DECODE_SOURCES = ("host_util.cuh", "keys.cuh", "layout.cuh", "msa_indexer.cu", "
                   os.path.join("..", "..", "include", "msa_indexer.h"))
 
 
-def kernel_source_hash() -> str:
-    """Hash of the decode kernels' sources: a profile taken at another hash is stale."""
+PREFILL_SOURCES = ("host_util.cuh", "keys.cuh", "layout.cuh", "prefill.cu", "ptx.cuh",
+                   "tcgen05.cuh", os.path.join("..", "..", "include", "msa_indexer.h"))
+
+
+def kernel_source_hash(path: str = "decode") -> str:
+    """Hash of a path's kernel sources: a profile taken at another hash is stale."""
     h = hashlib.sha256()
-    for name in DECODE_SOURCES:
+    for name in (PREFILL_SOURCES if path == "prefill" else DECODE_SOURCES):
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -130,7 +150,8 @@ def profiled_traffic(batch: int, cache: str = "bf16"):
         return None
     m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
     m_bytes = re.search(r"dram_bytes_per_launch_full_batch:\s*([0-9]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    path = "prefill" if cache == "prefill" else "decode"
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(path):
         return None
     return int(m_bytes.group(1)) * batch // 32
 
@@ -391,6 +412,180 @@ def run_ours(args):
     return line
 
 
+def prefill_workload():
+    """Chunked prefill: 4 requests, each appending 2048 tokens to a 131072-token context."""
+    import numpy as np
+    import workloads as wl
+    lens = [L for _, L in PREFILL_PAIRS]
+    w = wl.random_workload(lens, seed=7, q_scale=1 / np.sqrt(128), max_model_len=max(lens),
+                           name="chunked_prefill")
+    total = sum(n for n, _ in PREFILL_PAIRS)
+    rng = np.random.default_rng(8)
+    q = wl.f32_to_bf16_bits(rng.standard_normal((total, 4, 128), dtype=np.float32)
+                            / np.float32(np.sqrt(128)))
+    cu = np.zeros(len(PREFILL_PAIRS) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum([n for n, _ in PREFILL_PAIRS])
+    return w, q, cu
+
+
+def prefill_flops(pairs=PREFILL_PAIRS):
+    """Useful flops: every new token's 4 heads against every key it sees, 128 MACs each."""
+    vis = sum(n * (L - n) + n * (n + 1) // 2 for n, L in pairs)
+    return vis * 4 * 128 * 2
+
+
+def run_prefill_bench(args):
+    import numpy as np
+    import torch
+
+    import sparse_attention_decode_gb300 as msa
+
+    world, rank, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dist = init_dist(world, "nccl")
+    msa.load()
+    w, q_bits, cu_np = prefill_workload()
+    total, k, L = q_bits.shape[0], w.k, w.max_model_len
+    flops = prefill_flops()
+    q = torch.from_numpy(q_bits.view(np.int16)).view(torch.bfloat16).to(device)
+    pool = torch.from_numpy(w.pool.view(np.int16)).view(torch.bfloat16).to(device)
+    bt = torch.from_numpy(w.block_table).to(device)
+    seq = torch.from_numpy(w.seq_lens).to(device)
+    cu = torch.from_numpy(cu_np).to(device)
+    ids = torch.empty((total, 4, k), dtype=torch.int32, device=device)
+    sc = torch.empty((total, 4, k), dtype=torch.float32, device=device)
+    ws = torch.zeros(msa.msa_indexer_prefill_workspace_bytes(total, L), dtype=torch.uint8,
+                     device=device)
+    blk = torch.empty((total, 4, (L + 127) // 128), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(st):
+        msa.msa_indexer_prefill(q, cu, pool, bt, seq, k, w.n_sink, w.n_window, ids, sc, ws,
+                                max_model_len=L, stream=st)
+
+    def score_only(st):
+        msa.msa_indexer_prefill_score(q, cu, pool, bt, seq, blk, ws, max_model_len=L, stream=st)
+
+    side = torch.cuda.Stream(device)
+
+    def capture(fn, calls):
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(max(args.warmup, 3)):
+                fn(side)
+        stream.wait_stream(side)
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(calls):
+                fn(side)
+        torch.cuda.synchronize(device)
+        return g
+
+    g_step = capture(step, args.steps)
+    g_score = capture(score_only, args.steps)
+    assert msa.msa_indexer_get_error(ws, stream=stream) == 0
+
+    uuid = getattr(torch.cuda.get_device_properties(device), "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else None)
+    sampler.start()
+    t_soak = time.time()
+    while time.time() - t_soak < 1.5:  # keep the GPU busy so the clock samples see load
+        g_step.replay()
+        torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    start.record(stream)
+    g_step.replay()  # K prefill steps (score + top-k kernels)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    ms = max_over_ranks(dist, start.elapsed_time(end) / args.steps, device)
+    # the dominant kernel alone, same inputs, same stream, K launches
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    g_score.replay()
+    s1.record(stream)
+    torch.cuda.synchronize(device)
+    clocks = sampler.stop()
+    score_ms = s0.elapsed_time(s1) / args.steps
+    assert msa.msa_indexer_get_error(ws, stream=stream) == 0
+
+    e2e = None
+    if not args.no_e2e:
+        h_q = torch.from_numpy(q_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_bt = torch.from_numpy(w.block_table).pin_memory()
+        h_seq = torch.from_numpy(w.seq_lens).pin_memory()
+        h_cu = torch.from_numpy(cu_np).pin_memory()
+        h_ids = torch.empty((total, 4, k), dtype=torch.int32).pin_memory()
+        h_sc = torch.empty((total, 4, k), dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_bt, h_seq, h_cu))
+        d2h = sum(t.numel() * t.element_size() for t in (h_ids, h_sc))
+
+        def e2e_step():
+            q.copy_(h_q, non_blocking=True)
+            bt.copy_(h_bt, non_blocking=True)
+            seq.copy_(h_seq, non_blocking=True)
+            cu.copy_(h_cu, non_blocking=True)
+            step(stream)
+            h_ids.copy_(ids, non_blocking=True)
+            h_sc.copy_(sc, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(dist, device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(dist, device)
+        e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, device)
+        e2e = {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "us_per_call": round(e2e_ms * 1e3, 2), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+    if rank != 0:
+        return None
+    peak, peak_src = measured_bf16_peak()
+    achieved = flops / (score_ms * 1e-3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC,
+        "value": round(world * flops / (ms * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "us_per_call": round(ms * 1e3, 2),
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 (fp32 accumulate in TMEM)",
+        "data": "synthetic",
+        "config": {
+            "workload": "chunked_prefill: 4 requests x 2048 new tokens at 131072 tokens, 4 index "
+                        "heads, d=128, 128-token pages, k=16, n_sink=1, n_window=2",
+            "total_q": total, "useful_flops_per_step": flops, "parallelism": f"replicas x{world}",
+            "timing": "one CUDA graph of K consecutive prefill calls (score + top-k kernels), "
+                      "CUDA events on the stream",
+            "l2": "index-K pool 128 MiB + 128 MiB of block scores written per step vs 129 MB L2; "
+                  "no flush",
+        },
+        "roofline": {
+            "bound": "tensor", "kernel": "tc_prefill_score_kernel",
+            "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src,
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(32, "prefill"), "score_us": round(score_ms * 1e3, 2),
+        },
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = prefill_cpu_baseline(w, q_bits)
+    return line
+
+
 # ----------------------------------------------------------------------------
 # the CPU oracle (baseline leg and reference arm)
 # ----------------------------------------------------------------------------
@@ -421,6 +616,35 @@ def cpu_baseline(w, bytes_per_step, budget_s: float = 12.0):
             "kind": "oracle",
             "sample": f"first {rows} of {w.batch} requests of the same batch "
                       f"({nbytes} index-K bytes), {len(times)} passes, median"}
+
+
+def prefill_cpu_baseline(w, q_bits, budget_s: float = 12.0):
+    """The oracle's prefill scoring on the host cores, over the first tokens of request 0."""
+    import numpy as np
+    import oracle
+    orc = oracle.load()
+    n0, L0 = PREFILL_PAIRS[0]
+
+    def one(rows):
+        cu = np.array([0, rows], dtype=np.int32)
+        seq = np.array([L0 - n0 + rows], dtype=np.int32)
+        t0 = time.perf_counter()
+        orc.run_prefill(q_bits[:rows], cu, w.pool, w.block_table[:1], seq, w.k, w.n_sink,
+                        w.n_window)
+        return time.perf_counter() - t0, prefill_flops([(rows, L0 - n0 + rows)])
+
+    dt, _ = one(1)
+    rows = max(1, min(n0, int(budget_s / 3 / max(dt, 1e-6))))
+    times, fl = [], 0
+    t_all = time.perf_counter()
+    while len(times) < 3 and time.perf_counter() - t_all < budget_s:
+        dt, fl = one(rows)
+        times.append(dt)
+    med = statistics.median(times)
+    return {"value": round(fl / med / 1e12, 6), "unit": "TFLOP/s", "cores": orc.num_threads(),
+            "kind": "oracle",
+            "sample": f"first {rows} of request 0's {n0} new tokens ({fl} useful flops), "
+                      f"{len(times)} passes, median"}
 
 
 def run_reference(args):
@@ -461,7 +685,12 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
-    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.impl == "reference":
+        line = run_reference(args)
+    elif args.path == "prefill":
+        line = run_prefill_bench(args)
+    else:
+        line = run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

@@ -280,6 +280,19 @@ msa_status msa_indexer_expand_pages(const int32_t *ids, int batch, int k, const 
  */
 size_t msa_indexer_prefill_workspace_bytes(int max_total_q, int max_model_len);
 
+/*
+ * The block-score half of msa_indexer_prefill: writes out_block_scores
+ * (required, fp32 [total_q, 4, ceil(max_model_len/128)], each token's
+ * visible blocks only) and nothing else.  The workspace needs only its
+ * 256-byte header (the fault word).  One kernel.
+ */
+msa_status msa_indexer_prefill_score(const void *q, const int32_t *cu_seqlens_q, int total_q,
+                                     const void *kcache_pool, int64_t num_pages,
+                                     const int32_t *block_table, int64_t bt_stride,
+                                     const int32_t *seq_lens, int batch, int max_model_len,
+                                     float *out_block_scores, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
 msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqlens_q, int total_q,
                                const void *kcache_pool, int64_t num_pages,
                                const int32_t *block_table, int64_t bt_stride,

@@ -30,6 +30,7 @@ from ._binding import (  # noqa: F401
     msa_indexer_decode_fp8,
     msa_indexer_decode_mq,
     msa_indexer_prefill,
+    msa_indexer_prefill_score,
     msa_indexer_prefill_workspace_bytes,
     msa_indexer_workspace_bytes_mq,
     msa_indexer_score_fp8,

@@ -46,6 +46,7 @@ EXPORTED = (
     "msa_indexer_decode_mq",
     "msa_indexer_workspace_bytes_mq",
     "msa_indexer_prefill",
+    "msa_indexer_prefill_score",
     "msa_indexer_prefill_workspace_bytes",
 )
 
@@ -103,6 +104,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.msa_indexer_prefill.argtypes = [P, P, c_int, P, c_i64, P, c_i64, P, c_int, c_int, c_int,
                                         c_int, c_int, P, P, P, P, c_size, P]
     lib.msa_indexer_prefill.restype = c_int
+    lib.msa_indexer_prefill_score.argtypes = [P, P, c_int, P, c_i64, P, c_i64, P, c_int, c_int, P,
+                                              P, c_size, P]
+    lib.msa_indexer_prefill_score.restype = c_int
     lib.msa_status_string.argtypes = [c_int]
     lib.msa_status_string.restype = ctypes.c_char_p
     if path is None:
@@ -302,6 +306,24 @@ def msa_indexer_prefill(q, cu_seqlens_q, kcache_pool, block_table, seq_lens, k: 
         max_model_len, k, n_sink, n_window, _ptr(out_ids), _ptr(out_scores), _ptr(out_block_scores),
         _ptr(workspace), int(workspace.numel() * workspace.element_size()), _stream_ptr(stream))
     _check(st, "msa_indexer_prefill")
+
+
+def msa_indexer_prefill_score(q, cu_seqlens_q, kcache_pool, block_table, seq_lens, out_block_scores,
+                              workspace, *, max_model_len: int, stream=None) -> None:
+    """msa_indexer_prefill_score(): block scores only, fp32 [total_q, 4, ceil(max_model_len/128)]."""
+    import torch
+    assert q.dtype == torch.bfloat16 and q.is_contiguous() and tuple(q.shape[1:]) == (4, 128)
+    assert cu_seqlens_q.dtype == torch.int32 and cu_seqlens_q.is_contiguous()
+    assert kcache_pool.dtype == torch.bfloat16 and kcache_pool.is_contiguous()
+    assert block_table.dtype == torch.int32 and block_table.stride(1) == 1
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+    assert out_block_scores.dtype == torch.float32 and out_block_scores.is_contiguous()
+    st = load().msa_indexer_prefill_score(
+        _ptr(q), _ptr(cu_seqlens_q), int(q.shape[0]), _ptr(kcache_pool), int(kcache_pool.shape[0]),
+        _ptr(block_table), int(block_table.stride(0)), _ptr(seq_lens), int(seq_lens.shape[0]),
+        max_model_len, _ptr(out_block_scores), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _stream_ptr(stream))
+    _check(st, "msa_indexer_prefill_score")
 
 
 def msa_indexer_get_error(workspace, *, stream=None) -> int:

@@ -526,7 +526,12 @@ __device__ __forceinline__ uint64_t sort32_desc(uint64_t v, int lane)
     return v;
 }
 
-// One warp per (token, head) row of the prefill: pins and top-k of its blocks.
+// One warp per (token, head) row of the prefill: pins and top-k of its
+// blocks.  The row's block scores are read 32 at a time.  The first 32 are
+// sorted into the running list; afterwards only keys above the list's last
+// entry can enter it: when few do they are inserted one by one, when many do
+// the 32 are sorted and merged.  Either way the list stays the descending
+// top-KMAX of the keys seen so far.
 template <int KMAX>
 __global__ void __launch_bounds__(256) rows_topk_kernel(const float *scores, int64_t bs_stride,
                                                         const int32_t *cu_q, const int32_t *seq_lens,
@@ -555,21 +560,35 @@ __global__ void __launch_bounds__(256) rows_topk_kernel(const float *scores, int
     if (r.ok && r.c0 <= tok && tok < r.c0 + r.n)
         nb = (r.len - r.n + (tok - r.c0)) / kPage + 1;
     const float *srow = scores + row * bs_stride;
+    const float neg_inf = -__int_as_float(0x7f800000);
     uint64_t run = 0;
+    float s_next = (lane < nb) ? srow[lane] : neg_inf;
     for (int c0 = 0; c0 < nb; c0 += 32) {
         const int j = c0 + lane;
+        const float s = s_next;
+        if (c0 + 32 < nb)  // the next chunk's load is in flight while this one is merged
+            s_next = (j + 32 < nb) ? srow[j + 32] : neg_inf;
         uint64_t key = 0;
-        if (j < nb) {
-            const float s = srow[j];
-            // -inf marks a block whose page was out of range: never selected
-            if (s != -__int_as_float(0x7f800000))
-                key = pack_key(s, j, j < n_sink || j >= nb - n_window);
+        // -inf marks a block whose page was out of range: never selected
+        if (j < nb && s != neg_inf)
+            key = pack_key(s, j, j < n_sink || j >= nb - n_window);
+        const uint64_t thr = __shfl_sync(0xffffffffu, run, KMAX - 1);
+        unsigned m = __ballot_sync(0xffffffffu, key > thr);
+        if (c0 == 0 || __popc(m) > 6) {
+            const uint64_t sorted = sort32_desc(key, lane);
+            if constexpr (KMAX == 16)
+                run = merge_top<16>(run, __shfl_sync(0xffffffffu, sorted, (15 - lane) & 31), lane);
+            else
+                run = merge_top<32>(run, __shfl_sync(0xffffffffu, sorted, 31 - lane), lane);
+            continue;
         }
-        const uint64_t sorted = sort32_desc(key, lane);
-        if constexpr (KMAX == 16)
-            run = merge_top<16>(run, __shfl_sync(0xffffffffu, sorted, (15 - lane) & 31), lane);
-        else
-            run = merge_top<32>(run, __shfl_sync(0xffffffffu, sorted, 31 - lane), lane);
+        while (m) {
+            const int l = __ffs(m) - 1;
+            run = insert_desc<KMAX>(run, __shfl_sync(0xffffffffu, key, l), lane);
+            const uint64_t t2 = __shfl_sync(0xffffffffu, run, KMAX - 1);
+            m &= ~(1u << l);
+            m &= __ballot_sync(0xffffffffu, key > t2);
+        }
     }
     if (lane < k) {
         int id;
@@ -608,25 +627,21 @@ extern "C" size_t msa_indexer_prefill_workspace_bytes(int max_total_q, int max_m
                               static_cast<size_t>(blocks_for(max_model_len)) * sizeof(float);
 }
 
-extern "C" msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqlens_q, int total_q,
-                                          const void *kcache_pool, int64_t num_pages,
-                                          const int32_t *block_table, int64_t bt_stride,
-                                          const int32_t *seq_lens, int batch, int max_model_len,
-                                          int k, int n_sink, int n_window, int32_t *out_ids,
-                                          float *out_scores, float *out_block_scores,
-                                          void *workspace, size_t workspace_bytes, void *stream)
+// Checks the arguments and launches the score kernel; fills *pp (the block
+// score buffer it writes: the caller's, else the workspace's).
+static msa_status prefill_score_launch(const void *q, const int32_t *cu_seqlens_q, int total_q,
+                                       const void *kcache_pool, int64_t num_pages,
+                                       const int32_t *block_table, int64_t bt_stride,
+                                       const int32_t *seq_lens, int batch, int max_model_len,
+                                       float *out_block_scores, void *workspace,
+                                       size_t workspace_bytes, cudaStream_t st, TcParams *pp)
 {
-    if (!q || !cu_seqlens_q || !kcache_pool || !block_table || !seq_lens || !out_ids ||
-        !out_scores || !workspace)
+    if (!q || !cu_seqlens_q || !kcache_pool || !block_table || !seq_lens || !workspace)
         return MSA_ERR_INVALID_ARG;
-    if (total_q < 0 || batch < 1 || max_model_len < 1 || k < 1 || n_sink < 0 || n_window < 0 ||
-        num_pages < 1 || bt_stride < 1)
+    if (total_q < 0 || batch < 1 || max_model_len < 1 || num_pages < 1 || bt_stride < 1)
         return MSA_ERR_INVALID_ARG;
-    if (k > MSA_MAX_TOPK || batch > MSA_MAX_BATCH || num_pages > (int64_t{1} << 24) ||
-        total_q > (1 << 28))
+    if (batch > MSA_MAX_BATCH || num_pages > (int64_t{1} << 24) || total_q > (1 << 28))
         return MSA_ERR_UNSUPPORTED;
-    if (static_cast<int64_t>(n_sink) + n_window > k)
-        return MSA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(kcache_pool) & 15) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255))
         return MSA_ERR_INVALID_ARG;
@@ -635,6 +650,20 @@ extern "C" msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqle
     const size_t need = kHeaderBytes + (out_block_scores ? 0 : scores_bytes);
     if (workspace_bytes < need)
         return MSA_ERR_WORKSPACE_TOO_SMALL;
+    TcParams &p = *pp;
+    std::memset(&p, 0, sizeof p);
+    p.cu_q = cu_seqlens_q;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.scores = out_block_scores ? out_block_scores
+                                : reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kHeaderBytes);
+    p.fault = &static_cast<WorkspaceHeader *>(workspace)->fault;
+    p.bt_stride = bt_stride;
+    p.bs_stride = bs_stride;
+    p.num_pages = num_pages;
+    p.batch = batch;
+    p.seq_limit = static_cast<int>(bt_stride * kPage < max_model_len ? bt_stride * kPage : max_model_len);
+    p.total_q = total_q;
     if (total_q == 0)
         return MSA_OK;
     int dev = 0;
@@ -650,40 +679,65 @@ extern "C" msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqle
             return MSA_ERR_CUDA;
         attr_done[dev].store(true, std::memory_order_release);
     }
-    TcParams p;
-    std::memset(&p, 0, sizeof p);
     if (!make_rows_map(&p.kmap, kcache_pool, num_pages * kPage) ||
         !make_rows_map(&p.qmap, q, static_cast<int64_t>(total_q) * kHeads))
         return MSA_ERR_CUDA;
-    WorkspaceHeader *hdr = static_cast<WorkspaceHeader *>(workspace);
-    p.cu_q = cu_seqlens_q;
-    p.block_table = block_table;
-    p.seq_lens = seq_lens;
-    p.scores = out_block_scores ? out_block_scores
-                                : reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kHeaderBytes);
-    p.fault = &hdr->fault;
-    p.bt_stride = bt_stride;
-    p.bs_stride = bs_stride;
-    p.num_pages = num_pages;
-    p.batch = batch;
-    p.seq_limit = static_cast<int>(bt_stride * kPage < max_model_len ? bt_stride * kPage : max_model_len);
-    p.total_q = total_q;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(sms)), dim3(kTcThreads),
                                         kTcSmemBytes, st, attr);
-    if (cudaLaunchKernelEx(&cfg, tc_prefill_score_kernel, p) != cudaSuccess)
-        return MSA_ERR_CUDA;
+    return cudaLaunchKernelEx(&cfg, tc_prefill_score_kernel, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+extern "C" msa_status msa_indexer_prefill_score(const void *q, const int32_t *cu_seqlens_q,
+                                                int total_q, const void *kcache_pool,
+                                                int64_t num_pages, const int32_t *block_table,
+                                                int64_t bt_stride, const int32_t *seq_lens,
+                                                int batch, int max_model_len,
+                                                float *out_block_scores, void *workspace,
+                                                size_t workspace_bytes, void *stream)
+{
+    if (!out_block_scores)
+        return MSA_ERR_INVALID_ARG;
+    TcParams p;
+    return prefill_score_launch(q, cu_seqlens_q, total_q, kcache_pool, num_pages, block_table,
+                                bt_stride, seq_lens, batch, max_model_len, out_block_scores,
+                                workspace, workspace_bytes, static_cast<cudaStream_t>(stream), &p);
+}
+
+extern "C" msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqlens_q, int total_q,
+                                          const void *kcache_pool, int64_t num_pages,
+                                          const int32_t *block_table, int64_t bt_stride,
+                                          const int32_t *seq_lens, int batch, int max_model_len,
+                                          int k, int n_sink, int n_window, int32_t *out_ids,
+                                          float *out_scores, float *out_block_scores,
+                                          void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!out_ids || !out_scores)
+        return MSA_ERR_INVALID_ARG;
+    if (k < 1 || n_sink < 0 || n_window < 0)
+        return MSA_ERR_INVALID_ARG;
+    if (k > MSA_MAX_TOPK)
+        return MSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(n_sink) + n_window > k)
+        return MSA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    TcParams p;
+    const msa_status s = prefill_score_launch(q, cu_seqlens_q, total_q, kcache_pool, num_pages,
+                                              block_table, bt_stride, seq_lens, batch,
+                                              max_model_len, out_block_scores, workspace,
+                                              workspace_bytes, st, &p);
+    if (s != MSA_OK || total_q == 0)
+        return s;
     const int64_t rows = static_cast<int64_t>(total_q) * kHeads;
     cudaLaunchAttribute attr2[1];
     cudaLaunchConfig_t cfg2 = pdl_config(dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), 0,
                                          st, attr2);
     cudaError_t e = kmax_for(k) == 16
                         ? cudaLaunchKernelEx(&cfg2, rows_topk_kernel<16>, static_cast<const float *>(p.scores),
-                                             bs_stride, cu_seqlens_q, seq_lens, batch, total_q,
+                                             p.bs_stride, cu_seqlens_q, seq_lens, batch, total_q,
                                              p.seq_limit, k, n_sink, n_window, out_ids, out_scores)
                         : cudaLaunchKernelEx(&cfg2, rows_topk_kernel<32>, static_cast<const float *>(p.scores),
-                                             bs_stride, cu_seqlens_q, seq_lens, batch, total_q,
+                                             p.bs_stride, cu_seqlens_q, seq_lens, batch, total_q,
                                              p.seq_limit, k, n_sink, n_window, out_ids, out_scores);
     return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }

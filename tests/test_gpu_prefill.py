@@ -187,3 +187,21 @@ def test_prefill_outputs_do_not_spill(msa):
     torch.cuda.synchronize()
     assert (ids[total * 4 * k:] == -7).all() and (sc[total * 4 * k:] == 7.0).all()
     assert (ws[n:] == 0xA5).all()
+
+
+def test_prefill_score_only_entry_matches(msa):
+    """msa_indexer_prefill_score writes the same block scores as msa_indexer_prefill."""
+    import torch
+    w, q, cu = prefill_case(MIXED, seed=280, max_model_len=8192)
+    ids, sc, blk, fault, _ = run_prefill(msa, w, q, cu)
+    assert fault == 0
+    total = q.shape[0]
+    d = parity.to_device(w)
+    out = torch.full((total, 4, (w.max_model_len + 127) // 128), float("nan"), dtype=torch.float32,
+                     device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    msa.msa_indexer_prefill_score(torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).cuda(),
+                                  torch.from_numpy(cu).cuda(), d[1], d[2], d[3], out, ws,
+                                  max_model_len=w.max_model_len)
+    assert msa.msa_indexer_get_error(ws) == 0
+    np.testing.assert_array_equal(out.cpu().numpy(), blk)
