@@ -23,8 +23,8 @@
 //   warps 2-9  read their rows' 128 accumulators per page from TMEM and
 //              write the masked block max (keys <= the row's position).
 //
-// rows_topk_kernel: one warp per (token, head) row: pins and top-k over the
-// row's block scores (32 keys sorted at a time, merged into a running list).
+// rows_topk_kernel (rows_topk.cuh): one warp per (token, head) row: pins and
+// top-k over the row's block scores.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -510,94 +510,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
     }
 }
 
-// Sorts 32 keys (one per lane) into descending order across the warp.
-__device__ __forceinline__ uint64_t sort32_desc(uint64_t v, int lane)
-{
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int j = size >> 1; j > 0; j >>= 1) {
-            const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
-            const bool desc = (lane & size) == 0;  // always true at size 32
-            const bool low = (lane & j) == 0;
-            v = (low == desc) ? umax64(v, o) : umin64(v, o);
-        }
-    }
-    return v;
-}
+}  // namespace msa
 
-// One warp per (token, head) row of the prefill: pins and top-k of its
-// blocks.  The row's block scores are read 32 at a time.  The first 32 are
-// sorted into the running list; afterwards only keys above the list's last
-// entry can enter it: when few do they are inserted one by one, when many do
-// the 32 are sorted and merged.  Either way the list stays the descending
-// top-KMAX of the keys seen so far.
-template <int KMAX>
-__global__ void __launch_bounds__(256) rows_topk_kernel(const float *scores, int64_t bs_stride,
-                                                        const int32_t *cu_q, const int32_t *seq_lens,
-                                                        int batch, int total_q, int seq_limit, int k,
-                                                        int n_sink, int n_window, int32_t *out_ids,
-                                                        float *out_scores)
-{
-    griddep_wait();
-    griddep_launch_dependents();
-    const int lane = threadIdx.x & 31;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // (token, head)
-    if (row >= static_cast<int64_t>(total_q) * kHeads)
-        return;
-    const int tok = static_cast<int>(row / kHeads);
-    // the request of this token: the last b with cu_q[b] <= tok
-    int lo = 0, hi = batch - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (cu_q[mid] <= tok)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    const Req r = req_info(cu_q, seq_lens, total_q, seq_limit, lo);
-    int nb = 0;
-    if (r.ok && r.c0 <= tok && tok < r.c0 + r.n)
-        nb = (r.len - r.n + (tok - r.c0)) / kPage + 1;
-    const float *srow = scores + row * bs_stride;
-    const float neg_inf = -__int_as_float(0x7f800000);
-    uint64_t run = 0;
-    float s_next = (lane < nb) ? srow[lane] : neg_inf;
-    for (int c0 = 0; c0 < nb; c0 += 32) {
-        const int j = c0 + lane;
-        const float s = s_next;
-        if (c0 + 32 < nb)  // the next chunk's load is in flight while this one is merged
-            s_next = (j + 32 < nb) ? srow[j + 32] : neg_inf;
-        uint64_t key = 0;
-        // -inf marks a block whose page was out of range: never selected
-        if (j < nb && s != neg_inf)
-            key = pack_key(s, j, j < n_sink || j >= nb - n_window);
-        const uint64_t thr = __shfl_sync(0xffffffffu, run, KMAX - 1);
-        unsigned m = __ballot_sync(0xffffffffu, key > thr);
-        if (c0 == 0 || __popc(m) > 6) {
-            const uint64_t sorted = sort32_desc(key, lane);
-            if constexpr (KMAX == 16)
-                run = merge_top<16>(run, __shfl_sync(0xffffffffu, sorted, (15 - lane) & 31), lane);
-            else
-                run = merge_top<32>(run, __shfl_sync(0xffffffffu, sorted, 31 - lane), lane);
-            continue;
-        }
-        while (m) {
-            const int l = __ffs(m) - 1;
-            run = insert_desc<KMAX>(run, __shfl_sync(0xffffffffu, key, l), lane);
-            const uint64_t t2 = __shfl_sync(0xffffffffu, run, KMAX - 1);
-            m &= ~(1u << l);
-            m &= __ballot_sync(0xffffffffu, key > t2);
-        }
-    }
-    if (lane < k) {
-        int id;
-        float score;
-        unpack_key(run, id, score);
-        out_ids[row * k + lane] = id;
-        out_scores[row * k + lane] = score;
-    }
-}
+#include "rows_topk.cuh"
+
+namespace msa {
 
 // 2-D bf16 tensor map over `rows` rows of 128 elements (256 B), 64x128 boxes,
 // 128-byte swizzle: two boxes fill one 128x128 operand tile.
@@ -729,11 +646,12 @@ extern "C" msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqle
     if (s != MSA_OK || total_q == 0)
         return s;
     const int64_t rows = static_cast<int64_t>(total_q) * kHeads;
+    const bool k16 = kmax_for(k) == 16;
+    const int per = k16 ? rows_per_cta<16>() : rows_per_cta<32>();
     cudaLaunchAttribute attr2[1];
-    cudaLaunchConfig_t cfg2 = pdl_config(dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), 0,
-                                         st, attr2);
-    cudaError_t e = kmax_for(k) == 16
-                        ? cudaLaunchKernelEx(&cfg2, rows_topk_kernel<16>, static_cast<const float *>(p.scores),
+    cudaLaunchConfig_t cfg2 = pdl_config(dim3(static_cast<unsigned>((rows + per - 1) / per)),
+                                         dim3(32 * per), 0, st, attr2);
+    cudaError_t e = k16 ? cudaLaunchKernelEx(&cfg2, rows_topk_kernel<16>, static_cast<const float *>(p.scores),
                                              p.bs_stride, cu_seqlens_q, seq_lens, batch, total_q,
                                              p.seq_limit, k, n_sink, n_window, out_ids, out_scores)
                         : cudaLaunchKernelEx(&cfg2, rows_topk_kernel<32>, static_cast<const float *>(p.scores),
