@@ -8,6 +8,7 @@ valid token's 128 bf16 values once) with us/call beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --path prefill   # prefill scoring (tensor cores), its own line
+    python bench.py --configs        # every named workload: graph median + oracle timing
 
 Under torchrun (N > 1) every rank runs its own replica of the batch on its
 own GPU; there is no data-path collective (weak scaling), only a barrier and
@@ -54,6 +55,8 @@ def parse_args(argv=None):
                     help="index-K cache format (bf16 is the headline; fp8 = E4M3 + per-token scale)")
     ap.add_argument("--path", choices=["decode", "prefill"], default="decode",
                     help="decode (the headline) or prefill scoring (4 x 2048 new tokens at 128K)")
+    ap.add_argument("--configs", action="store_true",
+                    help="time every named workload (one JSON line each) instead of the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args(argv)
@@ -586,6 +589,112 @@ def run_prefill_bench(args):
     return line
 
 
+CONFIG_NAMES = ("tiny", "decode_point", "long_context", "ragged", "adversarial")
+L2_BYTES = 129 * 10**6
+
+
+def graph_median_us(fn, stream, device, calls=20, replays=50, rounds=7):
+    """10 warm-up calls, a graph of `calls` calls, `replays` replays per round: median us/call."""
+    import torch
+    side = torch.cuda.Stream(device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for i in range(10):
+            fn(side, i)
+    stream.wait_stream(side)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for i in range(calls):
+            fn(side, i)
+    torch.cuda.synchronize(device)
+    per = []
+    for _ in range(rounds):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        per.append(e0.elapsed_time(e1) * 1e3 / (replays * calls))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(calls):
+        fn(stream, i)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    return statistics.median(per), e0.elapsed_time(e1) * 1e3 / calls
+
+
+def run_configs(args):
+    """Every named workload: CUDA-graph median us/call, eager us/call, index-K GB/s,
+    and the oracle on all host cores and on one (one JSON line per config and variant)."""
+    import math
+    import numpy as np
+    import torch
+
+    import oracle
+    import sparse_attention_decode_gb300 as msa
+    import workloads as wl
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    msa.load()
+    stream = torch.cuda.current_stream(device)
+    peak, peak_src = measured_hbm_peak()
+    orc = oracle.load()
+    cores = orc.num_threads()
+    lines = []
+    for name in CONFIG_NAMES:
+        w = wl.make(name)
+        q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).to(device)
+        pool = torch.from_numpy(w.pool.view(np.int16)).view(torch.bfloat16).to(device)
+        bt = torch.from_numpy(w.block_table).to(device)
+        seq = torch.from_numpy(w.seq_lens).to(device)
+        B, k = w.batch, w.k
+        ids = torch.empty((B, 4, k), dtype=torch.int32, device=device)
+        sc = torch.empty((B, 4, k), dtype=torch.float32, device=device)
+        variants = [("auto", 0, [pool])]
+        if name == "adversarial":
+            variants.append(("W=64", 64, [pool]))
+        if name == "decode_point":
+            copies = math.ceil(2 * L2_BYTES / w.index_k_bytes) + 1
+            variants.append((f"L2-cold ({copies} pool copies, rotated)", 0,
+                             [pool] + [pool.clone() for _ in range(copies - 1)]))
+        t0 = time.perf_counter()
+        orc.run(w)
+        oracle_all = time.perf_counter() - t0
+        orc.set_num_threads(1)
+        t0 = time.perf_counter()
+        orc.run(w)
+        oracle_one = time.perf_counter() - t0
+        orc.set_num_threads(cores)
+        for label, split, pools in variants:
+            ws = msa.new_workspace(B, w.max_model_len, k, split, device=device)
+
+            def call(st, i, pools=pools, split=split, ws=ws):
+                msa.msa_indexer_decode(q, pools[i % len(pools)], bt, seq, k, w.n_sink, w.n_window,
+                                       ids, sc, ws, max_model_len=w.max_model_len,
+                                       split_blocks=split, stream=st)
+
+            us, eager = graph_median_us(call, stream, device)
+            assert msa.msa_indexer_get_error(ws, stream=stream) == 0
+            gbs = w.index_k_bytes / (us * 1e-6) / 1e9
+            lines.append({
+                "config": name, "variant": label, "batch": B,
+                "index_k_bytes": w.index_k_bytes, "us_per_call": round(us, 2),
+                "eager_us_per_call": round(eager, 2), "gb_s": round(gbs, 1),
+                "hbm_frac": round(gbs / peak, 4), "hbm_peak": peak, "hbm_peak_source": peak_src,
+                "timing": "graph of 20 calls, 50 replays x 7 rounds, median; eager: 20 calls",
+                "oracle_s": {"all_cores": round(oracle_all, 4), "cores": cores,
+                             "one_core": round(oracle_one, 4)},
+            })
+            del ws
+        del q, pool, bt, seq, variants
+        torch.cuda.empty_cache()
+    return lines
+
+
 # ----------------------------------------------------------------------------
 # the CPU oracle (baseline leg and reference arm)
 # ----------------------------------------------------------------------------
@@ -685,6 +794,10 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.configs and args.impl != "reference":
+        for line in run_configs(args):
+            print(json.dumps(line), flush=True)
+        return
     if args.impl == "reference":
         line = run_reference(args)
     elif args.path == "prefill":

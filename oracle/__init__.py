@@ -68,6 +68,8 @@ class Oracle:
         lib.msa_oracle_e4m3_value.restype = ctypes.c_double
         lib.msa_oracle_num_threads.argtypes = []
         lib.msa_oracle_num_threads.restype = c_int
+        lib.msa_oracle_set_num_threads.argtypes = [c_int]
+        lib.msa_oracle_set_num_threads.restype = None
         self.lib = lib
 
     @staticmethod
@@ -76,6 +78,10 @@ class Oracle:
 
     def num_threads(self) -> int:
         return int(self.lib.msa_oracle_num_threads())
+
+    def set_num_threads(self, n: int) -> None:
+        """Host threads for later calls (the arithmetic does not depend on it)."""
+        self.lib.msa_oracle_set_num_threads(int(n))
 
     def block_scores(self, q: np.ndarray, pool: np.ndarray, block_table: np.ndarray,
                      seq_lens: np.ndarray) -> np.ndarray:

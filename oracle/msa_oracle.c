@@ -131,6 +131,17 @@ int msa_oracle_num_threads(void)
 #endif
 }
 
+/* Sets the host threads later calls use (timing on one core or on all). */
+void msa_oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Step 1: the score of every block of every request, for every head. */
 int msa_oracle_block_scores(const uint16_t *q, const uint16_t *pool, int64_t num_pages,
                             const int32_t *bt, int64_t bt_stride, const int32_t *seq_lens,
