@@ -256,6 +256,24 @@ msa_status msa_indexer_expand_pages(const int32_t *ids, int batch, int k, const 
                                     void *stream);
 
 /*
+ * msa_indexer_decode followed by msa_indexer_expand_pages, with the
+ * expansion fused into the merge kernel (the last warp step of each (request,
+ * head) merge), so the selection reaches the page table without a third
+ * launch.  Arguments are those of the two calls; out_pages / out_num_pages
+ * get exactly what msa_indexer_expand_pages would write for this call's
+ * out_ids.  Two kernels.
+ */
+msa_status msa_indexer_decode_pages(const void *q, const void *kcache_pool, int64_t num_pages,
+                                    const int32_t *block_table, int64_t bt_stride,
+                                    const int32_t *seq_lens, int batch, int max_batch,
+                                    int max_model_len, int k, int n_sink, int n_window,
+                                    int32_t *out_ids, float *out_scores, float *out_block_scores,
+                                    void *workspace, size_t workspace_bytes, int split_blocks,
+                                    const int32_t *kv_block_table, int64_t kv_bt_stride,
+                                    int page_tokens, int32_t *out_pages, int32_t *out_num_pages,
+                                    void *stream);
+
+/*
  * Prefill scoring: every new token of every request selects blocks over its
  * own causal prefix (vLLM PR #57832: the prefill branch scores iq[nd:] with
  * cu_seqlens_q and takes the per-token top-k).  Request b's new tokens are

@@ -45,6 +45,7 @@ EXPORTED = (
     "msa_indexer_decode_fp8",
     "msa_indexer_decode_mq",
     "msa_indexer_workspace_bytes_mq",
+    "msa_indexer_decode_pages",
     "msa_indexer_prefill",
     "msa_indexer_prefill_score",
     "msa_indexer_prefill_workspace_bytes",
@@ -104,6 +105,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.msa_indexer_prefill.argtypes = [P, P, c_int, P, c_i64, P, c_i64, P, c_int, c_int, c_int,
                                         c_int, c_int, P, P, P, P, c_size, P]
     lib.msa_indexer_prefill.restype = c_int
+    lib.msa_indexer_decode_pages.argtypes = common + [P, P, P, P, c_size, c_int, P, c_i64, c_int,
+                                                      P, P, P]
+    lib.msa_indexer_decode_pages.restype = c_int
     lib.msa_indexer_prefill_score.argtypes = [P, P, c_int, P, c_i64, P, c_i64, P, c_int, c_int, P,
                                               P, c_size, P]
     lib.msa_indexer_prefill_score.restype = c_int
@@ -257,6 +261,25 @@ def msa_indexer_expand_pages(ids, seq_lens, kv_block_table, out_pages, out_num_p
                                          int(kv_block_table.stride(0)), page_tokens,
                                          _ptr(out_pages), _ptr(out_num_pages), _stream_ptr(stream))
     _check(st, "msa_indexer_expand_pages")
+
+
+def msa_indexer_decode_pages(q, kcache_pool, block_table, seq_lens, k: int, n_sink: int,
+                             n_window: int, out_ids, out_scores, workspace, kv_block_table,
+                             out_pages, out_num_pages, *, max_batch: Optional[int] = None,
+                             max_model_len: int, page_tokens: int = 16, out_block_scores=None,
+                             split_blocks: int = 0, stream=None) -> None:
+    """msa_indexer_decode_pages(): decode with the page expansion fused into the merge."""
+    import torch
+    assert kv_block_table.dtype == torch.int32 and kv_block_table.stride(1) == 1
+    B, num_pages, bt_stride = _shape_args(q, kcache_pool, block_table, seq_lens)
+    st = load().msa_indexer_decode_pages(
+        _ptr(q), _ptr(kcache_pool), num_pages, _ptr(block_table), bt_stride, _ptr(seq_lens), B,
+        B if max_batch is None else max_batch, max_model_len, k, n_sink, n_window, _ptr(out_ids),
+        _ptr(out_scores), _ptr(out_block_scores), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), split_blocks, _ptr(kv_block_table),
+        int(kv_block_table.stride(0)), page_tokens, _ptr(out_pages), _ptr(out_num_pages),
+        _stream_ptr(stream))
+    _check(st, "msa_indexer_decode_pages")
 
 
 def msa_indexer_workspace_bytes_mq(max_batch: int, max_model_len: int, k: int,

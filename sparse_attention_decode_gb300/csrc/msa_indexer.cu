@@ -830,6 +830,64 @@ __global__ void __launch_bounds__(Pipe<F>::kThreads, 1)
         run_consumer<KMAX, F, NQ>(p, part, smem, ctl, prefix, hdr, g_slots);
 }
 
+// Selected blocks -> small KV pages for one (request, head) row, by one full
+// warp: the <= 32 selected ids (`id` of lane < k, else -1) are sorted
+// ascending across the lanes (bitonic), each lane counts the small pages of
+// its block, a lane prefix gives the output offsets, and each lane copies
+// its pages' ids from the KV block table.
+struct ExpandArgs {
+    const int32_t *seq_lens;
+    const int32_t *kv_bt;
+    int64_t kv_stride;
+    int per_block;
+    int page_tokens;
+    int32_t *out_pages;  // null: no expansion
+    int32_t *out_num;
+};
+
+__device__ __forceinline__ void expand_row(const ExpandArgs &ex, int b, size_t row, int k, int id,
+                                           int lane)
+{
+    const int L = ex.seq_lens[b];
+    const int nb = L > 0 ? (L + kPage - 1) / kPage : 0;
+    long long small = L > 0 ? (static_cast<long long>(L) + ex.page_tokens - 1) / ex.page_tokens : 0;
+    if (small > ex.kv_stride)
+        small = ex.kv_stride;
+    int key = (id >= 0 && id < nb) ? id : 0x7fffffff;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int j = size >> 1; j > 0; j >>= 1) {
+            const int other = __shfl_xor_sync(0xffffffffu, key, j);
+            const bool ascending = (lane & size) == 0;
+            const bool low = (lane & j) == 0;
+            key = (low == ascending) ? min(key, other) : max(key, other);
+        }
+    }
+    const bool valid = key != 0x7fffffff;
+    const long long first = valid ? static_cast<long long>(key) * ex.per_block : 0;
+    int count = 0;
+    if (valid && first < small)
+        count = static_cast<int>(min(static_cast<long long>(ex.per_block), small - first));
+    int incl = count;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    const int width = k * ex.per_block;
+    int32_t *out = ex.out_pages + row * width;
+    const int32_t *src = ex.kv_bt + static_cast<size_t>(b) * ex.kv_stride;
+    for (int s = 0; s < count; ++s)
+        out[incl - count + s] = src[first + s];
+    for (int e = total + lane; e < width; e += 32)
+        out[e] = -1;
+    if (lane == 0)
+        ex.out_num[row] = total;
+}
+
 // a7: one CTA per (query column, request): column = 4 * position + head.  The request's chunk lists are staged in
 // shared memory a tile at a time (all loads in flight together), each group of
 // KMAX lanes folds every kGroups-th list of the tile into a running top-KMAX,
@@ -840,7 +898,8 @@ constexpr int kMergeTileKeys = 2048;  // 16 KiB of keys staged per pass
 template <int KMAX>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const uint8_t *ws, int batch, int k,
                                                               int cols, int slot_capacity,
-                                                              int32_t *out_ids, float *out_scores)
+                                                              int32_t *out_ids, float *out_scores,
+                                                              const ExpandArgs ex)
 {
     constexpr int kGroups = kMergeThreads / KMAX;
     constexpr int kTileLists = kMergeTileKeys / KMAX;
@@ -896,69 +955,27 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const uint8_t *ws,
         tree[threadIdx.x] = run;
         __syncthreads();
     }
+    int id = -1;
     if (grp == 0 && rank < k) {
-        int id;
         float score;
         unpack_key(run, id, score);
         const size_t o = (static_cast<size_t>(b) * cols + h) * k + rank;
         out_ids[o] = id;
         out_scores[o] = score;
     }
+    // fused page expansion (decode, one position): warp 0 holds the list
+    if (ex.out_pages != nullptr && threadIdx.x < 32)
+        expand_row(ex, b, static_cast<size_t>(b) * cols + h, k, id, lane);
 }
 
-// Selected blocks -> small KV pages.  One warp per (request, head): the
-// <= 32 selected ids are sorted ascending across the lanes (bitonic), each
-// lane counts the small pages of its block, a lane prefix gives the output
-// offsets, and each lane copies its pages' ids from the KV block table.
-__global__ void __launch_bounds__(128) expand_pages_kernel(const int32_t *ids, int k,
-                                                          const int32_t *seq_lens,
-                                                          const int32_t *kv_bt, int64_t kv_stride,
-                                                          int per_block, int page_tokens,
-                                                          int32_t *out_pages, int32_t *out_num)
+// Selected blocks -> small KV pages, one warp per (request, head).
+__global__ void __launch_bounds__(128) expand_pages_kernel(const int32_t *ids, int k, const ExpandArgs ex)
 {
     griddep_wait();
     griddep_launch_dependents();
     const int b = blockIdx.x, h = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int L = seq_lens[b];
-    const int nb = L > 0 ? (L + kPage - 1) / kPage : 0;
-    long long small = L > 0 ? (static_cast<long long>(L) + page_tokens - 1) / page_tokens : 0;
-    if (small > kv_stride)
-        small = kv_stride;
     const size_t row = static_cast<size_t>(b) * kHeads + h;
-    int id = lane < k ? ids[row * k + lane] : -1;
-    int key = (id >= 0 && id < nb) ? id : 0x7fffffff;
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int j = size >> 1; j > 0; j >>= 1) {
-            const int other = __shfl_xor_sync(0xffffffffu, key, j);
-            const bool ascending = (lane & size) == 0;
-            const bool low = (lane & j) == 0;
-            key = (low == ascending) ? min(key, other) : max(key, other);
-        }
-    }
-    const bool valid = key != 0x7fffffff;
-    long long first = valid ? static_cast<long long>(key) * per_block : 0;
-    int count = 0;
-    if (valid && first < small)
-        count = static_cast<int>(min(static_cast<long long>(per_block), small - first));
-    int incl = count;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o)
-            incl += y;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    const int width = k * per_block;
-    int32_t *out = out_pages + row * width;
-    const int32_t *src = kv_bt + static_cast<size_t>(b) * kv_stride;
-    for (int s = 0; s < count; ++s)
-        out[incl - count + s] = src[first + s];
-    for (int e = total + lane; e < width; e += 32)
-        out[e] = -1;
-    if (lane == 0)
-        out_num[row] = total;
+    expand_row(ex, b, row, k, lane < k ? ids[row * k + lane] : -1, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -1205,7 +1222,8 @@ extern "C" msa_status msa_indexer_score_fp8(const void *q, const void *kcache_fp
 }
 
 static msa_status merge_entry(int batch, int k, int cols, int32_t *out_ids, float *out_scores,
-                              const void *workspace, size_t workspace_bytes, void *stream)
+                              const void *workspace, size_t workspace_bytes, void *stream,
+                              const ExpandArgs &ex = ExpandArgs{})
 {
     if (!out_ids || !out_scores || !workspace || batch < 0 || batch > MSA_MAX_BATCH)
         return MSA_ERR_INVALID_ARG;
@@ -1231,9 +1249,9 @@ static msa_status merge_entry(int batch, int k, int cols, int32_t *out_ids, floa
                                         dim3(kMergeThreads), 0, s, attr);
     cudaError_t e = kmax == 16
                         ? cudaLaunchKernelEx(&cfg, merge_kernel<16>, ws, batch, k, cols, capacity,
-                                             out_ids, out_scores)
+                                             out_ids, out_scores, ex)
                         : cudaLaunchKernelEx(&cfg, merge_kernel<32>, ws, batch, k, cols, capacity,
-                                             out_ids, out_scores);
+                                             out_ids, out_scores, ex);
     return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
@@ -1355,10 +1373,32 @@ extern "C" msa_status msa_indexer_expand_pages(const int32_t *ids, int batch, in
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(batch)), dim3(32 * kHeads), 0, s, attr);
-    const cudaError_t e =
-        cudaLaunchKernelEx(&cfg, expand_pages_kernel, ids, k, seq_lens, kv_block_table,
-                           kv_bt_stride, kPage / page_tokens, page_tokens, out_pages, out_num_pages);
+    ExpandArgs ex{seq_lens, kv_block_table, kv_bt_stride, kPage / page_tokens, page_tokens, out_pages,
+                  out_num_pages};
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, expand_pages_kernel, ids, k, ex);
     return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+extern "C" msa_status msa_indexer_decode_pages(
+    const void *q, const void *kcache_pool, int64_t num_pages, const int32_t *block_table,
+    int64_t bt_stride, const int32_t *seq_lens, int batch, int max_batch, int max_model_len, int k,
+    int n_sink, int n_window, int32_t *out_ids, float *out_scores, float *out_block_scores,
+    void *workspace, size_t workspace_bytes, int split_blocks, const int32_t *kv_block_table,
+    int64_t kv_bt_stride, int page_tokens, int32_t *out_pages, int32_t *out_num_pages, void *stream)
+{
+    if (!out_ids || !out_scores || !kv_block_table || !out_pages || !out_num_pages)
+        return MSA_ERR_INVALID_ARG;
+    if (kv_bt_stride < 1 || page_tokens < 1 || kPage % page_tokens != 0)
+        return MSA_ERR_INVALID_ARG;
+    msa_status st = msa_indexer_score(q, kcache_pool, num_pages, block_table, bt_stride, seq_lens,
+                                      batch, max_batch, max_model_len, k, n_sink, n_window,
+                                      out_block_scores, workspace, workspace_bytes, split_blocks,
+                                      stream);
+    if (st != MSA_OK || batch == 0)
+        return st;
+    const ExpandArgs ex{seq_lens, kv_block_table, kv_bt_stride, kPage / page_tokens, page_tokens,
+                        out_pages, out_num_pages};
+    return merge_entry(batch, k, kHeads, out_ids, out_scores, workspace, workspace_bytes, stream, ex);
 }
 
 extern "C" msa_status msa_indexer_decode_mq(const void *q, int q_len, const void *kcache_pool,

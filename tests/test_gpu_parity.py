@@ -149,3 +149,40 @@ def test_expand_pages_matches_oracle(lib, orc, page_tokens):
         e_pages, e_num = orc.expand_pages(ids, w.seq_lens, kvb, page_tokens)
         np.testing.assert_array_equal(num.cpu().numpy(), e_num)
         np.testing.assert_array_equal(pages.cpu().numpy(), e_pages)
+
+
+@pytest.mark.parametrize("page_tokens", [16, 64])
+def test_decode_pages_fused_matches_separate(lib, orc, page_tokens):
+    """The page expansion fused into the merge equals decode + msa_indexer_expand_pages."""
+    import torch
+    for w in (wl.ragged(), wl.decode_point(), wl.tiny()):
+        q, pool, bt, seq = parity.to_device(w)
+        per = 128 // page_tokens
+        stride = int(w.num_blocks.max()) * per + 5
+        rng = np.random.default_rng(page_tokens + 1)
+        kvb = torch.from_numpy(rng.permutation(w.batch * stride).astype(np.int32)
+                               .reshape(w.batch, stride)).cuda()
+        B, k = w.batch, w.k
+        outs = []
+        for fused in (False, True):
+            ids = torch.full((B, 4, k), -7, dtype=torch.int32, device="cuda")
+            sc = torch.full((B, 4, k), 7.0, dtype=torch.float32, device="cuda")
+            pages = torch.full((B, 4, k * per), -7, dtype=torch.int32, device="cuda")
+            num = torch.full((B, 4), -7, dtype=torch.int32, device="cuda")
+            ws = lib.new_workspace(B, w.max_model_len, k)
+            if fused:
+                lib.msa_indexer_decode_pages(q, pool, bt, seq, k, w.n_sink, w.n_window, ids, sc, ws,
+                                             kvb, pages, num, max_model_len=w.max_model_len,
+                                             page_tokens=page_tokens)
+            else:
+                lib.msa_indexer_decode(q, pool, bt, seq, k, w.n_sink, w.n_window, ids, sc, ws,
+                                       max_model_len=w.max_model_len)
+                lib.msa_indexer_expand_pages(ids, seq, kvb, pages, num, page_tokens=page_tokens)
+            torch.cuda.synchronize()
+            assert lib.msa_indexer_get_error(ws) == 0
+            outs.append([t.cpu().numpy() for t in (ids, sc, pages, num)])
+        for a, b in zip(*outs):
+            np.testing.assert_array_equal(a, b)
+        e_pages, e_num = orc.expand_pages(outs[1][0], w.seq_lens, kvb.cpu().numpy(), page_tokens)
+        np.testing.assert_array_equal(outs[1][2], e_pages)
+        np.testing.assert_array_equal(outs[1][3], e_num)
