@@ -357,6 +357,37 @@ def check_multi_query_one_position_is_decode(orc) -> None:
     np.testing.assert_array_equal(s[:, 0], s1)
 
 
+def check_multi_query_fp8_golden(orc) -> None:
+    """The multi-position fixture on an E4M3 cache: each planted key is coded
+    by hand at twice its value (2, 8, 4, 16 -> E4M3 0x40, 0x50, 0x48, 0x58:
+    sign 0, biased exponent 8, 10, 9, 11, mantissa 0) with every token scale
+    0.5, so the dequantised keys are the fixture's and so are ids and scores."""
+    with open(os.path.join(GOLDEN_DIR, "multi_query_causal.json")) as f:
+        fx = json.load(f)
+    L, Q = int(fx["seq_len"]), int(fx["q_len"])
+    code_of_double = {1.0: 0x40, 4.0: 0x50, 2.0: 0x48, 8.0: 0x58}
+    codes = np.zeros((2, PAGE, DIM), dtype=np.uint8)
+    for tok, v in fx["planted_dim0"].items():
+        t = int(tok)
+        codes[t // PAGE, t % PAGE, 0] = code_of_double[float(v)]
+    scale = np.full((2, PAGE), 0.5, dtype=np.float32)
+    q = np.zeros((1, Q, HEADS, DIM), dtype=np.float32)
+    q[0, :, :, 0] = np.asarray(fx["alpha"], dtype=np.float32)[None, :]
+    s, ids, sel, lens = orc.run_multi(wl.f32_to_bf16_bits(q), None,
+                                      np.array([[0, 1]], dtype=np.int32),
+                                      np.array([L], dtype=np.int32), int(fx["k"]),
+                                      int(fx["n_sink"]), int(fx["n_window"]), pool8=codes,
+                                      kscale=scale)
+    assert list(lens[0]) == [127, 128, 129, 130]
+    np.testing.assert_array_equal(ids, np.asarray(fx["expected_ids"], dtype=np.int32))
+    for i in range(Q):
+        for h in range(HEADS):
+            row = fx["expected_scores"][0][i][h]
+            exp = np.full(int(fx["k"]), -np.inf)
+            exp[:len(row)] = row
+            np.testing.assert_array_equal(sel[0, i, h], exp, err_msg=f"position {i} head {h}")
+
+
 def check_prefill_matches_multi_query_fixture(orc) -> None:
     """Four new tokens at the end of a 130-token request are the four draft
     positions of the multi-position fixture: the same ids and scores."""
@@ -379,4 +410,4 @@ def check_prefill_matches_multi_query_fixture(orc) -> None:
 ALL_CHECKS = (check_golden, check_scores_vs_numpy, check_select_vs_rank_count, check_invariants,
               check_expand_golden, check_expand_invariants, check_e4m3_codes, check_fp8_golden,
               check_fp8_vs_numpy, check_multi_query_golden, check_multi_query_one_position_is_decode,
-              check_prefill_matches_multi_query_fixture)
+              check_prefill_matches_multi_query_fixture, check_multi_query_fp8_golden)

@@ -102,3 +102,7 @@ def test_multi_query_single_position_is_decode(orc):
 
 def test_prefill_matches_multi_query_fixture(orc):
     pins.check_prefill_matches_multi_query_fixture(orc)
+
+
+def test_multi_query_fp8_golden(orc):
+    pins.check_multi_query_fp8_golden(orc)
