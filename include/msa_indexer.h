@@ -189,6 +189,23 @@ msa_status msa_indexer_decode_fp8(const void *q, const void *kcache_fp8, const f
                                   void *stream);
 
 /*
+ * Several query positions per request (msa_indexer_decode_mq) on the E4M3
+ * cache of msa_indexer_decode_fp8: q is bf16 [batch, q_len, 4, 128] with
+ * q_len in {1, 2, 4}; position i sees the first seq_len - (q_len - 1 - i)
+ * tokens; outputs are [batch, q_len, 4, k] (out_block_scores
+ * [batch, q_len, 4, bt_stride]).  The workspace is sized by
+ * msa_indexer_workspace_bytes_mq.  Two kernels.
+ */
+msa_status msa_indexer_decode_mq_fp8(const void *q, int q_len, const void *kcache_fp8,
+                                     const float *kscale, int64_t num_pages,
+                                     const int32_t *block_table, int64_t bt_stride,
+                                     const int32_t *seq_lens, int batch, int max_batch,
+                                     int max_model_len, int k, int n_sink, int n_window,
+                                     int32_t *out_ids, float *out_scores, float *out_block_scores,
+                                     void *workspace, size_t workspace_bytes, int split_blocks,
+                                     void *stream);
+
+/*
  * Several query positions per request: speculative-decode verification runs
  * the indexer for the last q_len tokens at once (vLLM PR #57832, "Test
  * Plan": query_len 1/4; vLLM blog "Following the Bottleneck", section 2: one

@@ -29,6 +29,7 @@ from ._binding import (  # noqa: F401
     msa_indexer_decode_noalloc,
     msa_indexer_decode_fp8,
     msa_indexer_decode_mq,
+    msa_indexer_decode_mq_fp8,
     msa_indexer_decode_pages,
     msa_indexer_prefill,
     msa_indexer_prefill_score,

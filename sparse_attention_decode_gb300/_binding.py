@@ -45,6 +45,7 @@ EXPORTED = (
     "msa_indexer_decode_fp8",
     "msa_indexer_decode_mq",
     "msa_indexer_workspace_bytes_mq",
+    "msa_indexer_decode_mq_fp8",
     "msa_indexer_decode_pages",
     "msa_indexer_prefill",
     "msa_indexer_prefill_score",
@@ -100,6 +101,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.msa_indexer_workspace_bytes_mq.restype = c_size
     lib.msa_indexer_decode_mq.argtypes = [P, c_int] + common[1:] + [P, P, P, P, c_size, c_int, P]
     lib.msa_indexer_decode_mq.restype = c_int
+    lib.msa_indexer_decode_mq_fp8.argtypes = [P, c_int] + common8[1:] + [P, P, P, P, c_size, c_int, P]
+    lib.msa_indexer_decode_mq_fp8.restype = c_int
     lib.msa_indexer_prefill_workspace_bytes.argtypes = [c_int, c_int]
     lib.msa_indexer_prefill_workspace_bytes.restype = c_size
     lib.msa_indexer_prefill.argtypes = [P, P, c_int, P, c_i64, P, c_i64, P, c_int, c_int, c_int,
@@ -261,6 +264,30 @@ def msa_indexer_expand_pages(ids, seq_lens, kv_block_table, out_pages, out_num_p
                                          int(kv_block_table.stride(0)), page_tokens,
                                          _ptr(out_pages), _ptr(out_num_pages), _stream_ptr(stream))
     _check(st, "msa_indexer_expand_pages")
+
+
+def msa_indexer_decode_mq_fp8(q, kcache_fp8, kscale, block_table, seq_lens, k: int, n_sink: int,
+                              n_window: int, out_ids, out_scores, workspace, *,
+                              max_batch: Optional[int] = None, max_model_len: int,
+                              out_block_scores=None, split_blocks: int = 0, stream=None) -> None:
+    """msa_indexer_decode_mq_fp8(): q bf16 [B, q_len, 4, 128] on the E4M3 cache."""
+    import torch
+    assert q.dtype == torch.bfloat16 and q.is_contiguous() and q.dim() == 4
+    assert tuple(q.shape[2:]) == (MSA_NUM_HEADS, MSA_HEAD_DIM)
+    assert kcache_fp8.element_size() == 1 and kcache_fp8.is_contiguous(), "kcache_fp8: 1-byte E4M3 codes"
+    assert tuple(kcache_fp8.shape[1:]) == (MSA_PAGE_TOKENS, MSA_HEAD_DIM)
+    assert kscale.dtype == torch.float32 and kscale.is_contiguous()
+    assert tuple(kscale.shape) == tuple(kcache_fp8.shape[:2])
+    assert block_table.dtype == torch.int32 and block_table.dim() == 2 and block_table.stride(1) == 1
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+    B, q_len = int(q.shape[0]), int(q.shape[1])
+    num_pages, bt_stride = int(kcache_fp8.shape[0]), int(block_table.stride(0))
+    st = load().msa_indexer_decode_mq_fp8(
+        _ptr(q), q_len, _ptr(kcache_fp8), _ptr(kscale), num_pages, _ptr(block_table), bt_stride,
+        _ptr(seq_lens), B, B if max_batch is None else max_batch, max_model_len, k, n_sink,
+        n_window, _ptr(out_ids), _ptr(out_scores), _ptr(out_block_scores), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), split_blocks, _stream_ptr(stream))
+    _check(st, "msa_indexer_decode_mq_fp8")
 
 
 def msa_indexer_decode_pages(q, kcache_pool, block_table, seq_lens, k: int, n_sink: int,

@@ -78,6 +78,16 @@ struct Fp8Fmt {
     static constexpr int kScaleBytes = kPage * 4;    // 512 B: one fp32 per token
 };
 
+// fp8 pages for two or four query positions: the wider candidate lists leave
+// room for two stages per consumer warp.
+struct Fp8MqFmt {
+    static constexpr bool kFp8 = true;
+    static constexpr int kConsumers = 4;
+    static constexpr int kStagesPer = 2;
+    static constexpr int kDataBytes = kPage * kDim;
+    static constexpr int kScaleBytes = kPage * 4;
+};
+
 template <class F>
 struct Pipe {
     static constexpr int kConsumers = F::kConsumers;
@@ -310,22 +320,26 @@ __device__ __forceinline__ bool warp_wait(SmemCtl<F> *ctl, WorkspaceHeader *hdr,
 // power of two that keeps it in f16's normal range; f16 mma with fp32
 // accumulation.  The per-token scale multiplies each row before the max, the
 // per-head power of two is undone after it.
+template <int NF>
 __device__ __forceinline__ void score_page_fp8(uint32_t stage, const float *scl,
-                                               const uint32_t (&bq)[8][2], int valid, int lane,
-                                               float &m0, float &m1)
+                                               const uint32_t (&bq)[NF][8][2], const int (&vrows)[NF],
+                                               int lane, float (&m)[NF][2])
 {
     const float neg_inf = -__int_as_float(0x7f800000);
     const int g = lane >> 2;
-    m0 = neg_inf;
-    m1 = neg_inf;
+#pragma unroll
+    for (int f = 0; f < NF; ++f)
+        m[f][0] = m[f][1] = neg_inf;
 #pragma unroll
     for (int mt0 = 0; mt0 < 8; mt0 += 4) {
-        float acc[4][4];
+        float acc[4][NF][4];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                acc[u][e] = 0.0f;
+            for (int f = 0; f < NF; ++f)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    acc[u][f][e] = 0.0f;
 #pragma unroll
         for (int ks = 0; ks < 8; ks += 2) {
 #pragma unroll
@@ -343,85 +357,92 @@ __device__ __forceinline__ void score_page_fp8(uint32_t stage, const float *scl,
                     a[2] = e4m3x2_to_f16x2(static_cast<uint16_t>(r[2 * h] >> 16));
                     a[1] = e4m3x2_to_f16x2(static_cast<uint16_t>(r[2 * h + 1] & 0xffffu));
                     a[3] = e4m3x2_to_f16x2(static_cast<uint16_t>(r[2 * h + 1] >> 16));
-                    mma_f16_16816(acc[u], a, bq[ks + h][0], bq[ks + h][1]);
+#pragma unroll
+                    for (int f = 0; f < NF; ++f)
+                        mma_f16_16816(acc[u][f], a, bq[f][ks + h][0], bq[f][ks + h][1]);
                 }
             }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int row = (mt0 + u) * 16 + g;
-            const bool v0 = row < valid, v1 = row + 8 < valid;
             const float s0 = scl[row], s1 = scl[row + 8];
-            m0 = fmaxf(m0, v0 ? acc[u][0] * s0 : neg_inf);
-            m1 = fmaxf(m1, v0 ? acc[u][1] * s0 : neg_inf);
-            m0 = fmaxf(m0, v1 ? acc[u][2] * s1 : neg_inf);
-            m1 = fmaxf(m1, v1 ? acc[u][3] * s1 : neg_inf);
+#pragma unroll
+            for (int f = 0; f < NF; ++f) {
+                const bool v0 = row < vrows[f], v1 = row + 8 < vrows[f];
+                m[f][0] = fmaxf(m[f][0], v0 ? acc[u][f][0] * s0 : neg_inf);
+                m[f][1] = fmaxf(m[f][1], v0 ? acc[u][f][1] * s0 : neg_inf);
+                m[f][0] = fmaxf(m[f][0], v1 ? acc[u][f][2] * s1 : neg_inf);
+                m[f][1] = fmaxf(m[f][1], v1 ? acc[u][f][3] * s1 : neg_inf);
+            }
         }
     }
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-    }
+    for (int f = 0; f < NF; ++f)
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            m[f][0] = fmaxf(m[f][0], __shfl_xor_sync(0xffffffffu, m[f][0], o));
+            m[f][1] = fmaxf(m[f][1], __shfl_xor_sync(0xffffffffu, m[f][1], o));
+        }
 }
 
 // The query fragments of request b for the page scorer of format F.
-// bf16: the B fragments of m16n8k16: column c = 8f + g of fragment f is q row
-// b * kCols + c (position c / 4, head c % 4); columns past kCols are zero.
-// fp8 (one position): f16 pairs in the byte-to-column map of score_page_fp8,
-// scaled by 2^e per head so the largest |q| lands in [2^13, 2^14); inv_lo /
-// inv_hi receive 2^-e of heads 2t and 2t+1 (t = lane % 4).
+// Column c = 8f + g of fragment f is q row b * kCols + c (position c / 4,
+// head c % 4); columns past kCols are zero.
+// bf16: the B fragments of m16n8k16.
+// fp8: f16 pairs in the byte-to-column map of score_page_fp8, each column
+// scaled by 2^e so its largest |q| lands in [2^13, 2^14); inv_lo[f] /
+// inv_hi[f] receive 2^-e of columns 8f + 2t and 8f + 2t + 1 (t = lane % 4).
 template <class F, int NQ>
 __device__ __forceinline__ void load_query(const ScoreParams &p, int b, int lane,
-                                           uint32_t (&bq)[Cols<NQ>::kFrags][8][2], float &inv_lo,
-                                           float &inv_hi)
+                                           uint32_t (&bq)[Cols<NQ>::kFrags][8][2],
+                                           float (&inv_lo)[Cols<NQ>::kFrags],
+                                           float (&inv_hi)[Cols<NQ>::kFrags])
 {
     constexpr int NC = Cols<NQ>::kCols;
     const int g = lane >> 2, t = lane & 3;
-    if constexpr (!F::kFp8) {
 #pragma unroll
-        for (int f = 0; f < Cols<NQ>::kFrags; ++f) {
-            const int c = 8 * f + g;
-            const uint32_t *qw = reinterpret_cast<const uint32_t *>(
-                p.q + (static_cast<size_t>(b) * NC + (c < NC ? c : 0)) * kDim);
+    for (int f = 0; f < Cols<NQ>::kFrags; ++f) {
+        const int c = 8 * f + g;
+        const uint16_t *qrow = p.q + (static_cast<size_t>(b) * NC + (c < NC ? c : 0)) * kDim;
+        if constexpr (!F::kFp8) {
+            const uint32_t *qw = reinterpret_cast<const uint32_t *>(qrow);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 bq[f][ks][0] = c < NC ? __ldg(qw + 8 * ks + t) : 0u;
                 bq[f][ks][1] = c < NC ? __ldg(qw + 8 * ks + 4 + t) : 0u;
             }
-        }
-        inv_lo = inv_hi = 1.0f;
-    } else {
-        static_assert(NQ == 1, "the fp8 path scores one position");
-        const uint16_t *qrow = p.q + (static_cast<size_t>(b) * kHeads + (g & 3)) * kDim;
-        const uint2 *q8 = reinterpret_cast<const uint2 *>(qrow);  // 4 bf16 per load
-        float v[8][4];
-        float amax = 0.0f;
+            inv_lo[f] = inv_hi[f] = 1.0f;
+        } else {
+            const uint2 *q8 = reinterpret_cast<const uint2 *>(qrow);  // 4 bf16 per load
+            float v[8][4];
+            float amax = 0.0f;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint2 raw = g < kHeads ? __ldg(q8 + 4 * ks + t) : make_uint2(0u, 0u);
-            v[ks][0] = __uint_as_float(raw.x << 16);
-            v[ks][1] = __uint_as_float(raw.x & 0xffff0000u);
-            v[ks][2] = __uint_as_float(raw.y << 16);
-            v[ks][3] = __uint_as_float(raw.y & 0xffff0000u);
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint2 raw = c < NC ? __ldg(q8 + 4 * ks + t) : make_uint2(0u, 0u);
+                v[ks][0] = __uint_as_float(raw.x << 16);
+                v[ks][1] = __uint_as_float(raw.x & 0xffff0000u);
+                v[ks][2] = __uint_as_float(raw.y << 16);
+                v[ks][3] = __uint_as_float(raw.y & 0xffff0000u);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                amax = fmaxf(amax, fabsf(v[ks][e]));
-        }
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        int ex = 0;
-        if (amax > 0.0f)
-            frexpf(amax, &ex);              // amax = m * 2^ex, m in [0.5, 1)
-        const int sh = max(-100, min(100, 14 - ex));
-        const float up = __int_as_float((127 + sh) << 23), down = __int_as_float((127 - sh) << 23);
+                for (int e = 0; e < 4; ++e)
+                    amax = fmaxf(amax, fabsf(v[ks][e]));
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            int ex = 0;
+            if (amax > 0.0f)
+                frexpf(amax, &ex);              // amax = m * 2^ex, m in [0.5, 1)
+            const int sh = max(-100, min(100, 14 - ex));
+            const float up = __int_as_float((127 + sh) << 23), down = __int_as_float((127 - sh) << 23);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            bq[0][ks][0] = f32x2_to_f16x2(v[ks][0] * up, v[ks][1] * up);
-            bq[0][ks][1] = f32x2_to_f16x2(v[ks][2] * up, v[ks][3] * up);
+            for (int ks = 0; ks < 8; ++ks) {
+                bq[f][ks][0] = f32x2_to_f16x2(v[ks][0] * up, v[ks][1] * up);
+                bq[f][ks][1] = f32x2_to_f16x2(v[ks][2] * up, v[ks][3] * up);
+            }
+            inv_lo[f] = __shfl_sync(0xffffffffu, down, (8 * t) & 31);
+            inv_hi[f] = __shfl_sync(0xffffffffu, down, (8 * t + 4) & 31);
         }
-        inv_lo = __shfl_sync(0xffffffffu, down, (8 * t) & 31);
-        inv_hi = __shfl_sync(0xffffffffu, down, (8 * t + 4) & 31);
     }
 }
 
@@ -458,7 +479,10 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
     const uint32_t stage0 = smem_addr(smem + CL::stages);
     const float *scales = reinterpret_cast<const float *>(smem + CL::scales);
     uint32_t bq[NF][8][2];
-    float inv_lo = 1.0f, inv_hi = 1.0f;
+    float inv_lo[NF], inv_hi[NF];
+#pragma unroll
+    for (int f = 0; f < NF; ++f)
+        inv_lo[f] = inv_hi[f] = 1.0f;
     int q_row = -1;
     uint32_t it = 0;       // pages of this CTA so far (same count as the producer's)
     uint32_t segments = 0; // (chunk, request) segments finished so far
@@ -514,17 +538,20 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
                 const bool ok = ready && meta.y != 0;
                 if (ok) {
                     float m[NF][2];
-                    if constexpr (F::kFp8) {
-                        score_page_fp8(stage0 + s * F::kDataBytes, scales + s * kPage, bq[0], meta.x,
-                                       lane, m[0][0], m[0][1]);
-                        m[0][0] *= inv_lo;
-                        m[0][1] *= inv_hi;
-                    } else {
-                        const int rem = seq_len - j * kPage;  // tokens of the last position in this block on
-                        int vrows[NF];
+                    const int rem = seq_len - j * kPage;  // tokens of the last position in this block on
+                    int vrows[NF];
 #pragma unroll
-                        for (int f = 0; f < NF; ++f)
-                            vrows[f] = min(kPage, rem - (NQ - 1 - lane_pos[f]));
+                    for (int f = 0; f < NF; ++f)
+                        vrows[f] = min(kPage, rem - (NQ - 1 - lane_pos[f]));
+                    if constexpr (F::kFp8) {
+                        score_page_fp8<NF>(stage0 + s * F::kDataBytes, scales + s * kPage, bq, vrows,
+                                           lane, m);
+#pragma unroll
+                        for (int f = 0; f < NF; ++f) {
+                            m[f][0] *= inv_lo[f];
+                            m[f][1] *= inv_hi[f];
+                        }
+                    } else {
                         score_page<NQ>(stage0 + s * F::kDataBytes, bq, vrows, lane_off, xo, lane, m);
                     }
 #pragma unroll
@@ -1442,6 +1469,44 @@ extern "C" msa_status msa_indexer_decode_mq(const void *q, int q_len, const void
                                      seq_lens, batch, max_batch, max_model_len, k, n_sink, n_window,
                                      out_block_scores, workspace, workspace_bytes, split_blocks,
                                      stream);
+    if (st != MSA_OK || batch == 0)
+        return st;
+    return merge_entry(batch, k, kHeads * q_len, out_ids, out_scores, workspace, workspace_bytes,
+                       stream);
+}
+
+extern "C" msa_status msa_indexer_decode_mq_fp8(const void *q, int q_len, const void *kcache_fp8,
+                                                const float *kscale, int64_t num_pages,
+                                                const int32_t *block_table, int64_t bt_stride,
+                                                const int32_t *seq_lens, int batch, int max_batch,
+                                                int max_model_len, int k, int n_sink, int n_window,
+                                                int32_t *out_ids, float *out_scores,
+                                                float *out_block_scores, void *workspace,
+                                                size_t workspace_bytes, int split_blocks,
+                                                void *stream)
+{
+    if (!out_ids || !out_scores)
+        return MSA_ERR_INVALID_ARG;
+    if (q_len < 1)
+        return MSA_ERR_INVALID_ARG;
+    if (q_len != 1 && q_len != 2 && q_len != 4)
+        return MSA_ERR_UNSUPPORTED;
+    msa_status st;
+    if (q_len == 1)
+        st = score_entry<Fp8Fmt, 1>(q, kcache_fp8, kscale, num_pages, block_table, bt_stride,
+                                    seq_lens, batch, max_batch, max_model_len, k, n_sink, n_window,
+                                    out_block_scores, workspace, workspace_bytes, split_blocks,
+                                    stream);
+    else if (q_len == 2)
+        st = score_entry<Fp8MqFmt, 2>(q, kcache_fp8, kscale, num_pages, block_table, bt_stride,
+                                      seq_lens, batch, max_batch, max_model_len, k, n_sink,
+                                      n_window, out_block_scores, workspace, workspace_bytes,
+                                      split_blocks, stream);
+    else
+        st = score_entry<Fp8MqFmt, 4>(q, kcache_fp8, kscale, num_pages, block_table, bt_stride,
+                                      seq_lens, batch, max_batch, max_model_len, k, n_sink,
+                                      n_window, out_block_scores, workspace, workspace_bytes,
+                                      split_blocks, stream);
     if (st != MSA_OK || batch == 0)
         return st;
     return merge_entry(batch, k, kHeads * q_len, out_ids, out_scores, workspace, workspace_bytes,
