@@ -299,7 +299,8 @@ msa_status msa_indexer_decode_pages(const void *q, const void *kcache_pool, int6
  * Pins and top-k are per (token, head), over that token's block count.
  *
  *   q             bf16 [total_q, 4, 128]: rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
- *                 are request b's new tokens in order.
+ *                 are request b's new tokens in order (may be NULL when
+ *                 total_q is 0: nothing is launched).
  *   cu_seqlens_q  int32 [batch + 1], non-decreasing, cu_seqlens_q[batch] <= total_q.
  *   seq_lens      int32 [batch]: tokens of request b including its new ones.
  *   out_ids / out_scores  [total_q, 4, k].

@@ -553,7 +553,8 @@ static msa_status prefill_score_launch(const void *q, const int32_t *cu_seqlens_
                                        float *out_block_scores, void *workspace,
                                        size_t workspace_bytes, cudaStream_t st, TcParams *pp)
 {
-    if (!q || !cu_seqlens_q || !kcache_pool || !block_table || !seq_lens || !workspace)
+    if ((!q && total_q > 0) || !cu_seqlens_q || !kcache_pool || !block_table || !seq_lens ||
+        !workspace)
         return MSA_ERR_INVALID_ARG;
     if (total_q < 0 || batch < 1 || max_model_len < 1 || num_pages < 1 || bt_stride < 1)
         return MSA_ERR_INVALID_ARG;

@@ -202,3 +202,22 @@ def test_multi_query_fp8_golden_on_gpu(msa):
             exp = np.full(k, -np.inf)
             exp[:len(row)] = row
             np.testing.assert_array_equal(sc[0, i, h].astype(np.float64), exp)
+
+
+def test_multi_query_fp8_bad_page_is_reported(msa):
+    w, q = multi_workload([3000, 3000], 4, seed=97, num_pages=60, max_model_len=4096)
+    w8 = wl.to_fp8(w)
+    w8.block_table[1, 4] = w8.pool8.shape[0] + 3
+    import torch
+    B, k = w8.batch, 16
+    qd = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).cuda()
+    ids = torch.empty((B, 4, 4, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((B, 4, 4, k), dtype=torch.float32, device="cuda")
+    ws = msa.new_workspace(B, w8.max_model_len, k, q_len=4)
+    msa.msa_indexer_decode_mq_fp8(qd, torch.from_numpy(w8.pool8).cuda(),
+                                  torch.from_numpy(w8.kscale).cuda(),
+                                  torch.from_numpy(w8.block_table).cuda(),
+                                  torch.from_numpy(w8.seq_lens).cuda(), k, 1, 2, ids, sc, ws,
+                                  max_model_len=w8.max_model_len)
+    assert msa.msa_indexer_get_error(ws) & msa.MSA_FAULT_PAGE_ID
+    assert not (ids[1].cpu().numpy() == 4).any()

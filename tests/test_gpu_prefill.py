@@ -205,3 +205,64 @@ def test_prefill_score_only_entry_matches(msa):
                                   max_model_len=w.max_model_len)
     assert msa.msa_indexer_get_error(ws) == 0
     np.testing.assert_array_equal(out.cpu().numpy(), blk)
+
+
+def test_prefill_graph_replay_with_changed_batches(msa, orc):
+    """Captured once; replayed after new lengths, row splits, tables and queries (same total_q)."""
+    import torch
+    total, max_len, k = 300, 16384, 16
+    first = [(100, 9000), (200, 4000)]
+    w, q, cu = prefill_case(first, seed=300, max_model_len=max_len, num_pages=400)
+    d_q = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).cuda()
+    d_pool = torch.from_numpy(w.pool.view(np.int16)).view(torch.bfloat16).cuda()
+    d_bt = torch.zeros((3, w.bt_stride), dtype=torch.int32, device="cuda")
+    d_bt[:2].copy_(torch.from_numpy(w.block_table))
+    d_seq = torch.zeros(3, dtype=torch.int32, device="cuda")
+    d_seq[:2].copy_(torch.from_numpy(w.seq_lens))
+    d_cu = torch.tensor([0, 100, 300, 300], dtype=torch.int32, device="cuda")
+    ids = torch.empty((total, 4, k), dtype=torch.int32, device="cuda")
+    sc = torch.empty((total, 4, k), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(msa.msa_indexer_prefill_workspace_bytes(total, max_len), dtype=torch.uint8,
+                     device="cuda")
+
+    def call():
+        msa.msa_indexer_prefill(d_q, d_cu, d_pool, d_bt, d_seq, k, 1, 2, ids, sc, ws,
+                                max_model_len=max_len)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for seed, pairs in ((301, [(1, 1), (64, 16384), (235, 700)]), (302, [(300, 12000), (0, 5), (0, 0)])):
+        w2, q2, cu2 = prefill_case(pairs, seed=seed, max_model_len=max_len, num_pages=400)
+        assert q2.shape[0] == total
+        d_q.copy_(torch.from_numpy(q2.view(np.int16)).view(torch.bfloat16))
+        d_pool.copy_(torch.from_numpy(w2.pool.view(np.int16)).view(torch.bfloat16))
+        d_bt.copy_(torch.from_numpy(w2.block_table))
+        d_seq.copy_(torch.from_numpy(w2.seq_lens))
+        d_cu.copy_(torch.from_numpy(cu2))
+        g.replay()
+        torch.cuda.synchronize()
+        check_prefill(orc, w2, q2, cu2, (ids.cpu().numpy(), sc.cpu().numpy(), None))
+    assert msa.msa_indexer_get_error(ws) == 0
+
+
+def test_prefill_without_rows(msa):
+    """total_q = 0: the call succeeds and writes nothing."""
+    import torch
+    w, q, cu = prefill_case([(4, 300)], seed=310, max_model_len=1024)
+    d = parity.to_device(w)
+    q0 = torch.empty((0, 4, 128), dtype=torch.bfloat16, device="cuda")
+    cu0 = torch.zeros(2, dtype=torch.int32, device="cuda")
+    ids = torch.full((4,), -7, dtype=torch.int32, device="cuda")
+    sc = torch.full((4,), 7.0, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    msa.msa_indexer_prefill(q0, cu0, d[1], d[2], d[3], 16, 1, 2, ids, sc, ws,
+                            max_model_len=w.max_model_len)
+    torch.cuda.synchronize()
+    assert (ids == -7).all() and (sc == 7.0).all()
+    assert msa.msa_indexer_get_error(ws) == 0
