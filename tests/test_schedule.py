@@ -16,8 +16,6 @@ import random
 
 import pytest
 
-CONSUMERS, STAGES_PER_CONSUMER = 2, 3  # must match score_kernel's pipeline shape
-STAGES = CONSUMERS * STAGES_PER_CONSUMER
 MAX_GRID = 1024
 MAX_LEVELS = 6
 MIN_POOL_HOME = 64
@@ -85,8 +83,20 @@ def chunk_capacity(grid, max_pages, split_blocks):
     return ceil_div(max_pages, split_blocks) if split_blocks > 0 else grid * (1 + MAX_LEVELS)
 
 
-def stage_of(it):
-    return it % CONSUMERS + CONSUMERS * ((it // CONSUMERS) % STAGES_PER_CONSUMER)
+# (consumer warps, stages per consumer warp, stages per page) of each format;
+# the replay also covers pages split over several stages
+FORMATS = {"bf16": (2, 3, 1), "fp8": (4, 3, 1), "fp8_mq": (4, 2, 1), "bf16_wide4": (4, 1, 1)}
+
+
+def stage_of(it, h=0, fmt=FORMATS["bf16"]):
+    C, spc, units = fmt
+    local = (it // C) * units + h
+    return it % C + C * (local % spc)
+
+
+def use_of(it, h=0, fmt=FORMATS["bf16"]):
+    C, spc, units = fmt
+    return ((it // C) * units + h) // spc
 
 
 def find_row(prefix, batch, p):
@@ -106,7 +116,7 @@ def score_grid(sms, batch, max_blocks, split_blocks):
     return max(1, min(sms, MAX_GRID, units))
 
 
-def replay(seq, max_model_len, bt_stride, split_blocks, sms, rng):
+def replay(seq, max_model_len, bt_stride, split_blocks, sms, rng, fmt=FORMATS["bf16"]):
     B = len(seq)
     max_blocks = ceil_div(max_model_len, 128)
     grid = score_grid(sms, B, max_blocks, split_blocks)
@@ -159,15 +169,26 @@ def replay(seq, max_model_len, bt_stride, split_blocks, sms, rng):
                     assert 0 <= j < nb[b] <= bt_stride
                     assert (b, j) not in seen
                     seen.add((b, j))
-                    s = stage_of(my)
-                    assert s % CONSUMERS == my % CONSUMERS  # owned by the page's consumer warp
-                    assert uses.get(s, -1) == my // STAGES - 1  # phases in order
-                    uses[s] = my // STAGES
+                    for h in range(fmt[2]):
+                        s = stage_of(my, h, fmt)
+                        assert s % fmt[0] == my % fmt[0]  # owned by the page's consumer warp
+                        assert 0 <= s < fmt[0] * fmt[1]
+                        assert uses.get(s, -1) == use_of(my, h, fmt) - 1  # phases in order
+                        uses[s] = use_of(my, h, fmt)
                 it += seg_end - pg
                 slot = c + b
                 assert slot < capacity and slot not in written
                 written[slot] = (c, b)
                 pg = seg_end
+        # the producer's drain waits on the last C * spc units: each used
+        # stage's latest use is among them, exactly once
+        n_units = it * fmt[2]
+        last = [stage_of(u // fmt[2], u % fmt[2], fmt) for u in range(max(0, n_units - fmt[0] * fmt[1]), n_units)]
+        assert len(last) == len(set(last))
+        assert set(last) == set(uses)
+        for u in range(max(0, n_units - fmt[0] * fmt[1]), n_units):
+            q, h = divmod(u, fmt[2])
+            assert use_of(q, h, fmt) == uses[stage_of(q, h, fmt)]
     assert len(seen) == total
     for b in range(B):
         if prefix[b + 1] > prefix[b]:
@@ -207,3 +228,13 @@ def test_random_batches():
         W = rng.choice([0, 0, 0, 1, 2, 5, 17, 64])
         for sms in (152, 7):
             replay(seq, mml, bts, W, sms, rng)
+
+
+@pytest.mark.parametrize("fmt", sorted(FORMATS) + ["split_pages"])
+def test_stage_rings_of_every_format(fmt):
+    rng = random.Random(7)
+    for _ in range(60):
+        B = rng.randint(1, 40)
+        seq = [rng.choice([0, 1, 127, 128, 129, rng.randint(1, 20000)]) for _ in range(B)]
+        shape = FORMATS[fmt] if fmt in FORMATS else (4, 6, 2)
+        replay(seq, 20480, 160, rng.choice([0, 0, 1, 3, 64]), rng.choice([1, 7, 152]), rng, shape)
