@@ -256,6 +256,44 @@ __device__ __forceinline__ void give_up(const TcParams &p, TcSmem *ctl)
     *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
 }
 
+// The MMAs of pages [j0, je) of one segment, by the issuing thread: per page,
+// NMT M tiles of 8 tcgen05.mma each.  NMT = 1 for a tile whose second M tile
+// holds no new token (its epilogue writes nothing); the choice is made once
+// per segment so the per-page issue path carries no branch.  Returns false
+// when a wait ran out.
+template <int NMT>
+__device__ __forceinline__ bool mma_pages(const TcParams &p, TcSmem *ctl, uint32_t tmem,
+                                          uint32_t q_smem, uint32_t k_smem, int j0, int je,
+                                          uint32_t &kc, uint32_t &ac)
+{
+    for (int j = j0; j < je; ++j) {
+        const int s = static_cast<int>(kc % kTcStages);
+        const int a = static_cast<int>(ac & 1u);
+        if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->k_full[s]), (kc / kTcStages) & 1u) ||
+            (ac >= 2 && !mbar_wait(smem_addr(&ctl->acc_empty[a]), ((ac >> 1) - 1) & 1u))) {
+            give_up(p, ctl);
+            return false;
+        }
+        tc_fence_after_sync();
+        const uint32_t kst = k_smem + s * kPageBytes;
+#pragma unroll
+        for (int mt = 0; mt < NMT; ++mt) {
+            const uint32_t d = tmem + static_cast<uint32_t>(a * kMTiles * kPage + mt * kPage);
+#pragma unroll
+            for (int ks = 0; ks < kDim / 16; ++ks) {
+                const uint32_t off = (ks >> 2) * kHalfPageBytes + (ks & 3) * 32;
+                umma_bf16(d, umma_desc_sw128(q_smem + mt * kQTileBytes + off),
+                          umma_desc_sw128(kst + off), kIdesc, ks > 0 ? 1u : 0u);
+            }
+        }
+        umma_commit(smem_addr(&ctl->k_empty[s]));
+        umma_commit(smem_addr(&ctl->acc_full[a]));
+        ++kc;
+        ++ac;
+    }
+    return true;
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const __grid_constant__ TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -392,32 +430,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
                     break;
                 }
                 tc_fence_after_sync();
-                for (int j = c.j; j < je; ++j) {
-                    const int s = static_cast<int>(kc % kTcStages);
-                    const int a = static_cast<int>(ac & 1u);
-                    if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->k_full[s]), (kc / kTcStages) & 1u) ||
-                        (ac >= 2 && !mbar_wait(smem_addr(&ctl->acc_empty[a]), ((ac >> 1) - 1) & 1u))) {
-                        give_up(p, ctl);
-                        ok_run = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t kst = k_smem + s * kPageBytes;
-#pragma unroll
-                    for (int mt = 0; mt < kMTiles; ++mt) {
-                        const uint32_t d = tmem + static_cast<uint32_t>(a * kMTiles * kPage + mt * kPage);
-#pragma unroll
-                        for (int ks = 0; ks < kDim / 16; ++ks) {
-                            const uint32_t off = (ks >> 2) * kHalfPageBytes + (ks & 3) * 32;
-                            umma_bf16(d, umma_desc_sw128(q_smem + mt * kQTileBytes + off),
-                                      umma_desc_sw128(kst + off), kIdesc, ks > 0 ? 1u : 0u);
-                        }
-                    }
-                    umma_commit(smem_addr(&ctl->k_empty[s]));
-                    umma_commit(smem_addr(&ctl->acc_full[a]));
-                    ++kc;
-                    ++ac;
-                }
+                // M tiles holding at least one of the tile's new tokens
+                const int live_tokens = min(kTileTokens, c.r.n - kTileTokens * c.t);
+                const int live_mtiles = (live_tokens * kHeads + kMRows - 1) / kMRows;
+                ok_run = live_mtiles == kMTiles
+                             ? mma_pages<kMTiles>(p, ctl, tmem, q_smem, k_smem, c.j, je, kc, ac)
+                             : mma_pages<1>(p, ctl, tmem, q_smem, k_smem, c.j, je, kc, ac);
                 umma_commit(smem_addr(&ctl->q_empty));
                 ++seg;
                 left -= je - c.j;
