@@ -20,6 +20,8 @@
 //              (M = 128 rows, N = 128 keys, K = 16) for both 128-row halves
 //              of the tile against each page, fp32 accumulators in TMEM,
 //              double-buffered across pages (2 x 2 x 128 = 512 columns);
+//              (tiles of 32 tokens would allow four buffers but load every
+//              page for half as many rows: 1.3x slower when measured)
 //   warps 2-9  read their rows' 128 accumulators per page from TMEM and
 //              write the masked block max (keys <= the row's position).
 //
@@ -48,7 +50,9 @@ constexpr int kMTiles = kTileTokens * kHeads / kMRows;  // 2
 constexpr int kTcStages = 4;
 constexpr int kEpiWarps = 4 * kMTiles;                // one per (TMEM lane quarter, M tile)
 constexpr int kTcThreads = 32 * (2 + kEpiWarps);
-constexpr uint32_t kTmemCols = 2 * kMTiles * kPage;   // 512
+constexpr uint32_t kTmemCols = 512;                   // the whole tensor memory
+constexpr int kAccBufs = kTmemCols / (kMTiles * kPage);  // accumulator buffers (pages in flight)
+static_assert(kPage % kTileTokens == 0 && kAccBufs >= 2, "tile geometry");
 constexpr int kQTileBytes = kMRows * kDim * 2;        // 32 KiB per M tile
 constexpr uint32_t kQBytes = kMTiles * kQTileBytes;
 constexpr uint32_t kIdesc = umma_idesc_bf16_f32(kMRows, kPage);
@@ -74,8 +78,8 @@ struct TcSmem {
     uint64_t k_empty[kTcStages];
     uint64_t q_full;
     uint64_t q_empty;
-    uint64_t acc_full[2];
-    uint64_t acc_empty[2];
+    uint64_t acc_full[kAccBufs];
+    uint64_t acc_empty[kAccBufs];
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
@@ -116,14 +120,21 @@ __device__ __forceinline__ int tile_pages(const Req &r, int t)
 }
 
 // Pages of tiles [0, t) for t <= tiles - 1 (all full tiles).  Full tile t'
-// ends at position c + 64 t' with c = len - n + 63 and sees
-// floor((c + 64 t') / 128) + 1 pages; even t' = 2m gives m + floor(c / 128),
-// odd t' = 2m + 1 gives m + floor((c + 64) / 128).
+// ends at position c + T t' (T = kTileTokens, c = len - n + T - 1) and sees
+// floor((c + T t') / 128) + 1 pages; writing t' = R m + r with R = 128 / T,
+// that is m + floor((c + T r) / 128) + 1, so the tiles of residue r sum in
+// closed form.
 __device__ __forceinline__ long long pages_before(const Req &r, int t)
 {
+    constexpr int R = kPage / kTileTokens;
     const long long c = static_cast<long long>(r.len) - r.n + kTileTokens - 1;
-    const long long e = (t + 1) / 2, o = t / 2;
-    return t + e * (c / kPage) + e * (e - 1) / 2 + o * ((c + kTileTokens) / kPage) + o * (o - 1) / 2;
+    long long sum = t;
+#pragma unroll
+    for (int res = 0; res < R; ++res) {
+        const long long n_r = t > res ? (t - res + R - 1) / R : 0;  // tiles t' < t with t' % R == res
+        sum += n_r * ((c + static_cast<long long>(kTileTokens) * res) / kPage) + n_r * (n_r - 1) / 2;
+    }
+    return sum;
 }
 
 __device__ __forceinline__ long long req_units(const Req &r)
@@ -268,9 +279,9 @@ __device__ __forceinline__ bool mma_pages(const TcParams &p, TcSmem *ctl, uint32
 {
     for (int j = j0; j < je; ++j) {
         const int s = static_cast<int>(kc % kTcStages);
-        const int a = static_cast<int>(ac & 1u);
+        const int a = static_cast<int>(ac % kAccBufs);
         if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->k_full[s]), (kc / kTcStages) & 1u) ||
-            (ac >= 2 && !mbar_wait(smem_addr(&ctl->acc_empty[a]), ((ac >> 1) - 1) & 1u))) {
+            (ac >= kAccBufs && !mbar_wait(smem_addr(&ctl->acc_empty[a]), ((ac / kAccBufs) - 1) & 1u))) {
             give_up(p, ctl);
             return false;
         }
@@ -311,7 +322,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
         }
         mbar_init(smem_addr(&ctl->q_full), 1);
         mbar_init(smem_addr(&ctl->q_empty), 1);
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kAccBufs; ++a) {
             mbar_init(smem_addr(&ctl->acc_full[a]), 1);
             mbar_init(smem_addr(&ctl->acc_empty[a]), kEpiWarps);
         }
@@ -471,8 +482,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
             const int pos = c.r.len - c.r.n + tl;
             float *out = p.scores + (static_cast<int64_t>(c.r.c0 + tl) * kHeads + head) * p.bs_stride;
             for (int j = c.j; j < je; ++j) {
-                const int a = static_cast<int>(ac & 1u);
-                bool ready = !aborted(ctl) && mbar_wait(smem_addr(&ctl->acc_full[a]), (ac >> 1) & 1u);
+                const int a = static_cast<int>(ac % kAccBufs);
+                bool ready = !aborted(ctl) && mbar_wait(smem_addr(&ctl->acc_full[a]), (ac / kAccBufs) & 1u);
                 ready = __all_sync(0xffffffffu, ready);
                 if (!ready) {
                     if (lane == 0)

@@ -22,10 +22,17 @@ def tile_pages(n, L, t):
     return (L - n + last) // PAGE + 1
 
 
-def pages_before(n, L, t):
-    c = L - n + TILE - 1
-    e, o = (t + 1) // 2, t // 2
-    return t + e * (c // PAGE) + e * (e - 1) // 2 + o * ((c + TILE) // PAGE) + o * (o - 1) // 2
+def pages_before(n, L, t, tile=None):
+    """Closed form by residue: tile t' = R m + r (R = PAGE / tile) sees
+    m + floor((c + tile r) / PAGE) + 1 pages."""
+    tile = TILE if tile is None else tile
+    R = PAGE // tile
+    c = L - n + tile - 1
+    total = t
+    for r in range(R):
+        n_r = (t - r + R - 1) // R if t > r else 0
+        total += n_r * ((c + tile * r) // PAGE) + n_r * (n_r - 1) // 2
+    return total
 
 
 def req_units(n, L, ok=True):
@@ -84,17 +91,18 @@ def all_units(reqs):
             for t in range(tiles_of(n)) for j in range(tile_pages(n, L, t))]
 
 
-def test_closed_form_matches_brute_force():
-    rng = np.random.default_rng(0)
-    for _ in range(3000):
+@pytest.mark.parametrize("tile", [16, 32, 64, 128])
+def test_closed_form_matches_brute_force(tile):
+    rng = np.random.default_rng(tile)
+    for _ in range(1500):
         L = int(rng.integers(1, 300000))
         n = int(rng.integers(1, min(L, 5000) + 1))
-        T = tiles_of(n)
+        T = (n + tile - 1) // tile
         acc = 0
         for t in range(T):
-            assert pages_before(n, L, t) == acc, (n, L, t)
-            acc += tile_pages(n, L, t)
-        assert req_units(n, L) == acc
+            assert pages_before(n, L, t, tile) == acc, (n, L, t, tile)
+            last = min(n, tile * (t + 1)) - 1
+            acc += (L - n + last) // PAGE + 1
 
 
 def _random_batch(rng):
