@@ -266,3 +266,27 @@ def test_prefill_without_rows(msa):
     torch.cuda.synchronize()
     assert (ids == -7).all() and (sc == 7.0).all()
     assert msa.msa_indexer_get_error(ws) == 0
+
+
+@pytest.mark.slow
+def test_prefill_bench_workload_sampled_rows(msa, orc):
+    """The benchmarked prefill (4 x 2048 new tokens at 128K, the launch bench.py
+    times) on the GPU; sampled rows checked one by one against the oracle."""
+    import bench
+    w, q, cu = bench.prefill_workload()
+    got = run_prefill(msa, w, q, cu)
+    assert got[3] == 0
+    total = q.shape[0]
+    rng = np.random.default_rng(400)
+    firsts, lasts = cu[:-1], cu[1:] - 1
+    rows = np.unique(np.concatenate([firsts, lasts, rng.choice(total, 16, replace=False)]))
+    req = np.searchsorted(cu, rows, side="right") - 1
+    lens = (w.seq_lens[req] - np.diff(cu)[req] + (rows - cu[req]) + 1).astype(np.int32)
+    bt_rows = w.block_table[req]
+    s = orc.block_scores(q[rows], w.pool, bt_rows, lens)
+    o_ids, _ = orc.select(s, lens, w.k, w.n_sink, w.n_window)
+    sub = wl.Workload(name="bench_prefill_rows", q=q[rows], pool=w.pool, block_table=bt_rows,
+                      seq_lens=lens, k=w.k, n_sink=w.n_sink, n_window=w.n_window,
+                      max_model_len=w.max_model_len)
+    st = sub.bt_stride
+    parity.check(sub, s[:, :, :st], o_ids, got[0][rows], got[1][rows], got[2][rows][:, :, :st])
