@@ -9,6 +9,7 @@ valid token's 128 bf16 values once) with us/call beside it.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
     python bench.py --path prefill   # prefill scoring (tensor cores), its own line
     python bench.py --configs        # every named workload: graph median + oracle timing
+    python bench.py --sweep          # the SGLang page's batch x context grid, bf16 and fp8
 
 Under torchrun (N > 1) every rank runs its own replica of the batch on its
 own GPU; there is no data-path collective (weak scaling), only a barrier and
@@ -55,6 +56,8 @@ def parse_args(argv=None):
                     help="index-K cache format (bf16 is the headline; fp8 = E4M3 + per-token scale)")
     ap.add_argument("--path", choices=["decode", "prefill"], default="decode",
                     help="decode (the headline) or prefill scoring (4 x 2048 new tokens at 128K)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the SGLang page's batch x context shapes (bf16 and fp8 caches)")
     ap.add_argument("--configs", action="store_true",
                     help="time every named workload (one JSON line each) instead of the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -767,6 +770,84 @@ def run_configs(args):
     return lines
 
 
+# SGLang PR #41488, "Speed Tests": the indexer chain on 4x MI355X with an fp8
+# E4M3 index cache, native TP -> context parallel, in us (context only: other
+# hardware, four GPUs for the CP figure).  (batch, context, lengths) -> (tp, cp).
+SGLANG_SHAPES = [
+    ((1, 8192), (9.40, 15.40)), ((8, 8192), (7.72, 18.32)), ((32, 8192), (12.12, 19.58)),
+    ((16, 32768), (20.80, 20.04)), ((32, 32768), (30.41, 24.38)),
+    ((1, 131072), (12.71, 15.93)), ((8, 131072), (32.85, 24.02)), ((16, 131072), (51.71, 32.08)),
+    ((32, 131072), (109.84, 41.63)),
+    ((16, "one 131072 + 1024s"), (40.76, 27.82)), ((32, "one 131072 + 1024s"), (68.89, 34.62)),
+]
+
+
+def run_sweep(args):
+    """Decode on each shape of the SGLang speed table, bf16 and fp8 caches."""
+    import numpy as np
+    import torch
+
+    import sparse_attention_decode_gb300 as msa
+    import workloads as wl
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    msa.load()
+    stream = torch.cuda.current_stream(device)
+    peak, peak_src = measured_hbm_peak()
+    lines = []
+    for (B, ctx), (tp_us, cp_us) in SGLANG_SHAPES:
+        if isinstance(ctx, str):
+            lens = [131072] + [1024] * (B - 1)
+        else:
+            lens = [ctx] * B
+        w = wl.random_workload(lens, seed=500 + B, max_model_len=max(lens), name=f"sweep_{B}")
+        w8 = wl.to_fp8(w)
+        q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).to(device)
+        bt = torch.from_numpy(w.block_table).to(device)
+        seq = torch.from_numpy(w.seq_lens).to(device)
+        ids = torch.empty((B, 4, w.k), dtype=torch.int32, device=device)
+        sc = torch.empty((B, 4, w.k), dtype=torch.float32, device=device)
+        ws = msa.new_workspace(B, w.max_model_len, w.k, device=device)
+        for cache in ("bf16", "fp8"):
+            if cache == "bf16":
+                pool = torch.from_numpy(w.pool.view(np.int16)).view(torch.bfloat16).to(device)
+                nbytes = w.index_k_bytes
+
+                def call(st, i, pool=pool):
+                    msa.msa_indexer_decode(q, pool, bt, seq, w.k, w.n_sink, w.n_window, ids, sc,
+                                           ws, max_model_len=w.max_model_len, stream=st)
+            else:
+                pool8 = torch.from_numpy(w8.pool8).to(device)
+                kscale = torch.from_numpy(w8.kscale).to(device)
+                nbytes = w8.index_k_bytes
+
+                def call(st, i, pool8=pool8, kscale=kscale):
+                    msa.msa_indexer_decode_fp8(q, pool8, kscale, bt, seq, w.k, w.n_sink,
+                                               w.n_window, ids, sc, ws,
+                                               max_model_len=w.max_model_len, stream=st)
+            us, eager = graph_median_us(call, stream, device)
+            assert msa.msa_indexer_get_error(ws, stream=stream) == 0
+            gbs = nbytes / (us * 1e-6) / 1e9
+            lines.append({
+                "sweep": "SGLang PR #41488 speed-test shapes", "cache": cache, "batch": B,
+                "context": ctx, "index_k_bytes": nbytes, "us_per_call": round(us, 2),
+                "eager_us_per_call": round(eager, 2), "gb_s": round(gbs, 1),
+                "hbm_frac": round(gbs / peak, 4), "hbm_peak_source": peak_src,
+                "timing": "graph of 20 calls, 50 replays x 7 rounds, median",
+                "context_only": {"sglang_mi355x_fp8_native_tp_us": tp_us,
+                                 "sglang_4x_mi355x_fp8_cp_us": cp_us},
+            })
+            if cache == "bf16":
+                del pool
+            else:
+                del pool8, kscale
+            torch.cuda.empty_cache()
+        del q, bt, seq, ids, sc, ws
+        torch.cuda.empty_cache()
+    return lines
+
+
 # ----------------------------------------------------------------------------
 # the CPU oracle (baseline leg and reference arm)
 # ----------------------------------------------------------------------------
@@ -868,6 +949,10 @@ def main(argv=None):
     args = parse_args(argv)
     if args.configs and args.impl != "reference":
         for line in run_configs(args):
+            print(json.dumps(line), flush=True)
+        return
+    if args.sweep and args.impl != "reference":
+        for line in run_sweep(args):
             print(json.dumps(line), flush=True)
         return
     if args.impl == "reference":
