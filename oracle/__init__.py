@@ -199,9 +199,10 @@ class Oracle:
         return (s.reshape(B, Q, HEADS, stride), ids.reshape(B, Q, HEADS, k),
                 sel.reshape(B, Q, HEADS, k), lens)
 
-    def run_prefill(self, q: np.ndarray, cu_seqlens_q: np.ndarray, pool: np.ndarray,
+    def run_prefill(self, q: np.ndarray, cu_seqlens_q: np.ndarray, pool: Optional[np.ndarray],
                     block_table: np.ndarray, seq_lens: np.ndarray, k: int, n_sink: int,
-                    n_window: int):
+                    n_window: int, pool8: Optional[np.ndarray] = None,
+                    kscale: Optional[np.ndarray] = None):
         """Prefill: the new tokens of every request, each over its own causal prefix.
 
         q is [total_q, 4, 128]; request b's new tokens are rows
@@ -209,7 +210,8 @@ class Oracle:
         (vLLM PR #57832, "Question ... mixed batches": the prefill branch
         scores iq[nd:] with cu_seqlens_q).  New token t of request b sits at
         position seq_len - n_b + t and sees the first seq_len - n_b + t + 1
-        tokens, so each row is one decode query over that length.
+        tokens, so each row is one decode query over that length.  With pool8 /
+        kscale the keys are the E4M3 cache of block_scores_fp8.
         Returns (scores [total_q,4,stride], ids [total_q,4,k], sel, lens [total_q]).
         """
         q = np.ascontiguousarray(q, dtype=np.uint16)
@@ -224,7 +226,10 @@ class Oracle:
                 lens.append(max(0, int(seq[b]) - n + t + 1))
         lens = np.asarray(lens, dtype=np.int32)
         rows_bt = np.asarray(rows_bt, dtype=np.int32).reshape(-1, bt.shape[1])
-        s = self.block_scores(q, pool, rows_bt, lens)
+        if pool8 is not None:
+            s = self.block_scores_fp8(q, pool8, kscale, rows_bt, lens)
+        else:
+            s = self.block_scores(q, pool, rows_bt, lens)
         ids, sel = self.select(s, lens, k, n_sink, n_window)
         return s, ids, sel, lens
 

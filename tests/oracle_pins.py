@@ -407,7 +407,35 @@ def check_prefill_matches_multi_query_fixture(orc) -> None:
     np.testing.assert_array_equal(ids, np.asarray(fx["expected_ids"], dtype=np.int32)[0])
 
 
+def check_prefill_fp8_matches_fixture(orc) -> None:
+    """The E4M3 causal fixture through the prefill route: the request's last
+    four tokens as new tokens give the fixture's ids and scores."""
+    with open(os.path.join(GOLDEN_DIR, "multi_query_causal.json")) as f:
+        fx = json.load(f)
+    L, Q, k = int(fx["seq_len"]), int(fx["q_len"]), int(fx["k"])
+    code_of_double = {1.0: 0x40, 4.0: 0x50, 2.0: 0x48, 8.0: 0x58}
+    codes = np.zeros((2, PAGE, DIM), dtype=np.uint8)
+    for tok, v in fx["planted_dim0"].items():
+        codes[int(tok) // PAGE, int(tok) % PAGE, 0] = code_of_double[float(v)]
+    scale = np.full((2, PAGE), 0.5, dtype=np.float32)
+    q = np.zeros((Q, HEADS, DIM), dtype=np.float32)
+    q[:, :, 0] = np.asarray(fx["alpha"], dtype=np.float32)[None, :]
+    s, ids, sel, lens = orc.run_prefill(wl.f32_to_bf16_bits(q), np.array([0, Q]), None,
+                                        np.array([[0, 1]], dtype=np.int32),
+                                        np.array([L], dtype=np.int32), k, int(fx["n_sink"]),
+                                        int(fx["n_window"]), pool8=codes, kscale=scale)
+    assert list(lens) == [127, 128, 129, 130]
+    np.testing.assert_array_equal(ids, np.asarray(fx["expected_ids"], dtype=np.int32)[0])
+    for i in range(Q):
+        for h in range(HEADS):
+            row = fx["expected_scores"][0][i][h]
+            exp = np.full(k, -np.inf)
+            exp[:len(row)] = row
+            np.testing.assert_array_equal(sel[i, h], exp, err_msg=f"token {i} head {h}")
+
+
 ALL_CHECKS = (check_golden, check_scores_vs_numpy, check_select_vs_rank_count, check_invariants,
               check_expand_golden, check_expand_invariants, check_e4m3_codes, check_fp8_golden,
               check_fp8_vs_numpy, check_multi_query_golden, check_multi_query_one_position_is_decode,
-              check_prefill_matches_multi_query_fixture, check_multi_query_fp8_golden)
+              check_prefill_matches_multi_query_fixture, check_multi_query_fp8_golden,
+              check_prefill_fp8_matches_fixture)

@@ -106,3 +106,7 @@ def test_prefill_matches_multi_query_fixture(orc):
 
 def test_multi_query_fp8_golden(orc):
     pins.check_multi_query_fp8_golden(orc)
+
+
+def test_prefill_fp8_matches_fixture(orc):
+    pins.check_prefill_fp8_matches_fixture(orc)
