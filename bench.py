@@ -537,10 +537,18 @@ def run_prefill_bench(args):
     dist = init_dist(world, "nccl")
     msa.load()
     w, q_bits, cu_np = prefill_workload()
+    fp8 = args.cache == "fp8"
+    if fp8:
+        import workloads as wl
+        w = wl.to_fp8(w)
     total, k, L = q_bits.shape[0], w.k, w.max_model_len
     flops = prefill_flops()
     q = torch.from_numpy(q_bits.view(np.int16)).view(torch.bfloat16).to(device)
-    pool = torch.from_numpy(w.pool.view(np.int16)).view(torch.bfloat16).to(device)
+    if fp8:
+        pool = torch.from_numpy(w.pool8).to(device)
+        kscale = torch.from_numpy(w.kscale).to(device)
+    else:
+        pool = torch.from_numpy(w.pool.view(np.int16)).view(torch.bfloat16).to(device)
     bt = torch.from_numpy(w.block_table).to(device)
     seq = torch.from_numpy(w.seq_lens).to(device)
     cu = torch.from_numpy(cu_np).to(device)
@@ -552,11 +560,20 @@ def run_prefill_bench(args):
     stream = torch.cuda.current_stream(device)
 
     def step(st):
-        msa.msa_indexer_prefill(q, cu, pool, bt, seq, k, w.n_sink, w.n_window, ids, sc, ws,
-                                max_model_len=L, stream=st)
+        if fp8:
+            msa.msa_indexer_prefill_fp8(q, cu, pool, kscale, bt, seq, k, w.n_sink, w.n_window, ids,
+                                        sc, ws, max_model_len=L, stream=st)
+        else:
+            msa.msa_indexer_prefill(q, cu, pool, bt, seq, k, w.n_sink, w.n_window, ids, sc, ws,
+                                    max_model_len=L, stream=st)
 
     def score_only(st):
-        msa.msa_indexer_prefill_score(q, cu, pool, bt, seq, blk, ws, max_model_len=L, stream=st)
+        if fp8:
+            msa.msa_indexer_prefill_score_fp8(q, cu, pool, kscale, bt, seq, blk, ws,
+                                              max_model_len=L, stream=st)
+        else:
+            msa.msa_indexer_prefill_score(q, cu, pool, bt, seq, blk, ws, max_model_len=L,
+                                          stream=st)
 
     side = torch.cuda.Stream(device)
 
@@ -613,8 +630,13 @@ def run_prefill_bench(args):
 
         def e2e_call(slot):
             (e_q, e_bt, e_seq, e_cu), (e_ids, e_sc) = io.views(slot)
-            msa.msa_indexer_prefill(e_q, e_cu, pool, e_bt, e_seq, k, w.n_sink, w.n_window, e_ids,
-                                    e_sc, ws, max_model_len=L, stream=stream)
+            if fp8:
+                msa.msa_indexer_prefill_fp8(e_q, e_cu, pool, kscale, e_bt, e_seq, k, w.n_sink,
+                                            w.n_window, e_ids, e_sc, ws, max_model_len=L,
+                                            stream=stream)
+            else:
+                msa.msa_indexer_prefill(e_q, e_cu, pool, e_bt, e_seq, k, w.n_sink, w.n_window,
+                                        e_ids, e_sc, ws, max_model_len=L, stream=stream)
 
         io.run(4, stream, e2e_call)
         _, (r_ids, r_sc) = io.views(1)
@@ -638,11 +660,14 @@ def run_prefill_bench(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16 (fp32 accumulate in TMEM)",
+        "dtype": ("fp8-e4m3 keys x bf16 q, both widened to f16 (fp32 accumulate in TMEM)"
+                  if fp8 else "bf16 (fp32 accumulate in TMEM)"),
         "data": "synthetic",
         "config": {
             "workload": "chunked_prefill: 4 requests x 2048 new tokens at 131072 tokens, 4 index "
-                        "heads, d=128, 128-token pages, k=16, n_sink=1, n_window=2",
+                        "heads, d=128, 128-token pages, k=16, n_sink=1, n_window=2"
+                        + (", fp8 E4M3 cache + fp32 per-token scales" if fp8 else ""),
+            "cache": args.cache,
             "total_q": total, "useful_flops_per_step": flops, "parallelism": f"replicas x{world}",
             "timing": "one CUDA graph of K consecutive prefill calls (score + top-k kernels), "
                       "CUDA events on the stream",
@@ -650,16 +675,17 @@ def run_prefill_bench(args):
                   "no flush",
         },
         "roofline": {
-            "bound": "tensor", "kernel": "tc_prefill_score_kernel",
+            "bound": "tensor", "kernel": "tc_prefill_fp8_kernel" if fp8 else "tc_prefill_score_kernel",
             "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src,
             "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic(32, "prefill"), "score_us": round(score_ms * 1e3, 2),
+            "traffic": None if fp8 else profiled_traffic(32, "prefill"),
+            "score_us": round(score_ms * 1e3, 2),
         },
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "e2e": e2e,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and not fp8:
         line["cpu_baseline"] = prefill_cpu_baseline(w, q_bits)
     return line
 

@@ -317,6 +317,31 @@ msa_status msa_indexer_decode_pages(const void *q, const void *kcache_pool, int6
 size_t msa_indexer_prefill_workspace_bytes(int max_total_q, int max_model_len);
 
 /*
+ * msa_indexer_prefill on the E4M3 cache of msa_indexer_decode_fp8
+ * (kcache_fp8 uint8 [num_pages, 128, 128] codes, kscale fp32 [num_pages, 128]
+ * per-token scales, 16-byte aligned).  The keys are widened to f16 exactly
+ * and each query row is scaled to f16 by a power of two (exact for values
+ * within 2^-14..2^14 of the row's largest |q|) before the tensor-core
+ * product; the per-token scale multiplies each key's product before the max.
+ * Other arguments, layouts and errors as msa_indexer_prefill.  Two kernels.
+ */
+msa_status msa_indexer_prefill_fp8(const void *q, const int32_t *cu_seqlens_q, int total_q,
+                                   const void *kcache_fp8, const float *kscale, int64_t num_pages,
+                                   const int32_t *block_table, int64_t bt_stride,
+                                   const int32_t *seq_lens, int batch, int max_model_len, int k,
+                                   int n_sink, int n_window, int32_t *out_ids, float *out_scores,
+                                   float *out_block_scores, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/* The block-score half of msa_indexer_prefill_fp8 (see msa_indexer_prefill_score). */
+msa_status msa_indexer_prefill_score_fp8(const void *q, const int32_t *cu_seqlens_q, int total_q,
+                                         const void *kcache_fp8, const float *kscale,
+                                         int64_t num_pages, const int32_t *block_table,
+                                         int64_t bt_stride, const int32_t *seq_lens, int batch,
+                                         int max_model_len, float *out_block_scores,
+                                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * The block-score half of msa_indexer_prefill: writes out_block_scores
  * (required, fp32 [total_q, 4, ceil(max_model_len/128)], each token's
  * visible blocks only) and nothing else.  The workspace needs only its

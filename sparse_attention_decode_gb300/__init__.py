@@ -32,7 +32,9 @@ from ._binding import (  # noqa: F401
     msa_indexer_decode_mq_fp8,
     msa_indexer_decode_pages,
     msa_indexer_prefill,
+    msa_indexer_prefill_fp8,
     msa_indexer_prefill_score,
+    msa_indexer_prefill_score_fp8,
     msa_indexer_prefill_workspace_bytes,
     msa_indexer_workspace_bytes_mq,
     msa_indexer_score_fp8,

@@ -48,7 +48,9 @@ EXPORTED = (
     "msa_indexer_decode_mq_fp8",
     "msa_indexer_decode_pages",
     "msa_indexer_prefill",
+    "msa_indexer_prefill_fp8",
     "msa_indexer_prefill_score",
+    "msa_indexer_prefill_score_fp8",
     "msa_indexer_prefill_workspace_bytes",
 )
 
@@ -114,6 +116,12 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.msa_indexer_prefill_score.argtypes = [P, P, c_int, P, c_i64, P, c_i64, P, c_int, c_int, P,
                                               P, c_size, P]
     lib.msa_indexer_prefill_score.restype = c_int
+    lib.msa_indexer_prefill_fp8.argtypes = [P, P, c_int, P, P, c_i64, P, c_i64, P, c_int, c_int,
+                                            c_int, c_int, c_int, P, P, P, P, c_size, P]
+    lib.msa_indexer_prefill_fp8.restype = c_int
+    lib.msa_indexer_prefill_score_fp8.argtypes = [P, P, c_int, P, P, c_i64, P, c_i64, P, c_int,
+                                                  c_int, P, P, c_size, P]
+    lib.msa_indexer_prefill_score_fp8.restype = c_int
     lib.msa_status_string.argtypes = [c_int]
     lib.msa_status_string.restype = ctypes.c_char_p
     if path is None:
@@ -374,6 +382,45 @@ def msa_indexer_prefill_score(q, cu_seqlens_q, kcache_pool, block_table, seq_len
         max_model_len, _ptr(out_block_scores), _ptr(workspace),
         int(workspace.numel() * workspace.element_size()), _stream_ptr(stream))
     _check(st, "msa_indexer_prefill_score")
+
+
+def _prefill_fp8_args(q, cu_seqlens_q, kcache_fp8, kscale, block_table, seq_lens):
+    import torch
+    assert q.dtype == torch.bfloat16 and q.is_contiguous() and tuple(q.shape[1:]) == (4, 128)
+    assert cu_seqlens_q.dtype == torch.int32 and cu_seqlens_q.is_contiguous()
+    assert kcache_fp8.element_size() == 1 and kcache_fp8.is_contiguous(), "kcache_fp8: 1-byte E4M3 codes"
+    assert tuple(kcache_fp8.shape[1:]) == (MSA_PAGE_TOKENS, MSA_HEAD_DIM)
+    assert kscale.dtype == torch.float32 and kscale.is_contiguous()
+    assert tuple(kscale.shape) == tuple(kcache_fp8.shape[:2])
+    assert block_table.dtype == torch.int32 and block_table.stride(1) == 1
+    assert seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+
+
+def msa_indexer_prefill_fp8(q, cu_seqlens_q, kcache_fp8, kscale, block_table, seq_lens, k: int,
+                            n_sink: int, n_window: int, out_ids, out_scores, workspace, *,
+                            max_model_len: int, out_block_scores=None, stream=None) -> None:
+    """msa_indexer_prefill_fp8(): prefill scoring on the E4M3 cache."""
+    _prefill_fp8_args(q, cu_seqlens_q, kcache_fp8, kscale, block_table, seq_lens)
+    st = load().msa_indexer_prefill_fp8(
+        _ptr(q), _ptr(cu_seqlens_q), int(q.shape[0]), _ptr(kcache_fp8), _ptr(kscale),
+        int(kcache_fp8.shape[0]), _ptr(block_table), int(block_table.stride(0)), _ptr(seq_lens),
+        int(seq_lens.shape[0]), max_model_len, k, n_sink, n_window, _ptr(out_ids), _ptr(out_scores),
+        _ptr(out_block_scores), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+        _stream_ptr(stream))
+    _check(st, "msa_indexer_prefill_fp8")
+
+
+def msa_indexer_prefill_score_fp8(q, cu_seqlens_q, kcache_fp8, kscale, block_table, seq_lens,
+                                  out_block_scores, workspace, *, max_model_len: int,
+                                  stream=None) -> None:
+    """msa_indexer_prefill_score_fp8(): block scores only, on the E4M3 cache."""
+    _prefill_fp8_args(q, cu_seqlens_q, kcache_fp8, kscale, block_table, seq_lens)
+    st = load().msa_indexer_prefill_score_fp8(
+        _ptr(q), _ptr(cu_seqlens_q), int(q.shape[0]), _ptr(kcache_fp8), _ptr(kscale),
+        int(kcache_fp8.shape[0]), _ptr(block_table), int(block_table.stride(0)), _ptr(seq_lens),
+        int(seq_lens.shape[0]), max_model_len, _ptr(out_block_scores), _ptr(workspace),
+        int(workspace.numel() * workspace.element_size()), _stream_ptr(stream))
+    _check(st, "msa_indexer_prefill_score_fp8")
 
 
 def msa_indexer_get_error(workspace, *, stream=None) -> int:

@@ -58,8 +58,10 @@ constexpr uint32_t kQBytes = kMTiles * kQTileBytes;
 constexpr uint32_t kIdesc = umma_idesc_bf16_f32(kMRows, kPage);
 
 struct TcParams {
-    CUtensorMap kmap;  // pool as [num_pages*128][128] bf16, 64x128 boxes, 128B swizzle
+    CUtensorMap kmap;  // pool: bf16 [num_pages*128][128] in 64x128 boxes, or E4M3
+                       // codes [num_pages*128][128 B] in 128x128 boxes; 128B swizzle
     CUtensorMap qmap;  // q as [total_q*4][128] bf16, 64x128 boxes, 128B swizzle
+    const float *kscale;  // E4M3 cache: fp32 [num_pages, 128] per-token scales
     const int32_t *cu_q;
     const int32_t *block_table;
     const int32_t *seq_lens;
@@ -198,7 +200,8 @@ struct Cursor {
 
 // This CTA's range of work units: [W*g/G, W*(g+1)/G) of the batch's
 // (tile, page) units in order.  Run by one warp; writes the start and count.
-__device__ void plan_range(const TcParams &p, TcSmem *ctl, int lane)
+template <class Ctl>
+__device__ void plan_range(const TcParams &p, Ctl *ctl, int lane)
 {
     long long W = 0;
     for (int b0 = 0; b0 < p.batch; b0 += 32) {
@@ -256,12 +259,14 @@ __device__ void plan_range(const TcParams &p, TcSmem *ctl, int lane)
     }
 }
 
-__device__ __forceinline__ bool aborted(const TcSmem *ctl)
+template <class Ctl>
+__device__ __forceinline__ bool aborted(const Ctl *ctl)
 {
     return *reinterpret_cast<const volatile int *>(&ctl->abort) != 0;
 }
 
-__device__ __forceinline__ void give_up(const TcParams &p, TcSmem *ctl)
+template <class Ctl>
+__device__ __forceinline__ void give_up(const TcParams &p, Ctl *ctl)
 {
     atomicOr(p.fault, MSA_FAULT_TIMEOUT);
     *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
@@ -541,9 +546,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
 
 }  // namespace msa
 
+#include "prefill_fp8.cuh"
 #include "rows_topk.cuh"
 
 namespace msa {
+
+// 2-D tensor map over the E4M3 codes: [num_pages*128 rows][128 B], one
+// 128x128-byte box per page, 128-byte swizzle.
+static bool make_codes_map(CUtensorMap *map, const void *base, int64_t rows)
+{
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim)};
+    const cuuint32_t box[2] = {128u, 128u};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // 2-D bf16 tensor map over `rows` rows of 128 elements (256 B), 64x128 boxes,
 // 128-byte swizzle: two boxes fill one 128x128 operand tile.
@@ -576,14 +598,17 @@ extern "C" size_t msa_indexer_prefill_workspace_bytes(int max_total_q, int max_m
 // Checks the arguments and launches the score kernel; fills *pp (the block
 // score buffer it writes: the caller's, else the workspace's).
 static msa_status prefill_score_launch(const void *q, const int32_t *cu_seqlens_q, int total_q,
-                                       const void *kcache_pool, int64_t num_pages,
-                                       const int32_t *block_table, int64_t bt_stride,
-                                       const int32_t *seq_lens, int batch, int max_model_len,
-                                       float *out_block_scores, void *workspace,
-                                       size_t workspace_bytes, cudaStream_t st, TcParams *pp)
+                                       const void *kcache_pool, const float *kscale,
+                                       int64_t num_pages, const int32_t *block_table,
+                                       int64_t bt_stride, const int32_t *seq_lens, int batch,
+                                       int max_model_len, float *out_block_scores, void *workspace,
+                                       size_t workspace_bytes, cudaStream_t st, TcParams *pp,
+                                       bool fp8)
 {
     if ((!q && total_q > 0) || !cu_seqlens_q || !kcache_pool || !block_table || !seq_lens ||
         !workspace)
+        return MSA_ERR_INVALID_ARG;
+    if (fp8 && (!kscale || (reinterpret_cast<uintptr_t>(kscale) & 15)))
         return MSA_ERR_INVALID_ARG;
     if (total_q < 0 || batch < 1 || max_model_len < 1 || num_pages < 1 || bt_stride < 1)
         return MSA_ERR_INVALID_ARG;
@@ -611,6 +636,7 @@ static msa_status prefill_score_launch(const void *q, const int32_t *cu_seqlens_
     p.batch = batch;
     p.seq_limit = static_cast<int>(bt_stride * kPage < max_model_len ? bt_stride * kPage : max_model_len);
     p.total_q = total_q;
+    p.kscale = fp8 ? kscale : nullptr;
     if (total_q == 0)
         return MSA_OK;
     int dev = 0;
@@ -619,20 +645,28 @@ static msa_status prefill_score_launch(const void *q, const int32_t *cu_seqlens_
     const int sms = device_sms(dev);
     if (sms <= 0)
         return MSA_ERR_CUDA;
-    static std::atomic<bool> attr_done[kMaxDevices];
-    if (dev >= 0 && dev < kMaxDevices && !attr_done[dev].load(std::memory_order_acquire)) {
-        if (cudaFuncSetAttribute(tc_prefill_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kTcSmemBytes)) != cudaSuccess)
+    static std::atomic<bool> attr_done[2][kMaxDevices];
+    if (dev >= 0 && dev < kMaxDevices && !attr_done[fp8][dev].load(std::memory_order_acquire)) {
+        const cudaError_t e =
+            fp8 ? cudaFuncSetAttribute(tc_prefill_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kF8SmemBytes))
+                : cudaFuncSetAttribute(tc_prefill_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kTcSmemBytes));
+        if (e != cudaSuccess)
             return MSA_ERR_CUDA;
-        attr_done[dev].store(true, std::memory_order_release);
+        attr_done[fp8][dev].store(true, std::memory_order_release);
     }
-    if (!make_rows_map(&p.kmap, kcache_pool, num_pages * kPage) ||
-        !make_rows_map(&p.qmap, q, static_cast<int64_t>(total_q) * kHeads))
+    const bool maps = fp8 ? make_codes_map(&p.kmap, kcache_pool, num_pages * kPage)
+                          : make_rows_map(&p.kmap, kcache_pool, num_pages * kPage);
+    if (!maps || !make_rows_map(&p.qmap, q, static_cast<int64_t>(total_q) * kHeads))
         return MSA_ERR_CUDA;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(sms)), dim3(kTcThreads),
-                                        kTcSmemBytes, st, attr);
-    return cudaLaunchKernelEx(&cfg, tc_prefill_score_kernel, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(sms)),
+                                        dim3(fp8 ? kF8Threads : kTcThreads),
+                                        fp8 ? kF8SmemBytes : kTcSmemBytes, st, attr);
+    const cudaError_t e = fp8 ? cudaLaunchKernelEx(&cfg, tc_prefill_fp8_kernel, p)
+                              : cudaLaunchKernelEx(&cfg, tc_prefill_score_kernel, p);
+    return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 extern "C" msa_status msa_indexer_prefill_score(const void *q, const int32_t *cu_seqlens_q,
@@ -646,18 +680,19 @@ extern "C" msa_status msa_indexer_prefill_score(const void *q, const int32_t *cu
     if (!out_block_scores)
         return MSA_ERR_INVALID_ARG;
     TcParams p;
-    return prefill_score_launch(q, cu_seqlens_q, total_q, kcache_pool, num_pages, block_table,
-                                bt_stride, seq_lens, batch, max_model_len, out_block_scores,
-                                workspace, workspace_bytes, static_cast<cudaStream_t>(stream), &p);
+    return prefill_score_launch(q, cu_seqlens_q, total_q, kcache_pool, nullptr, num_pages,
+                                block_table, bt_stride, seq_lens, batch, max_model_len,
+                                out_block_scores, workspace, workspace_bytes,
+                                static_cast<cudaStream_t>(stream), &p, false);
 }
 
-extern "C" msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqlens_q, int total_q,
-                                          const void *kcache_pool, int64_t num_pages,
-                                          const int32_t *block_table, int64_t bt_stride,
-                                          const int32_t *seq_lens, int batch, int max_model_len,
-                                          int k, int n_sink, int n_window, int32_t *out_ids,
-                                          float *out_scores, float *out_block_scores,
-                                          void *workspace, size_t workspace_bytes, void *stream)
+static msa_status prefill_entry(const void *q, const int32_t *cu_seqlens_q, int total_q,
+                                const void *kcache_pool, const float *kscale, int64_t num_pages,
+                                const int32_t *block_table, int64_t bt_stride,
+                                const int32_t *seq_lens, int batch, int max_model_len, int k,
+                                int n_sink, int n_window, int32_t *out_ids, float *out_scores,
+                                float *out_block_scores, void *workspace, size_t workspace_bytes,
+                                void *stream, bool fp8)
 {
     if (!out_ids || !out_scores)
         return MSA_ERR_INVALID_ARG;
@@ -669,10 +704,10 @@ extern "C" msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqle
         return MSA_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     TcParams p;
-    const msa_status s = prefill_score_launch(q, cu_seqlens_q, total_q, kcache_pool, num_pages,
-                                              block_table, bt_stride, seq_lens, batch,
+    const msa_status s = prefill_score_launch(q, cu_seqlens_q, total_q, kcache_pool, kscale,
+                                              num_pages, block_table, bt_stride, seq_lens, batch,
                                               max_model_len, out_block_scores, workspace,
-                                              workspace_bytes, st, &p);
+                                              workspace_bytes, st, &p, fp8);
     if (s != MSA_OK || total_q == 0)
         return s;
     const int64_t rows = static_cast<int64_t>(total_q) * kHeads;
@@ -688,4 +723,50 @@ extern "C" msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqle
                                              p.bs_stride, cu_seqlens_q, seq_lens, batch, total_q,
                                              p.seq_limit, k, n_sink, n_window, out_ids, out_scores);
     return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+extern "C" msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqlens_q, int total_q,
+                                          const void *kcache_pool, int64_t num_pages,
+                                          const int32_t *block_table, int64_t bt_stride,
+                                          const int32_t *seq_lens, int batch, int max_model_len,
+                                          int k, int n_sink, int n_window, int32_t *out_ids,
+                                          float *out_scores, float *out_block_scores,
+                                          void *workspace, size_t workspace_bytes, void *stream)
+{
+    return prefill_entry(q, cu_seqlens_q, total_q, kcache_pool, nullptr, num_pages, block_table,
+                         bt_stride, seq_lens, batch, max_model_len, k, n_sink, n_window, out_ids,
+                         out_scores, out_block_scores, workspace, workspace_bytes, stream, false);
+}
+
+extern "C" msa_status msa_indexer_prefill_fp8(const void *q, const int32_t *cu_seqlens_q,
+                                              int total_q, const void *kcache_fp8,
+                                              const float *kscale, int64_t num_pages,
+                                              const int32_t *block_table, int64_t bt_stride,
+                                              const int32_t *seq_lens, int batch,
+                                              int max_model_len, int k, int n_sink, int n_window,
+                                              int32_t *out_ids, float *out_scores,
+                                              float *out_block_scores, void *workspace,
+                                              size_t workspace_bytes, void *stream)
+{
+    return prefill_entry(q, cu_seqlens_q, total_q, kcache_fp8, kscale, num_pages, block_table,
+                         bt_stride, seq_lens, batch, max_model_len, k, n_sink, n_window, out_ids,
+                         out_scores, out_block_scores, workspace, workspace_bytes, stream, true);
+}
+
+extern "C" msa_status msa_indexer_prefill_score_fp8(const void *q, const int32_t *cu_seqlens_q,
+                                                    int total_q, const void *kcache_fp8,
+                                                    const float *kscale, int64_t num_pages,
+                                                    const int32_t *block_table, int64_t bt_stride,
+                                                    const int32_t *seq_lens, int batch,
+                                                    int max_model_len, float *out_block_scores,
+                                                    void *workspace, size_t workspace_bytes,
+                                                    void *stream)
+{
+    if (!out_block_scores)
+        return MSA_ERR_INVALID_ARG;
+    TcParams p;
+    return prefill_score_launch(q, cu_seqlens_q, total_q, kcache_fp8, kscale, num_pages,
+                                block_table, bt_stride, seq_lens, batch, max_model_len,
+                                out_block_scores, workspace, workspace_bytes,
+                                static_cast<cudaStream_t>(stream), &p, true);
 }

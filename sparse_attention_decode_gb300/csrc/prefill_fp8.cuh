@@ -1,0 +1,467 @@
+// Prefill scoring on the E4M3 index-K cache (tcgen05, included by prefill.cu).
+//
+// One tcgen05.mma multiplies operands of one type, so neither the bf16
+// query nor the E4M3 keys can enter it as they are.  Both become f16, exactly:
+//  * an E4M3 code is exactly an f16 value (cvt.rn.f16x2.e4m3x2);
+//  * a query row is scaled by a power of two so its largest |q| lands in
+//    [2^13, 2^14) and rounded to f16 (exact for values within 2^-14..2^14 of
+//    that maximum: the same treatment as the fp8 decode path).
+// Products of f16 values are exact in the fp32 accumulators.  The per-token
+// scale multiplies each key's column of the accumulators before the masked
+// max, and the row's power of two is undone after it.
+//
+// Per CTA (persistent, one per SM; the same (tile, page) work split as the
+// bf16 kernel):
+//   warp 0       TMA producer: the tile's 256 bf16 query rows, and each page's
+//                16 KiB of codes (one 128x128-byte box) + 512 B of scales
+//                (one bulk copy) into a 3-stage raw ring;
+//   warp 1       one thread issues tcgen05.mma (f16, M = 128, N = 128, K = 16)
+//                for both M tiles against each converted page;
+//   warps 2-3    converters: two key rows per thread, E4M3 -> f16 into a
+//                3-stage operand ring (the 128-byte swizzle layout of a bf16
+//                TMA page), scales into an 8-slot ring;
+//   warps 4-11   epilogue: first its query row to f16 in place (per segment),
+//                then per page the scaled, masked block max.
+// (12 warps: three per SM sub-partition, whose 16K-register file then allows
+// up to 168 registers a thread.)
+#pragma once
+
+namespace msa {
+
+constexpr int kF8RawStages = 3;
+constexpr int kF8OpStages = 3;
+constexpr int kF8Ring = 8;                   // scale slots, one page each
+constexpr int kF8ConvWarps = 2;              // two key rows per thread
+constexpr int kF8FirstEpiWarp = 2 + kF8ConvWarps;
+constexpr int kF8Threads = 32 * (kF8FirstEpiWarp + kEpiWarps);
+constexpr uint32_t kF8RawBytes = kPage * kDim;  // 16 KiB of codes
+constexpr uint32_t kF8ScaleBytes = kPage * 4;   // 512 B
+constexpr uint32_t kIdescF16 = umma_idesc_f16_f32(kMRows, kPage);
+
+struct F8Smem {
+    uint64_t raw_full[kF8RawStages];   // codes + scales landed (TMA bytes)
+    uint64_t raw_empty[kF8RawStages];  // converted (converter warps)
+    uint64_t op_full[kF8OpStages];     // f16 page written (converter warps)
+    uint64_t op_empty[kF8OpStages];    // multiplied (MMA commit)
+    uint64_t sc_full[kF8Ring];         // scales copied (converter warps)
+    uint64_t sc_empty[kF8Ring];        // scales used (epilogue warps)
+    uint64_t q_full;                   // bf16 query tile landed (TMA bytes)
+    uint64_t q_conv;                   // query tile converted (epilogue warps)
+    uint64_t q_empty;                  // multiplied (MMA commit)
+    uint64_t acc_full[kAccBufs];
+    uint64_t acc_empty[kAccBufs];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+    int b0, t0, j0;
+    long long units;
+};
+
+// Shared memory: query tile | operand ring | raw ring | raw scales | scale ring | control.
+constexpr uint32_t kF8OpOff = kQBytes;
+constexpr uint32_t kF8RawOff = kF8OpOff + kF8OpStages * kPageBytes;
+constexpr uint32_t kF8RawScOff = kF8RawOff + kF8RawStages * kF8RawBytes;
+constexpr uint32_t kF8RingOff = kF8RawScOff + kF8RawStages * kF8ScaleBytes;
+constexpr uint32_t kF8CtlOff = kF8RingOff + kF8Ring * kF8ScaleBytes;
+constexpr size_t kF8SmemBytes = 1024 /* alignment slack */ + kF8CtlOff + sizeof(F8Smem);
+static_assert(kF8OpOff % 1024 == 0 && kF8RawOff % 1024 == 0, "swizzled tiles need 1 KiB alignment");
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Four E4M3 codes (byte i -> element i) -> two f16x2 words, exactly.
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    lo = e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xffffu));
+    hi = e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16));
+}
+
+// bf16 pair -> f32 pair.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__global__ void __launch_bounds__(kF8Threads, 1) tc_prefill_fp8_kernel(const __grid_constant__ TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t q_smem = smem_addr(smem);
+    const uint32_t op_smem = q_smem + kF8OpOff;
+    const uint32_t raw_smem = q_smem + kF8RawOff;
+    const uint32_t rawsc_smem = q_smem + kF8RawScOff;
+    float *ring = reinterpret_cast<float *>(smem + kF8RingOff);
+    F8Smem *ctl = reinterpret_cast<F8Smem *>(smem + kF8CtlOff);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kF8RawStages; ++s) {
+            mbar_init(smem_addr(&ctl->raw_full[s]), 1);
+            mbar_init(smem_addr(&ctl->raw_empty[s]), kF8ConvWarps);
+        }
+        for (int s = 0; s < kF8OpStages; ++s) {
+            mbar_init(smem_addr(&ctl->op_full[s]), kF8ConvWarps);
+            mbar_init(smem_addr(&ctl->op_empty[s]), 1);
+        }
+        for (int s = 0; s < kF8Ring; ++s) {
+            mbar_init(smem_addr(&ctl->sc_full[s]), kF8ConvWarps);
+            mbar_init(smem_addr(&ctl->sc_empty[s]), kEpiWarps);
+        }
+        mbar_init(smem_addr(&ctl->q_full), 1);
+        mbar_init(smem_addr(&ctl->q_conv), kEpiWarps);
+        mbar_init(smem_addr(&ctl->q_empty), 1);
+        for (int a = 0; a < kAccBufs; ++a) {
+            mbar_init(smem_addr(&ctl->acc_full[a]), 1);
+            mbar_init(smem_addr(&ctl->acc_empty[a]), kEpiWarps);
+        }
+        mbar_init(smem_addr(&ctl->mma_done), 1);
+        ctl->abort = 0;
+        fence_barrier_init();
+    }
+    griddep_wait();
+    griddep_launch_dependents();
+    if (warp == 0)
+        plan_range(p, ctl, lane);
+    __syncthreads();
+    const long long units = ctl->units;
+    if (units <= 0)
+        return;  // uniform: no TMEM taken yet
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish_alloc_permit();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = ctl->tmem_base;
+    const int sb = ctl->b0, st = ctl->t0, sj = ctl->j0;
+
+    if (warp == 0) {
+        // ---------------- producer: query tiles and raw pages ----------------
+        Cursor c;
+        c.load(p, sb, st, sj);
+        long long left = units;
+        uint32_t kc = 0, seg = 0;
+        bool ok_run = true;
+        while (left > 0 && ok_run) {
+            const int nb = tile_pages(c.r, c.t);
+            const int je = static_cast<int>(min(static_cast<long long>(nb), c.j + left));
+            if (lane == 0) {
+                if (seg > 0 && !mbar_wait(smem_addr(&ctl->q_empty), (seg - 1) & 1u)) {
+                    give_up(p, ctl);
+                    ok_run = false;
+                } else {
+                    const uint32_t qf = smem_addr(&ctl->q_full);
+                    const int row0 = (c.r.c0 + kTileTokens * c.t) * kHeads;
+                    mbar_arrive_expect_tx(qf, kQBytes);
+#pragma unroll
+                    for (int mt = 0; mt < kMTiles; ++mt)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_2d(q_smem + mt * kQTileBytes + h * kHalfPageBytes, &p.qmap, 64 * h,
+                                        row0 + mt * kMRows, qf);
+                }
+            }
+            ok_run = __shfl_sync(0xffffffffu, ok_run ? 1 : 0, 0) != 0;
+            for (int jb = c.j; jb < je && ok_run; jb += 32) {
+                const int jl = jb + lane;
+                int page = 0, ok = 0;
+                if (jl < je) {
+                    page = p.block_table[static_cast<int64_t>(c.b) * p.bt_stride + jl];
+                    ok = (page >= 0 && page < p.num_pages) ? 1 : 0;
+                    if (!ok)
+                        atomicOr(p.fault, MSA_FAULT_PAGE_ID);
+                }
+                const int cnt = min(32, je - jb);
+                for (int i = 0; i < cnt; ++i) {
+                    const int pg = __shfl_sync(0xffffffffu, page, i);
+                    const int pok = __shfl_sync(0xffffffffu, ok, i);
+                    int good = 1;
+                    if (lane == 0) {
+                        const int s = static_cast<int>(kc % kF8RawStages);
+                        const uint32_t full = smem_addr(&ctl->raw_full[s]);
+                        if (aborted(ctl) ||
+                            (kc >= kF8RawStages &&
+                             !mbar_wait(smem_addr(&ctl->raw_empty[s]), ((kc / kF8RawStages) - 1) & 1u))) {
+                            give_up(p, ctl);
+                            good = 0;
+                        } else if (pok) {
+                            mbar_arrive_expect_tx(full, kF8RawBytes + kF8ScaleBytes);
+                            tma_load_2d(raw_smem + s * kF8RawBytes, &p.kmap, 0, pg * kPage, full);
+                            bulk_load_hint(rawsc_smem + s * kF8ScaleBytes,
+                                           p.kscale + static_cast<size_t>(pg) * kPage, kF8ScaleBytes,
+                                           full, l2_evict_first_policy());
+                        } else {
+                            mbar_arrive(full);  // nothing to load; the epilogue writes -inf
+                        }
+                    }
+                    if (__shfl_sync(0xffffffffu, good, 0) == 0) {
+                        ok_run = false;
+                        break;
+                    }
+                    ++kc;
+                }
+            }
+            ++seg;
+            left -= je - c.j;
+            if (left > 0 && !c.next(p))
+                break;
+        }
+        if (lane == 0) {  // drain: no copy may land after the CTA exits
+            for (uint32_t i = kc > kF8RawStages ? kc - kF8RawStages : 0; i < kc; ++i)
+                if (!mbar_wait(smem_addr(&ctl->raw_full[i % kF8RawStages]), (i / kF8RawStages) & 1u))
+                    give_up(p, ctl);
+            if (seg > 0 && !mbar_wait(smem_addr(&ctl->q_full), (seg - 1) & 1u))
+                give_up(p, ctl);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issue (one thread) ----------------
+        if (lane == 0) {
+            Cursor c;
+            c.load(p, sb, st, sj);
+            long long left = units;
+            uint32_t kc = 0, ac = 0, seg = 0;
+            bool ok_run = true;
+            while (left > 0 && ok_run) {
+                const int nb = tile_pages(c.r, c.t);
+                const int je = static_cast<int>(min(static_cast<long long>(nb), c.j + left));
+                if (!mbar_wait(smem_addr(&ctl->q_conv), seg & 1u)) {
+                    give_up(p, ctl);
+                    break;
+                }
+                tc_fence_after_sync();
+                const int live_tokens = min(kTileTokens, c.r.n - kTileTokens * c.t);
+                const int nmt = (live_tokens * kHeads + kMRows - 1) / kMRows;
+                for (int j = c.j; j < je; ++j) {
+                    const int s = static_cast<int>(kc % kF8OpStages);
+                    const int a = static_cast<int>(ac % kAccBufs);
+                    if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->op_full[s]), (kc / kF8OpStages) & 1u) ||
+                        (ac >= kAccBufs &&
+                         !mbar_wait(smem_addr(&ctl->acc_empty[a]), ((ac / kAccBufs) - 1) & 1u))) {
+                        give_up(p, ctl);
+                        ok_run = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t kst = op_smem + s * kPageBytes;
+                    for (int mt = 0; mt < nmt; ++mt) {
+                        const uint32_t d = tmem + static_cast<uint32_t>(a * kMTiles * kPage + mt * kPage);
+#pragma unroll
+                        for (int ks = 0; ks < kDim / 16; ++ks) {
+                            const uint32_t off = (ks >> 2) * kHalfPageBytes + (ks & 3) * 32;
+                            umma_bf16(d, umma_desc_sw128(q_smem + mt * kQTileBytes + off),
+                                      umma_desc_sw128(kst + off), kIdescF16, ks > 0 ? 1u : 0u);
+                        }
+                    }
+                    umma_commit(smem_addr(&ctl->op_empty[s]));
+                    umma_commit(smem_addr(&ctl->acc_full[a]));
+                    ++kc;
+                    ++ac;
+                }
+                umma_commit(smem_addr(&ctl->q_empty));
+                ++seg;
+                left -= je - c.j;
+                if (left > 0 && !c.next(p))
+                    break;
+            }
+            umma_commit(smem_addr(&ctl->mma_done));
+            if (!mbar_wait(smem_addr(&ctl->mma_done), 0))
+                give_up(p, ctl);
+        }
+        __syncwarp();
+    } else if (warp < kF8FirstEpiWarp) {
+        // ---------------- converters: E4M3 page -> f16 operand ----------------
+        const int kr0 = static_cast<int>(threadIdx.x) - 64;  // key rows kr0 and kr0 + 64
+        for (long long pc = 0; pc < units; ++pc) {
+            const uint32_t u = static_cast<uint32_t>(pc);
+            const int rs = static_cast<int>(u % kF8RawStages);
+            const int os = static_cast<int>(u % kF8OpStages);
+            const int slot = static_cast<int>(u % kF8Ring);
+            bool ready = !aborted(ctl) && mbar_wait(smem_addr(&ctl->raw_full[rs]), (u / kF8RawStages) & 1u);
+            ready = ready && (u < kF8OpStages ||
+                              mbar_wait(smem_addr(&ctl->op_empty[os]), ((u / kF8OpStages) - 1) & 1u));
+            ready = ready && (u < kF8Ring ||
+                              mbar_wait(smem_addr(&ctl->sc_empty[slot]), ((u / kF8Ring) - 1) & 1u));
+            ready = __all_sync(0xffffffffu, ready);
+            if (!ready) {
+                if (lane == 0)
+                    give_up(p, ctl);
+                break;
+            }
+#pragma unroll
+            for (int rh = 0; rh < 2; ++rh) {
+                const int kr = kr0 + 64 * rh;
+                const uint32_t swz = static_cast<uint32_t>(kr & 7);
+                const uint32_t src = raw_smem + rs * kF8RawBytes + static_cast<uint32_t>(kr) * 128;
+                const uint32_t dst = op_smem + os * kPageBytes + static_cast<uint32_t>(kr) * 128;
+#pragma unroll
+                for (int cch = 0; cch < 8; ++cch) {
+                    // codes of dims 16 cch .. 16 cch + 15 -> f16 chunks 2 cch, 2 cch + 1
+                    // (dims 16 cch + 8 i .. + 7) of half cch / 4
+                    const uint4 v = lds128(src + ((static_cast<uint32_t>(cch) ^ swz) << 4));
+                    uint4 f0, f1;
+                    e4m3x4_to_f16(v.x, f0.x, f0.y);
+                    e4m3x4_to_f16(v.y, f0.z, f0.w);
+                    e4m3x4_to_f16(v.z, f1.x, f1.y);
+                    e4m3x4_to_f16(v.w, f1.z, f1.w);
+                    const uint32_t half = static_cast<uint32_t>(cch >> 2) * kHalfPageBytes;
+                    const uint32_t c0 = static_cast<uint32_t>((cch & 3) * 2);
+                    sts128(dst + half + ((c0 ^ swz) << 4), f0);
+                    sts128(dst + half + (((c0 + 1) ^ swz) << 4), f1);
+                }
+                ring[slot * kPage + kr] = reinterpret_cast<const float *>(smem + kF8RawScOff)[rs * kPage + kr];
+            }
+            fence_proxy_async_smem();  // the f16 page is read by the tensor cores
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_addr(&ctl->op_full[os]));
+                mbar_arrive(smem_addr(&ctl->raw_empty[rs]));
+                mbar_arrive(smem_addr(&ctl->sc_full[slot]));
+            }
+        }
+    } else {
+        // ---------------- epilogue: query row to f16, then block scores ----------------
+        const int e = warp - kF8FirstEpiWarp;
+        const int quarter = warp & 3;        // TMEM lanes this warp may read
+        const int mt = e >> 2;               // M tile of this warp
+        const int rr = 32 * quarter + lane;  // row within the M tile
+        const int row_in_tile = mt * kMRows + rr;
+        const uint32_t qrow = q_smem + static_cast<uint32_t>(mt) * kQTileBytes + static_cast<uint32_t>(rr) * 128;
+        const uint32_t qswz = static_cast<uint32_t>(rr & 7);
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16) +
+                                   static_cast<uint32_t>(mt * kPage);
+        const float neg_inf = -__int_as_float(0x7f800000);
+        Cursor c;
+        c.load(p, sb, st, sj);
+        long long left = units;
+        uint32_t ac = 0, seg = 0;
+        bool ok_run = true;
+        while (left > 0 && ok_run) {
+            const int nb = tile_pages(c.r, c.t);
+            const int je = static_cast<int>(min(static_cast<long long>(nb), c.j + left));
+            // this row of the segment's query tile to f16, scaled by 2^sh
+            bool qready = !aborted(ctl) && mbar_wait(smem_addr(&ctl->q_full), seg & 1u);
+            qready = __all_sync(0xffffffffu, qready);
+            if (!qready) {
+                if (lane == 0)
+                    give_up(p, ctl);
+                break;
+            }
+            float amax = 0.0f;  // pass 1: the row's largest |q|
+#pragma unroll 4
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t half = static_cast<uint32_t>(i >> 3) * kHalfPageBytes;
+                const uint4 v = lds128(qrow + half + ((static_cast<uint32_t>(i & 7) ^ qswz) << 4));
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[t])), fabsf(bf16_hi(w[t]))));
+            }
+            int ex = 0;
+            if (amax > 0.0f)
+                frexpf(amax, &ex);  // amax = m * 2^ex, m in [0.5, 1)
+            const int sh = max(-100, min(100, 14 - ex));
+            const float up = __int_as_float((127 + sh) << 23);
+            const float inv_row = __int_as_float((127 - sh) << 23);
+#pragma unroll 4
+            for (int i = 0; i < 16; ++i) {  // pass 2: scale, round to f16, write back in place
+                const uint32_t half = static_cast<uint32_t>(i >> 3) * kHalfPageBytes;
+                const uint32_t addr = qrow + half + ((static_cast<uint32_t>(i & 7) ^ qswz) << 4);
+                const uint4 v = lds128(addr);
+                uint4 o;
+                o.x = f32x2_to_f16x2(bf16_lo(v.x) * up, bf16_hi(v.x) * up);
+                o.y = f32x2_to_f16x2(bf16_lo(v.y) * up, bf16_hi(v.y) * up);
+                o.z = f32x2_to_f16x2(bf16_lo(v.z) * up, bf16_hi(v.z) * up);
+                o.w = f32x2_to_f16x2(bf16_lo(v.w) * up, bf16_hi(v.w) * up);
+                sts128(addr, o);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&ctl->q_conv));
+
+            const int tl = kTileTokens * c.t + (row_in_tile >> 2);  // token within the request's new ones
+            const int head = row_in_tile & 3;
+            const bool live = tl < c.r.n;
+            const int pos = c.r.len - c.r.n + tl;
+            float *out = p.scores + (static_cast<int64_t>(c.r.c0 + tl) * kHeads + head) * p.bs_stride;
+            for (int j = c.j; j < je; ++j) {
+                const int a = static_cast<int>(ac % kAccBufs);
+                const int slot = static_cast<int>(ac % kF8Ring);
+                bool ready = !aborted(ctl) &&
+                             mbar_wait(smem_addr(&ctl->acc_full[a]), (ac / kAccBufs) & 1u) &&
+                             mbar_wait(smem_addr(&ctl->sc_full[slot]), (ac / kF8Ring) & 1u);
+                ready = __all_sync(0xffffffffu, ready);
+                if (!ready) {
+                    if (lane == 0)
+                        give_up(p, ctl);
+                    ok_run = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const int page = p.block_table[static_cast<int64_t>(c.b) * p.bt_stride + j];
+                const bool page_ok = page >= 0 && page < p.num_pages;
+                const int first_key = j * kPage;
+                const bool want = live && first_key <= pos;
+                if (page_ok && __any_sync(0xffffffffu, want)) {
+                    const float4 *scl = reinterpret_cast<const float4 *>(ring + slot * kPage);
+                    float mx = neg_inf;
+#pragma unroll
+                    for (int q4 = 0; q4 < kPage / 32; ++q4) {
+                        uint32_t r[32];
+                        tmem_ld32(lane_addr + static_cast<uint32_t>(a * kMTiles * kPage + 32 * q4), r);
+                        tmem_wait_ld(r);
+                        const int lim = pos - (first_key + 32 * q4);  // keys i <= lim are visible
+#pragma unroll
+                        for (int i4 = 0; i4 < 8; ++i4) {
+                            const float4 s4 = scl[8 * q4 + i4];
+                            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const int i = 4 * i4 + t;
+                                const float v = __uint_as_float(r[i]) * sv[t];
+                                mx = fmaxf(mx, i <= lim ? v : neg_inf);
+                            }
+                        }
+                    }
+                    if (want)
+                        out[j] = mx * inv_row;
+                } else if (!page_ok && want) {
+                    out[j] = neg_inf;
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(smem_addr(&ctl->acc_empty[a]));
+                    mbar_arrive(smem_addr(&ctl->sc_empty[slot]));
+                }
+                ++ac;
+            }
+            ++seg;
+            left -= je - c.j;
+            if (left > 0 && !c.next(p))
+                break;
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace msa

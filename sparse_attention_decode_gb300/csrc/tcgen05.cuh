@@ -72,6 +72,15 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16_f32(int m, int n)
            | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
 }
 
+// Instruction descriptor of kind::f16 with f16 A and B (both K-major) and an
+// fp32 accumulator, shape M x N (K = 16).
+__host__ __device__ constexpr uint32_t umma_idesc_f16_f32(int m, int n)
+{
+    return (1u << 4)                                   // D: fp32
+           | (static_cast<uint32_t>(n >> 3) << 17)     // N / 8 (A, B: f16 = 0)
+           | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate)
