@@ -17,13 +17,13 @@
 //                (one bulk copy) into a 3-stage raw ring;
 //   warp 1       one thread issues tcgen05.mma (f16, M = 128, N = 128, K = 16)
 //                for both M tiles against each converted page;
-//   warps 2-3    converters: two key rows per thread, E4M3 -> f16 into a
+//   warps 2-5    converters: one key row per thread, E4M3 -> f16 into a
 //                3-stage operand ring (the 128-byte swizzle layout of a bf16
 //                TMA page), scales into an 8-slot ring;
-//   warps 4-11   epilogue: first its query row to f16 in place (per segment),
+//   warps 6-13   epilogue: first its query row to f16 in place (per segment),
 //                then per page the scaled, masked block max.
-// (12 warps: three per SM sub-partition, whose 16K-register file then allows
-// up to 168 registers a thread.)
+// (14 warps: up to four on one SM sub-partition, whose 16K-register file then
+// allows 128 registers a thread; the launch bound keeps the kernel there.)
 #pragma once
 
 namespace msa {
@@ -31,7 +31,7 @@ namespace msa {
 constexpr int kF8RawStages = 3;
 constexpr int kF8OpStages = 3;
 constexpr int kF8Ring = 8;                   // scale slots, one page each
-constexpr int kF8ConvWarps = 2;              // two key rows per thread
+constexpr int kF8ConvWarps = 4;              // one key row per thread, one warp per SM sub-partition
 constexpr int kF8FirstEpiWarp = 2 + kF8ConvWarps;
 constexpr int kF8Threads = 32 * (kF8FirstEpiWarp + kEpiWarps);
 constexpr uint32_t kF8RawBytes = kPage * kDim;  // 16 KiB of codes
@@ -89,11 +89,26 @@ __device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &lo, uint32_t
     hi = e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16));
 }
 
+// Two fp32 products in one instruction (packed f32x2 multiply, sm_100+).
+__device__ __forceinline__ void mul2(float a0, float a1, float b0, float b1, float &d0, float &d1)
+{
+    uint64_t a, b, d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(b0), "f"(b1));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+
 // bf16 pair -> f32 pair.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__global__ void __launch_bounds__(kF8Threads, 1) tc_prefill_fp8_kernel(const __grid_constant__ TcParams p)
+// 14 warps leave four on one SM sub-partition, whose 16K registers then hold
+// 128 a thread; the cap keeps the launch inside that.
+constexpr int kF8MaxRegs = 16384 / (32 * ((kF8Threads / 32 + 3) / 4));
+static_assert(kF8MaxRegs >= 96, "too many warps for the register file");
+
+__global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_constant__ TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -283,7 +298,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) tc_prefill_fp8_kernel(const __g
         __syncwarp();
     } else if (warp < kF8FirstEpiWarp) {
         // ---------------- converters: E4M3 page -> f16 operand ----------------
-        const int kr0 = static_cast<int>(threadIdx.x) - 64;  // key rows kr0 and kr0 + 64
+        const int kr0 = static_cast<int>(threadIdx.x) - 64;  // this thread's key row
         for (long long pc = 0; pc < units; ++pc) {
             const uint32_t u = static_cast<uint32_t>(pc);
             const int rs = static_cast<int>(u % kF8RawStages);
@@ -300,9 +315,8 @@ __global__ void __launch_bounds__(kF8Threads, 1) tc_prefill_fp8_kernel(const __g
                     give_up(p, ctl);
                 break;
             }
-#pragma unroll
-            for (int rh = 0; rh < 2; ++rh) {
-                const int kr = kr0 + 64 * rh;
+            {
+                const int kr = kr0;
                 const uint32_t swz = static_cast<uint32_t>(kr & 7);
                 const uint32_t src = raw_smem + rs * kF8RawBytes + static_cast<uint32_t>(kr) * 128;
                 const uint32_t dst = op_smem + os * kPageBytes + static_cast<uint32_t>(kr) * 128;
@@ -424,15 +438,33 @@ __global__ void __launch_bounds__(kF8Threads, 1) tc_prefill_fp8_kernel(const __g
                         tmem_ld32(lane_addr + static_cast<uint32_t>(a * kMTiles * kPage + 32 * q4), r);
                         tmem_wait_ld(r);
                         const int lim = pos - (first_key + 32 * q4);  // keys i <= lim are visible
+                        if (lim >= 31) {
+                            float m4[4] = {neg_inf, neg_inf, neg_inf, neg_inf};
 #pragma unroll
-                        for (int i4 = 0; i4 < 8; ++i4) {
-                            const float4 s4 = scl[8 * q4 + i4];
-                            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+                            for (int i4 = 0; i4 < 8; ++i4) {
+                                const float4 s4 = scl[8 * q4 + i4];
+                                float v0, v1, v2, v3;
+                                mul2(__uint_as_float(r[4 * i4]), __uint_as_float(r[4 * i4 + 1]), s4.x, s4.y,
+                                     v0, v1);
+                                mul2(__uint_as_float(r[4 * i4 + 2]), __uint_as_float(r[4 * i4 + 3]), s4.z,
+                                     s4.w, v2, v3);
+                                m4[0] = fmaxf(m4[0], v0);
+                                m4[1] = fmaxf(m4[1], v1);
+                                m4[2] = fmaxf(m4[2], v2);
+                                m4[3] = fmaxf(m4[3], v3);
+                            }
+                            mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                        } else {
 #pragma unroll
-                            for (int t = 0; t < 4; ++t) {
-                                const int i = 4 * i4 + t;
-                                const float v = __uint_as_float(r[i]) * sv[t];
-                                mx = fmaxf(mx, i <= lim ? v : neg_inf);
+                            for (int i4 = 0; i4 < 8; ++i4) {
+                                const float4 s4 = scl[8 * q4 + i4];
+                                const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                                for (int t = 0; t < 4; ++t) {
+                                    const int i = 4 * i4 + t;
+                                    const float v = __uint_as_float(r[i]) * sv[t];
+                                    mx = fmaxf(mx, i <= lim ? v : neg_inf);
+                                }
                             }
                         }
                     }
