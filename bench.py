@@ -38,7 +38,9 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_SUMMARY = {"bf16": os.path.join(ROOT, "profiles", "score_kernel_long_context.md"),
                    "fp8": os.path.join(ROOT, "profiles", "score_kernel_fp8_long_context.md"),
-                   "prefill": os.path.join(ROOT, "profiles", "prefill_kernel_chunked_128k.md")}
+                   "prefill": os.path.join(ROOT, "profiles", "prefill_kernel_chunked_128k.md"),
+                   "prefill_fp8": os.path.join(ROOT, "profiles",
+                                               "prefill_fp8_kernel_chunked_128k.md")}
 PREFILL_METRIC = "prefill index-score TFLOP/s (4 x 2048 new tokens at 128K ctx) vs GB300 bf16 peak"
 PREFILL_PAIRS = [(2048, 131072)] * 4  # (new tokens, tokens) per request
 CSRC = os.path.join(ROOT, "sparse_attention_decode_gb300", "csrc")
@@ -137,11 +139,14 @@ DECODE_SOURCES = ("host_util.cuh", "keys.cuh", "layout.cuh", "msa_indexer.cu", "
 PREFILL_SOURCES = ("host_util.cuh", "keys.cuh", "layout.cuh", "prefill.cu", "ptx.cuh",
                    "tcgen05.cuh", os.path.join("..", "..", "include", "msa_indexer.h"))
 
+PREFILL_FP8_SOURCES = PREFILL_SOURCES + ("prefill_fp8.cuh",)
+
 
 def kernel_source_hash(path: str = "decode") -> str:
     """Hash of a path's kernel sources: a profile taken at another hash is stale."""
     h = hashlib.sha256()
-    for name in (PREFILL_SOURCES if path == "prefill" else DECODE_SOURCES):
+    names = {"prefill": PREFILL_SOURCES, "prefill_fp8": PREFILL_FP8_SOURCES}.get(path, DECODE_SOURCES)
+    for name in names:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -156,7 +161,7 @@ def profiled_traffic(batch: int, cache: str = "bf16"):
         return None
     m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
     m_bytes = re.search(r"dram_bytes_per_launch_full_batch:\s*([0-9]+)", text)
-    path = "prefill" if cache == "prefill" else "decode"
+    path = cache if cache.startswith("prefill") else "decode"
     if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(path):
         return None
     return int(m_bytes.group(1)) * batch // 32
@@ -678,7 +683,7 @@ def run_prefill_bench(args):
             "bound": "tensor", "kernel": "tc_prefill_fp8_kernel" if fp8 else "tc_prefill_score_kernel",
             "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src,
             "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-            "traffic": None if fp8 else profiled_traffic(32, "prefill"),
+            "traffic": profiled_traffic(32, "prefill_fp8" if fp8 else "prefill"),
             "score_us": round(score_ms * 1e3, 2),
         },
         "gpu_launches": 2 * args.steps,

@@ -291,15 +291,21 @@ __device__ __forceinline__ bool mma_pages(const TcParams &p, TcSmem *ctl, uint32
             return false;
         }
         tc_fence_after_sync();
-        const uint32_t kst = k_smem + s * kPageBytes;
+        // descriptors as base low words plus byte offsets >> 4: one integer add
+        // per operand keeps the single issuing thread ahead of the tensor pipe
+        const uint32_t a_lo = umma_desc_lo(q_smem);
+        const uint32_t b_lo = umma_desc_lo(k_smem + s * kPageBytes);
+        const uint32_t d0 = tmem + static_cast<uint32_t>(a * kMTiles * kPage);
 #pragma unroll
         for (int mt = 0; mt < NMT; ++mt) {
-            const uint32_t d = tmem + static_cast<uint32_t>(a * kMTiles * kPage + mt * kPage);
 #pragma unroll
             for (int ks = 0; ks < kDim / 16; ++ks) {
-                const uint32_t off = (ks >> 2) * kHalfPageBytes + (ks & 3) * 32;
-                umma_bf16(d, umma_desc_sw128(q_smem + mt * kQTileBytes + off),
-                          umma_desc_sw128(kst + off), kIdesc, ks > 0 ? 1u : 0u);
+                const uint32_t off = ((ks >> 2) * kHalfPageBytes + (ks & 3) * 32) >> 4;
+                const uint32_t qo = (mt * kQTileBytes) >> 4;
+                if (ks == 0)
+                    umma_f16<false>(d0 + mt * kPage, a_lo + qo + off, b_lo + off, kIdesc);
+                else
+                    umma_f16<true>(d0 + mt * kPage, a_lo + qo + off, b_lo + off, kIdesc);
             }
         }
         umma_commit(smem_addr(&ctl->k_empty[s]));

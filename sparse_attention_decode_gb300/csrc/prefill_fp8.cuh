@@ -99,6 +99,35 @@ __device__ __forceinline__ void mul2(float a0, float a1, float b0, float b1, flo
     asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
 }
 
+// Scaled maximum over one 16x256b.x4 TMEM load (tmem_ld16x256b_x4): r holds
+// rows g and g + 8 of a 16-row block at the 8 columns 8 i + 2 c + {0, 1} of a
+// 32-column chunk (g = lane / 4, c = lane % 4); sc points at the chunk's
+// per-key scales as pairs.  Folds the products of row g into ma and of row
+// g + 8 into mb; with MASK, column kbase + k counts for row g only if
+// kbase + k <= lim_a (row g + 8: lim_b), the causal edge.
+template <bool MASK>
+__device__ __forceinline__ void scaled_max_frag(const uint32_t (&r)[16], const float2 *sc, int c, int kbase,
+                                                int lim_a, int lim_b, float &ma, float &mb)
+{
+    const float neg_inf = -__int_as_float(0x7f800000);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 si = sc[4 * i + c];
+        float v0, v1, v2, v3;
+        mul2(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]), si.x, si.y, v0, v1);
+        mul2(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]), si.x, si.y, v2, v3);
+        if (MASK) {
+            const int k0 = kbase + 8 * i + 2 * c;
+            v0 = k0 <= lim_a ? v0 : neg_inf;
+            v1 = k0 + 1 <= lim_a ? v1 : neg_inf;
+            v2 = k0 <= lim_b ? v2 : neg_inf;
+            v3 = k0 + 1 <= lim_b ? v3 : neg_inf;
+        }
+        ma = fmaxf(ma, fmaxf(v0, v1));
+        mb = fmaxf(mb, fmaxf(v2, v3));
+    }
+}
+
 // bf16 pair -> f32 pair.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -270,14 +299,21 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t kst = op_smem + s * kPageBytes;
-                    for (int mt = 0; mt < nmt; ++mt) {
-                        const uint32_t d = tmem + static_cast<uint32_t>(a * kMTiles * kPage + mt * kPage);
+                    const uint32_t a_lo = umma_desc_lo(q_smem);
+                    const uint32_t b_lo = umma_desc_lo(op_smem + s * kPageBytes);
+                    const uint32_t d0 = tmem + static_cast<uint32_t>(a * kMTiles * kPage);
 #pragma unroll
-                        for (int ks = 0; ks < kDim / 16; ++ks) {
-                            const uint32_t off = (ks >> 2) * kHalfPageBytes + (ks & 3) * 32;
-                            umma_bf16(d, umma_desc_sw128(q_smem + mt * kQTileBytes + off),
-                                      umma_desc_sw128(kst + off), kIdescF16, ks > 0 ? 1u : 0u);
+                    for (int mt = 0; mt < kMTiles; ++mt) {
+                        if (mt < nmt) {
+#pragma unroll
+                            for (int ks = 0; ks < kDim / 16; ++ks) {
+                                const uint32_t off = ((ks >> 2) * kHalfPageBytes + (ks & 3) * 32) >> 4;
+                                const uint32_t qo = (mt * kQTileBytes) >> 4;
+                                if (ks == 0)
+                                    umma_f16<false>(d0 + mt * kPage, a_lo + qo + off, b_lo + off, kIdescF16);
+                                else
+                                    umma_f16<true>(d0 + mt * kPage, a_lo + qo + off, b_lo + off, kIdescF16);
+                            }
                         }
                     }
                     umma_commit(smem_addr(&ctl->op_empty[s]));
@@ -350,8 +386,7 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
         const int e = warp - kF8FirstEpiWarp;
         const int quarter = warp & 3;        // TMEM lanes this warp may read
         const int mt = e >> 2;               // M tile of this warp
-        const int rr = 32 * quarter + lane;  // row within the M tile
-        const int row_in_tile = mt * kMRows + rr;
+        const int rr = 32 * quarter + lane;  // the query row this lane converts
         const uint32_t qrow = q_smem + static_cast<uint32_t>(mt) * kQTileBytes + static_cast<uint32_t>(rr) * 128;
         const uint32_t qswz = static_cast<uint32_t>(rr & 7);
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16) +
@@ -406,11 +441,22 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
             if (lane == 0)
                 mbar_arrive(smem_addr(&ctl->q_conv));
 
-            const int tl = kTileTokens * c.t + (row_in_tile >> 2);  // token within the request's new ones
-            const int head = row_in_tile & 3;
+            // Per page the accumulator is read in the mma-fragment layout: lane
+            // (g, cq) = (lane / 4, lane % 4) holds rows g + 8 m (m = 0..3) of the
+            // warp's 32 at the 32 key columns 8 i + 2 cq + {0, 1}, so it needs only
+            // those columns' scales (a quarter of the shared-memory traffic of a
+            // row-per-lane read).  After the quad's max, lane (g, cq) writes row
+            // g + 8 cq.
+            const int g = lane >> 2, cq = lane & 3;
+            const int my_rr = 32 * quarter + g + 8 * cq;  // the row this lane writes
+            const float my_inv = __shfl_sync(0xffffffffu, inv_row, g + 8 * cq);
+            const int tl = kTileTokens * c.t + ((mt * kMRows + my_rr) >> 2);  // token within the new ones
             const bool live = tl < c.r.n;
             const int pos = c.r.len - c.r.n + tl;
-            float *out = p.scores + (static_cast<int64_t>(c.r.c0 + tl) * kHeads + head) * p.bs_stride;
+            float *out =
+                p.scores + (static_cast<int64_t>(c.r.c0 + tl) * kHeads + (my_rr & 3)) * p.bs_stride;
+            const int pos_lo = c.r.len - c.r.n + kTileTokens * c.t + (mt * kMRows + 32 * quarter) / 4;
+            const int pos_q = pos_lo + (g >> 2);  // rows g + 8 m are the tokens at pos_q + 2 m
             for (int j = c.j; j < je; ++j) {
                 const int a = static_cast<int>(ac % kAccBufs);
                 const int slot = static_cast<int>(ac % kF8Ring);
@@ -430,46 +476,43 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
                 const int first_key = j * kPage;
                 const bool want = live && first_key <= pos;
                 if (page_ok && __any_sync(0xffffffffu, want)) {
-                    const float4 *scl = reinterpret_cast<const float4 *>(ring + slot * kPage);
-                    float mx = neg_inf;
+                    const float2 *sc2 = reinterpret_cast<const float2 *>(ring + slot * kPage);
+                    const uint32_t acc = lane_addr + static_cast<uint32_t>(a * kMTiles * kPage);
+                    // the page fully visible to every row of the warp, or its causal edge
+                    const bool full = pos_lo >= first_key + kPage - 1;
+                    const int l0 = pos_q - first_key;
+                    float m4[4] = {neg_inf, neg_inf, neg_inf, neg_inf};
+                    // 8 loads of 16 rows x 32 columns (column chunk cb, row half h),
+                    // two in flight
+                    uint32_t ra[16], rb[16];
+                    tmem_ld16x256b_x4(acc, ra);
+                    tmem_ld16x256b_x4(acc + (16u << 16), rb);
 #pragma unroll
-                    for (int q4 = 0; q4 < kPage / 32; ++q4) {
-                        uint32_t r[32];
-                        tmem_ld32(lane_addr + static_cast<uint32_t>(a * kMTiles * kPage + 32 * q4), r);
-                        tmem_wait_ld(r);
-                        const int lim = pos - (first_key + 32 * q4);  // keys i <= lim are visible
-                        if (lim >= 31) {
-                            float m4[4] = {neg_inf, neg_inf, neg_inf, neg_inf};
-#pragma unroll
-                            for (int i4 = 0; i4 < 8; ++i4) {
-                                const float4 s4 = scl[8 * q4 + i4];
-                                float v0, v1, v2, v3;
-                                mul2(__uint_as_float(r[4 * i4]), __uint_as_float(r[4 * i4 + 1]), s4.x, s4.y,
-                                     v0, v1);
-                                mul2(__uint_as_float(r[4 * i4 + 2]), __uint_as_float(r[4 * i4 + 3]), s4.z,
-                                     s4.w, v2, v3);
-                                m4[0] = fmaxf(m4[0], v0);
-                                m4[1] = fmaxf(m4[1], v1);
-                                m4[2] = fmaxf(m4[2], v2);
-                                m4[3] = fmaxf(m4[3], v3);
-                            }
-                            mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
-                        } else {
-#pragma unroll
-                            for (int i4 = 0; i4 < 8; ++i4) {
-                                const float4 s4 = scl[8 * q4 + i4];
-                                const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-                                for (int t = 0; t < 4; ++t) {
-                                    const int i = 4 * i4 + t;
-                                    const float v = __uint_as_float(r[i]) * sv[t];
-                                    mx = fmaxf(mx, i <= lim ? v : neg_inf);
-                                }
-                            }
-                        }
+                    for (int cb = 0; cb < kPage / 32; ++cb) {
+                        tmem_wait_ld(ra);
+                        tmem_regs_ready(rb);
+                        const float2 *sc = sc2 + 16 * cb;
+                        if (full)
+                            scaled_max_frag<false>(ra, sc, cq, 32 * cb, 0, 0, m4[0], m4[1]);
+                        else
+                            scaled_max_frag<true>(ra, sc, cq, 32 * cb, l0, l0 + 2, m4[0], m4[1]);
+                        if (cb + 1 < kPage / 32)
+                            tmem_ld16x256b_x4(acc + 32 * (cb + 1), ra);
+                        if (full)
+                            scaled_max_frag<false>(rb, sc, cq, 32 * cb, 0, 0, m4[2], m4[3]);
+                        else
+                            scaled_max_frag<true>(rb, sc, cq, 32 * cb, l0 + 4, l0 + 6, m4[2], m4[3]);
+                        if (cb + 1 < kPage / 32)
+                            tmem_ld16x256b_x4(acc + (16u << 16) + 32 * (cb + 1), rb);
                     }
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        m4[m] = fmaxf(m4[m], __shfl_xor_sync(0xffffffffu, m4[m], 1));
+                        m4[m] = fmaxf(m4[m], __shfl_xor_sync(0xffffffffu, m4[m], 2));
+                    }
+                    const float mx = cq == 0 ? m4[0] : cq == 1 ? m4[1] : cq == 2 ? m4[2] : m4[3];
                     if (want)
-                        out[j] = mx * inv_row;
+                        out[j] = mx * my_inv;
                 } else if (!page_ok && want) {
                     out[j] = neg_inf;
                 }

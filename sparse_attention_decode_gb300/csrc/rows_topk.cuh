@@ -88,8 +88,10 @@ __global__ void __launch_bounds__(32 * rows_per_cta<KMAX>()) rows_topk_kernel(
     constexpr int kCandCap = KMAX * kKeysPerLane;
     __shared__ float cand_s[kRowsPerCta][kCandCap];  // candidate scores
     __shared__ int cand_j[kRowsPerCta][kCandCap];    // and their block ids
+    // No early trigger: this grid runs in many waves, and a dependent persistent
+    // scoring grid launched before its last wave slows that wave (its CTAs are
+    // released at this grid's exit instead).
     griddep_wait();
-    griddep_launch_dependents();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kRowsPerCta + wid;  // (token, head)
     if (row >= static_cast<int64_t>(total_q) * kHeads)

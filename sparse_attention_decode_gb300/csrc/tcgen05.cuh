@@ -46,20 +46,22 @@ __device__ __forceinline__ void tc_fence_after_sync()
 }
 
 // Shared-memory matrix descriptor of a K-major operand in the 128-byte
-// swizzle layout: start address, stride between 8-row atoms (1024 B), the
-// descriptor version bit of sm_100-class parts and the swizzle mode.  The
-// leading-dimension offset is not used by swizzled K-major operands whose K
-// extent per instruction (16 bf16 = 32 B) lies inside one 128-byte row; a
-// K step inside the row advances the start address by 32 B.
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr)
+// swizzle layout, as two 32-bit words.  Low word: start address >> 4 (bits
+// 0-13) and the leading-dimension offset (bits 16-29; 16 B, not used by
+// swizzled K-major operands whose K extent per instruction, 16 elements =
+// 32 B, lies inside one 128-byte row).  High word: the stride between 8-row
+// atoms (1024 B >> 4), the descriptor version bit of sm_100-class parts and
+// the swizzle mode.  Only the start address changes between instructions, so
+// an operand one K step (32 B) or one tile further on is the low word plus
+// that byte offset >> 4: shared addresses stay below 2^18, so the 14-bit field
+// never carries.
+__device__ __forceinline__ uint32_t umma_desc_lo(uint32_t saddr)
 {
-    uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>(1) << 16;            // leading byte offset (16 B, unused)
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;    // stride byte offset: 8 rows x 128 B
-    d |= static_cast<uint64_t>(1) << 46;            // version
-    d |= static_cast<uint64_t>(2) << 61;            // 128-byte swizzle
-    return d;
+    return ((saddr >> 4) & 0x3FFFu) | (1u << 16);
 }
+constexpr uint32_t kUmmaDescHi = (1024u >> 4)    // stride byte offset: 8 rows x 128 B
+                                 | (1u << 14)   // version (bit 46)
+                                 | (2u << 29);  // 128-byte swizzle (bits 61-63)
 
 // Instruction descriptor of kind::f16 with bf16 A and B (both K-major) and an
 // fp32 accumulator, shape M x N (K = 16).
@@ -81,17 +83,20 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16_f32(int m, int n)
            | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate)
+// D[tmem] (+)= A[smem] * B[smem]^T (kind::f16, cta_group::1), issued by one
+// thread; the operands are given by their descriptors' low words
+// (umma_desc_lo), ACC = false overwrites D.
+template <bool ACC>
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc)
 {
     asm volatile(
         "{\n"
-        "  .reg .pred p;\n"
-        "  setp.ne.b32 p, %4, 0;\n"
-        "  tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        "  .reg .b64 ad, bd;\n"
+        "  mov.b64 ad, {%1, %5};\n"
+        "  mov.b64 bd, {%2, %5};\n"
+        "  tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %3, %4;\n"
         "}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "n"(ACC ? 1 : 0), "r"(kUmmaDescHi)
         : "memory");
 }
 
@@ -119,6 +124,41 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
           "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
+}
+
+// 16 lanes x 32 fp32 columns in the mma-fragment layout: with g = lane / 4 and
+// c = lane % 4, repetition i (0..3) gives r[4i], r[4i+1] = row g, columns
+// 8i + 2c, 8i + 2c + 1 and r[4i+2], r[4i+3] = row g + 8, the same columns.
+// taddr's lane field is the first of the 16 rows (inside the warp's quarter).
+__device__ __forceinline__ void tmem_ld16x256b_x4(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// Waits for all of this thread's TMEM loads (r and any other in flight); r
+// passes through the asm so that no use of it is scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
+// Marks r as written here: placed after a tmem_wait_ld that also covered r's
+// load, it keeps r's uses after that wait.
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[16])
+{
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 
 // Waits for this thread's TMEM loads; the registers pass through the asm so

@@ -78,3 +78,12 @@ def test_peak_falls_back_when_no_measurement(monkeypatch, tmp_path):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     v, src = bench.measured_hbm_peak()
     assert v == bench.FALLBACK_HBM_GBS and src.startswith("fallback")
+
+
+def test_fp8_prefill_profile_hash_covers_its_kernel():
+    """The fp8 prefill kernel lives in its own header: a change there must
+    invalidate its profile and not the bf16 prefill one."""
+    assert "prefill_fp8.cuh" in bench.PREFILL_FP8_SOURCES
+    assert "prefill_fp8.cuh" not in bench.PREFILL_SOURCES
+    assert bench.kernel_source_hash("prefill_fp8") != bench.kernel_source_hash("prefill")
+    assert bench.kernel_source_hash("prefill") != bench.kernel_source_hash("decode")
