@@ -15,9 +15,11 @@
 //   warp 0       TMA producer: the tile's 256 bf16 query rows, and each page's
 //                16 KiB of codes (one 128x128-byte box) + 512 B of scales
 //                (one bulk copy) into a 3-stage raw ring;
-//   warp 1       one thread issues tcgen05.mma (f16, M = 128, N = 128, K = 16)
-//                for both M tiles against each converted page;
-//   warps 2-5    converters: one key row per thread, E4M3 -> f16 into a
+//   warp 2       one thread issues tcgen05.mma (f16, M = 128, N = 128, K = 16)
+//                for both M tiles against each converted page (its SM
+//                sub-partition holds no converter warp, which would slow the
+//                issue);
+//   warps 1, 3-5 converters: one key row per thread, E4M3 -> f16 into a
 //                3-stage operand ring (the 128-byte swizzle layout of a bf16
 //                TMA page), scales into an 8-slot ring;
 //   warps 6-13   epilogue: first its query row to f16 in place (per segment),
@@ -270,7 +272,7 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
             if (seg > 0 && !mbar_wait(smem_addr(&ctl->q_full), (seg - 1) & 1u))
                 give_up(p, ctl);
         }
-    } else if (warp == 1) {
+    } else if (warp == 2) {
         // ---------------- MMA issue (one thread) ----------------
         if (lane == 0) {
             Cursor c;
@@ -334,7 +336,7 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
         __syncwarp();
     } else if (warp < kF8FirstEpiWarp) {
         // ---------------- converters: E4M3 page -> f16 operand ----------------
-        const int kr0 = static_cast<int>(threadIdx.x) - 64;  // this thread's key row
+        const int kr0 = 32 * (warp == 1 ? 0 : warp - 2) + lane;  // this thread's key row
         for (long long pc = 0; pc < units; ++pc) {
             const uint32_t u = static_cast<uint32_t>(pc);
             const int rs = static_cast<int>(u % kF8RawStages);
