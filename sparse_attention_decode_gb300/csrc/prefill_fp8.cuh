@@ -22,10 +22,13 @@
 //   warps 1, 3-5 converters: one key row per thread, E4M3 -> f16 into a
 //                3-stage operand ring (the 128-byte swizzle layout of a bf16
 //                TMA page), scales into an 8-slot ring;
-//   warps 6-13   epilogue: first its query row to f16 in place (per segment),
-//                then per page the scaled, masked block max.
-// (14 warps: up to four on one SM sub-partition, whose 16K-register file then
-// allows 128 registers a thread; the launch bound keeps the kernel there.)
+//   warps 6-21   epilogue, four per TMEM lane quarter (2 M tiles x 2 halves of
+//                the quarter's 32 rows): first its 16 query rows to f16 in
+//                place (per segment), then per page their scaled, masked
+//                block max.  Sixteen warps of 16 rows keep the per-page work
+//                of each short enough to follow the tensor pipe.
+// (22 warps: up to six on one SM sub-partition, whose 16K-register file then
+// allows 80 registers a thread; the register cap keeps the kernel there.)
 #pragma once
 
 namespace msa {
@@ -35,7 +38,8 @@ constexpr int kF8OpStages = 3;
 constexpr int kF8Ring = 8;                   // scale slots, one page each
 constexpr int kF8ConvWarps = 4;              // one key row per thread, one warp per SM sub-partition
 constexpr int kF8FirstEpiWarp = 2 + kF8ConvWarps;
-constexpr int kF8Threads = 32 * (kF8FirstEpiWarp + kEpiWarps);
+constexpr int kF8EpiWarps = 16;             // four per TMEM lane quarter: 2 M tiles x 2 row halves
+constexpr int kF8Threads = 32 * (kF8FirstEpiWarp + kF8EpiWarps);
 constexpr uint32_t kF8RawBytes = kPage * kDim;  // 16 KiB of codes
 constexpr uint32_t kF8ScaleBytes = kPage * 4;   // 512 B
 constexpr uint32_t kIdescF16 = umma_idesc_f16_f32(kMRows, kPage);
@@ -134,10 +138,10 @@ __device__ __forceinline__ void scaled_max_frag(const uint32_t (&r)[16], const f
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// 14 warps leave four on one SM sub-partition, whose 16K registers then hold
-// 128 a thread; the cap keeps the launch inside that.
-constexpr int kF8MaxRegs = 16384 / (32 * ((kF8Threads / 32 + 3) / 4));
-static_assert(kF8MaxRegs >= 96, "too many warps for the register file");
+// 22 warps leave six on two SM sub-partitions, whose 16K registers then hold
+// 80 a thread (a multiple of 8); the cap keeps the launch inside that.
+constexpr int kF8MaxRegs = (16384 / (32 * ((kF8Threads / 32 + 3) / 4))) & ~7;
+static_assert(kF8MaxRegs >= 64, "too many warps for the register file");
 
 __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_constant__ TcParams p)
 {
@@ -163,14 +167,14 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
         }
         for (int s = 0; s < kF8Ring; ++s) {
             mbar_init(smem_addr(&ctl->sc_full[s]), kF8ConvWarps);
-            mbar_init(smem_addr(&ctl->sc_empty[s]), kEpiWarps);
+            mbar_init(smem_addr(&ctl->sc_empty[s]), kF8EpiWarps);
         }
         mbar_init(smem_addr(&ctl->q_full), 1);
-        mbar_init(smem_addr(&ctl->q_conv), kEpiWarps);
+        mbar_init(smem_addr(&ctl->q_conv), kF8EpiWarps);
         mbar_init(smem_addr(&ctl->q_empty), 1);
         for (int a = 0; a < kAccBufs; ++a) {
             mbar_init(smem_addr(&ctl->acc_full[a]), 1);
-            mbar_init(smem_addr(&ctl->acc_empty[a]), kEpiWarps);
+            mbar_init(smem_addr(&ctl->acc_empty[a]), kF8EpiWarps);
         }
         mbar_init(smem_addr(&ctl->mma_done), 1);
         ctl->abort = 0;
@@ -386,13 +390,16 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
     } else {
         // ---------------- epilogue: query row to f16, then block scores ----------------
         const int e = warp - kF8FirstEpiWarp;
-        const int quarter = warp & 3;        // TMEM lanes this warp may read
-        const int mt = e >> 2;               // M tile of this warp
-        const int rr = 32 * quarter + lane;  // the query row this lane converts
-        const uint32_t qrow = q_smem + static_cast<uint32_t>(mt) * kQTileBytes + static_cast<uint32_t>(rr) * 128;
+        const int quarter = warp & 3;  // TMEM lanes this warp may read
+        const int mt = e >> 3;         // M tile of this warp
+        const int hh = (e >> 2) & 1;   // its 16 of the quarter's 32 rows
+        const int row0 = 32 * quarter + 16 * hh;  // first of those rows within the M tile
+        // Query conversion: two lanes per row, each half of the row's 128 dims.
+        const int rr = row0 + (lane & 15);
+        const uint32_t qrow = q_smem + static_cast<uint32_t>(mt) * kQTileBytes + static_cast<uint32_t>(rr) * 128 +
+                              static_cast<uint32_t>(lane >> 4) * kHalfPageBytes;
         const uint32_t qswz = static_cast<uint32_t>(rr & 7);
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16) +
-                                   static_cast<uint32_t>(mt * kPage);
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(row0) << 16) + static_cast<uint32_t>(mt * kPage);
         const float neg_inf = -__int_as_float(0x7f800000);
         Cursor c;
         c.load(p, sb, st, sj);
@@ -410,16 +417,16 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
                     give_up(p, ctl);
                 break;
             }
-            float amax = 0.0f;  // pass 1: the row's largest |q|
+            float amax = 0.0f;  // pass 1: the row's largest |q| (this lane's half, then both)
 #pragma unroll 4
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t half = static_cast<uint32_t>(i >> 3) * kHalfPageBytes;
-                const uint4 v = lds128(qrow + half + ((static_cast<uint32_t>(i & 7) ^ qswz) << 4));
+            for (int i = 0; i < 8; ++i) {
+                const uint4 v = lds128(qrow + ((static_cast<uint32_t>(i) ^ qswz) << 4));
                 const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int t = 0; t < 4; ++t)
                     amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[t])), fabsf(bf16_hi(w[t]))));
             }
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
             int ex = 0;
             if (amax > 0.0f)
                 frexpf(amax, &ex);  // amax = m * 2^ex, m in [0.5, 1)
@@ -427,9 +434,8 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
             const float up = __int_as_float((127 + sh) << 23);
             const float inv_row = __int_as_float((127 - sh) << 23);
 #pragma unroll 4
-            for (int i = 0; i < 16; ++i) {  // pass 2: scale, round to f16, write back in place
-                const uint32_t half = static_cast<uint32_t>(i >> 3) * kHalfPageBytes;
-                const uint32_t addr = qrow + half + ((static_cast<uint32_t>(i & 7) ^ qswz) << 4);
+            for (int i = 0; i < 8; ++i) {  // pass 2: scale, round to f16, write back in place
+                const uint32_t addr = qrow + ((static_cast<uint32_t>(i) ^ qswz) << 4);
                 const uint4 v = lds128(addr);
                 uint4 o;
                 o.x = f32x2_to_f16x2(bf16_lo(v.x) * up, bf16_hi(v.x) * up);
@@ -444,22 +450,29 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
                 mbar_arrive(smem_addr(&ctl->q_conv));
 
             // Per page the accumulator is read in the mma-fragment layout: lane
-            // (g, cq) = (lane / 4, lane % 4) holds rows g + 8 m (m = 0..3) of the
-            // warp's 32 at the 32 key columns 8 i + 2 cq + {0, 1}, so it needs only
-            // those columns' scales (a quarter of the shared-memory traffic of a
-            // row-per-lane read).  After the quad's max, lane (g, cq) writes row
-            // g + 8 cq.
+            // (g, cq) = (lane / 4, lane % 4) holds rows g and g + 8 of the warp's
+            // 16 at the 32 key columns 8 i + 2 cq + {0, 1}, so it needs only
+            // those columns' scales.  After the quad's max, lane (g, 0) writes
+            // row g and lane (g, 1) row g + 8.
             const int g = lane >> 2, cq = lane & 3;
-            const int my_rr = 32 * quarter + g + 8 * cq;  // the row this lane writes
-            const float my_inv = __shfl_sync(0xffffffffu, inv_row, g + 8 * cq);
+            const int my_local = g + 8 * (cq & 1);  // the row this lane writes, of the warp's 16
+            const float my_inv = __shfl_sync(0xffffffffu, inv_row, my_local);
+            const int my_rr = row0 + my_local;
             const int tl = kTileTokens * c.t + ((mt * kMRows + my_rr) >> 2);  // token within the new ones
-            const bool live = tl < c.r.n;
+            const bool live = cq < 2 && tl < c.r.n;
             const int pos = c.r.len - c.r.n + tl;
             float *out =
                 p.scores + (static_cast<int64_t>(c.r.c0 + tl) * kHeads + (my_rr & 3)) * p.bs_stride;
-            const int pos_lo = c.r.len - c.r.n + kTileTokens * c.t + (mt * kMRows + 32 * quarter) / 4;
-            const int pos_q = pos_lo + (g >> 2);  // rows g + 8 m are the tokens at pos_q + 2 m
+            const int pos_lo = c.r.len - c.r.n + kTileTokens * c.t + (mt * kMRows + row0) / 4;
+            const int pos_q = pos_lo + (g >> 2);  // rows g and g + 8 are the tokens at pos_q, pos_q + 2
+            // the block-table entry of the next page is fetched while this one is
+            // reduced: a global load on each page's critical path otherwise
+            const int32_t *bt_row = p.block_table + static_cast<int64_t>(c.b) * p.bt_stride;
+            int page_next = c.j < je ? __ldg(bt_row + c.j) : 0;
             for (int j = c.j; j < je; ++j) {
+                const int page = page_next;
+                if (j + 1 < je)
+                    page_next = __ldg(bt_row + j + 1);
                 const int a = static_cast<int>(ac % kAccBufs);
                 const int slot = static_cast<int>(ac % kF8Ring);
                 bool ready = !aborted(ctl) &&
@@ -473,7 +486,6 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
                     break;
                 }
                 tc_fence_after_sync();
-                const int page = p.block_table[static_cast<int64_t>(c.b) * p.bt_stride + j];
                 const bool page_ok = page >= 0 && page < p.num_pages;
                 const int first_key = j * kPage;
                 const bool want = live && first_key <= pos;
@@ -483,36 +495,34 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
                     // the page fully visible to every row of the warp, or its causal edge
                     const bool full = pos_lo >= first_key + kPage - 1;
                     const int l0 = pos_q - first_key;
-                    float m4[4] = {neg_inf, neg_inf, neg_inf, neg_inf};
-                    // 8 loads of 16 rows x 32 columns (column chunk cb, row half h),
-                    // two in flight
+                    float ma = neg_inf, mb = neg_inf;
+                    // 4 loads of 16 rows x 32 columns, two in flight
                     uint32_t ra[16], rb[16];
                     tmem_ld16x256b_x4(acc, ra);
-                    tmem_ld16x256b_x4(acc + (16u << 16), rb);
+                    tmem_ld16x256b_x4(acc + 32, rb);
 #pragma unroll
-                    for (int cb = 0; cb < kPage / 32; ++cb) {
+                    for (int cp = 0; cp < kPage / 64; ++cp) {
                         tmem_wait_ld(ra);
                         tmem_regs_ready(rb);
-                        const float2 *sc = sc2 + 16 * cb;
+                        const int c0 = 64 * cp;
                         if (full)
-                            scaled_max_frag<false>(ra, sc, cq, 32 * cb, 0, 0, m4[0], m4[1]);
+                            scaled_max_frag<false>(ra, sc2 + c0 / 2, cq, c0, 0, 0, ma, mb);
                         else
-                            scaled_max_frag<true>(ra, sc, cq, 32 * cb, l0, l0 + 2, m4[0], m4[1]);
-                        if (cb + 1 < kPage / 32)
-                            tmem_ld16x256b_x4(acc + 32 * (cb + 1), ra);
+                            scaled_max_frag<true>(ra, sc2 + c0 / 2, cq, c0, l0, l0 + 2, ma, mb);
+                        if (cp + 1 < kPage / 64)
+                            tmem_ld16x256b_x4(acc + c0 + 64, ra);
                         if (full)
-                            scaled_max_frag<false>(rb, sc, cq, 32 * cb, 0, 0, m4[2], m4[3]);
+                            scaled_max_frag<false>(rb, sc2 + c0 / 2 + 16, cq, c0 + 32, 0, 0, ma, mb);
                         else
-                            scaled_max_frag<true>(rb, sc, cq, 32 * cb, l0 + 4, l0 + 6, m4[2], m4[3]);
-                        if (cb + 1 < kPage / 32)
-                            tmem_ld16x256b_x4(acc + (16u << 16) + 32 * (cb + 1), rb);
+                            scaled_max_frag<true>(rb, sc2 + c0 / 2 + 16, cq, c0 + 32, l0, l0 + 2, ma, mb);
+                        if (cp + 1 < kPage / 64)
+                            tmem_ld16x256b_x4(acc + c0 + 96, rb);
                     }
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        m4[m] = fmaxf(m4[m], __shfl_xor_sync(0xffffffffu, m4[m], 1));
-                        m4[m] = fmaxf(m4[m], __shfl_xor_sync(0xffffffffu, m4[m], 2));
-                    }
-                    const float mx = cq == 0 ? m4[0] : cq == 1 ? m4[1] : cq == 2 ? m4[2] : m4[3];
+                    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+                    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+                    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+                    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+                    const float mx = (cq & 1) ? mb : ma;
                     if (want)
                         out[j] = mx * my_inv;
                 } else if (!page_ok && want) {
