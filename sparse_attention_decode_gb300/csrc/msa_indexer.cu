@@ -531,10 +531,10 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
 
                 const bool ready = warp_wait(ctl, hdr, smem_addr(&ctl->full[s]), P::use_of(my) & 1u);
                 const int2 meta = ctl->meta[s];
-                float sc[NC];
+                float mk[NF][2];  // the page's column maxima (-inf when skipped)
 #pragma unroll
-                for (int cc = 0; cc < NC; ++cc)
-                    sc[cc] = neg_inf;
+                for (int f = 0; f < NF; ++f)
+                    mk[f][0] = mk[f][1] = neg_inf;
                 const bool ok = ready && meta.y != 0;
                 if (ok) {
                     float m[NF][2];
@@ -555,34 +555,54 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
                         score_page<NQ>(stage0 + s * F::kDataBytes, bq, vrows, lane_off, xo, lane, m);
                     }
 #pragma unroll
-                    for (int cc = 0; cc < NC; ++cc)
-                        sc[cc] = __shfl_sync(0xffffffffu, m[cc >> 3][cc & 1], (cc & 7) >> 1);
+                    for (int f = 0; f < NF; ++f) {
+                        mk[f][0] = m[f][0];
+                        mk[f][1] = m[f][1];
+                    }
                 }
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&ctl->empty[s]));
 
-                if (p.out_block_scores != nullptr && lane < NC) {
-                    float v = sc[0];
+                // Column cc's maximum is held by lanes with t = (cc % 8) / 2, as
+                // mk[cc / 8][cc % 2].  Every column on every lane is needed only
+                // for 32-wide lists or the block-score output.
+                if (KMAX == 32 || p.out_block_scores != nullptr) {
+                    float sc[NC];
 #pragma unroll
-                    for (int cc = 1; cc < NC; ++cc)
-                        v = lane == cc ? sc[cc] : v;
-                    p.out_block_scores[(static_cast<size_t>(b) * NC + lane) * p.bt_stride + j] = v;
+                    for (int cc = 0; cc < NC; ++cc)
+                        sc[cc] = __shfl_sync(0xffffffffu, mk[cc >> 3][cc & 1], (cc & 7) >> 1);
+                    if (p.out_block_scores != nullptr && lane < NC) {
+                        float v = sc[0];
+#pragma unroll
+                        for (int cc = 1; cc < NC; ++cc)
+                            v = lane == cc ? sc[cc] : v;
+                        p.out_block_scores[(static_cast<size_t>(b) * NC + lane) * p.bt_stride + j] = v;
+                    }
+                    if constexpr (KMAX == 32) {
+#pragma unroll
+                        for (int r = 0; r < NR; ++r) {
+                            const int nbp = nb_pos[r >> 2];
+                            const bool pinned = j < p.n_sink || j >= nbp - p.n_window;
+                            const uint64_t key = (ok && j < nbp) ? pack_key(sc[r], j, pinned) : 0ull;
+                            lst[r] = insert_desc<32>(lst[r], key, lane);
+                        }
+                    }
                 }
-
-                uint64_t key[NC];
+                if constexpr (KMAX == 16) {
+                    // list register r: lanes 0-15 hold column 2r, lanes 16-31 column
+                    // 2r + 1.  Lane (lane & 16) | (r & 3) holds both as mk[r / 4][h]
+                    // with h its own half, so one shuffle gives each half its column.
+                    const int h = lane >> 4;
 #pragma unroll
-                for (int cc = 0; cc < NC; ++cc) {
-                    const int nbp = nb_pos[cc >> 2];
-                    const bool pinned = j < p.n_sink || j >= nbp - p.n_window;
-                    key[cc] = (ok && j < nbp) ? pack_key(sc[cc], j, pinned) : 0ull;
-                }
-#pragma unroll
-                for (int r = 0; r < NR; ++r) {
-                    if constexpr (KMAX == 16)
-                        lst[r] = insert_desc<16>(lst[r], lane < 16 ? key[2 * r] : key[2 * r + 1], lane);
-                    else
-                        lst[r] = insert_desc<32>(lst[r], key[r], lane);
+                    for (int r = 0; r < NR; ++r) {
+                        const float v =
+                            __shfl_sync(0xffffffffu, h ? mk[r >> 2][1] : mk[r >> 2][0], (lane & 16) | (r & 3));
+                        const int nbp = nb_pos[r >> 1];  // position of columns 2r, 2r + 1
+                        const bool pinned = j < p.n_sink || j >= nbp - p.n_window;
+                        const uint64_t key = (ok && j < nbp) ? pack_key(v, j, pinned) : 0ull;
+                        lst[r] = insert_desc<16>(lst[r], key, lane);
+                    }
                 }
             }
             it += static_cast<uint32_t>(seg_end - pg);
