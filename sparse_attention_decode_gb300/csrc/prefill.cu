@@ -85,7 +85,8 @@ struct TcSmem {
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
-    int b0, t0, j0;
+    int b0, t0, j0;  // the range's first unit
+    int b1, t1, j1;  // its last unit + 1 page
     long long units;
 };
 
@@ -166,40 +167,89 @@ __device__ __forceinline__ long long warp_incl_scan64(long long v, int lane)
     return v;
 }
 
-// Walks the work tiles of the batch in order, from a given (request, tile).
+// Walks a CTA's range of (tile, page) units one segment (the range's pages
+// of one tile) at a time, last tile first: the range's last tile begins at
+// page 0, so the CTAs that score the tiles of one request step through its
+// pages nearly together (two fronts: those still in their last tile and those
+// back in the tail of the one before), and each page is read from DRAM about
+// twice instead of once per tile.  Pages within a segment go in order.
 struct Cursor {
-    int b, t, j, T;
+    int b, t, j, je;  // segment: pages [j, je) of tile t of request b
     Req r;
+    int fb, ft, fj;   // the range's first unit
 
-    __device__ __forceinline__ void load(const TcParams &p, int b_, int t_, int j_)
+    __device__ __forceinline__ void load(const TcParams &p, int b0, int t0, int j0, int b1, int t1, int j1)
     {
-        b = b_;
-        t = t_;
-        j = j_;
+        fb = b0;
+        ft = t0;
+        fj = j0;
+        b = b1;
+        t = t1;
         r = req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, b);
-        T = tiles_of(r);
+        je = j1;
+        j = (b == fb && t == ft) ? fj : 0;
     }
 
-    // Moves to the next tile; false past the last request.
+    // Moves to the segment before; false past the range's first tile.
     __device__ __forceinline__ bool next(const TcParams &p)
     {
-        j = 0;
-        if (++t < T)
-            return true;
-        t = 0;
-        for (++b; b < p.batch; ++b) {
-            r = req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, b);
-            if (r.ok && r.n > 0) {
-                T = tiles_of(r);
-                return true;
-            }
+        if (b == fb && t == ft)
+            return false;
+        if (t > 0) {
+            --t;
+        } else {
+            do {
+                --b;
+                r = req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, b);
+            } while (b > fb && !(r.ok && r.n > 0));
+            t = tiles_of(r) - 1;
         }
-        return false;
+        je = tile_pages(r, t);
+        j = (b == fb && t == ft) ? fj : 0;
+        return true;
     }
 };
 
+// The (request, tile, page) of unit u of the batch's (tile, page) units in
+// order (0 <= u < the unit count).  Run by one warp; every lane gets it.
+__device__ __forceinline__ void locate_unit(const TcParams &p, long long u, int lane, int &ub, int &ut, int &uj)
+{
+    int fb = 0;
+    long long base = 0, cum = 0;
+    for (int b0 = 0; b0 < p.batch; b0 += 32) {
+        long long v = 0;
+        if (b0 + lane < p.batch)
+            v = req_units(req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, b0 + lane));
+        const long long incl = warp_incl_scan64(v, lane);
+        const long long total = __shfl_sync(0xffffffffu, incl, 31);
+        if (cum + total > u) {
+            const unsigned m = __ballot_sync(0xffffffffu, cum + incl > u);
+            const int l = __ffs(m) - 1;
+            fb = b0 + l;
+            base = cum + __shfl_sync(0xffffffffu, incl - v, l);
+            break;
+        }
+        cum += total;
+    }
+    const Req r = req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, fb);
+    const long long rel = u - base;
+    // the last tile t with pages_before(t) <= rel
+    int lo = 0, hi = tiles_of(r) - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pages_before(r, mid) <= rel)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    ub = fb;
+    ut = lo;
+    uj = static_cast<int>(rel - pages_before(r, lo));
+}
+
 // This CTA's range of work units: [W*g/G, W*(g+1)/G) of the batch's
-// (tile, page) units in order.  Run by one warp; writes the start and count.
+// (tile, page) units in order.  Run by one warp; writes its first and last
+// positions and its unit count.
 template <class Ctl>
 __device__ void plan_range(const TcParams &p, Ctl *ctl, int lane)
 {
@@ -216,46 +266,22 @@ __device__ void plan_range(const TcParams &p, Ctl *ctl, int lane)
     }
     const long long G = gridDim.x, g = blockIdx.x;
     const long long u0 = W * g / G, u1 = W * (g + 1) / G;
-    int fb = -1;
-    long long base = 0;
-    if (u1 > u0) {
-        long long cum = 0;
-        for (int b0 = 0; b0 < p.batch && fb < 0; b0 += 32) {
-            long long v = 0;
-            if (b0 + lane < p.batch)
-                v = req_units(req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, b0 + lane));
-            const long long incl = warp_incl_scan64(v, lane);
-            const long long total = __shfl_sync(0xffffffffu, incl, 31);
-            if (cum + total > u0) {
-                const unsigned m = __ballot_sync(0xffffffffu, cum + incl > u0);
-                const int l = __ffs(m) - 1;
-                fb = b0 + l;
-                base = cum + __shfl_sync(0xffffffffu, incl - v, l);
-            } else {
-                cum += total;
-            }
-        }
-    }
-    if (lane == 0) {
-        if (fb < 0) {
+    if (u1 <= u0) {
+        if (lane == 0)
             ctl->units = 0;
-        } else {
-            const Req r = req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, fb);
-            const long long rel = u0 - base;
-            // the last tile t with pages_before(t) <= rel
-            int lo = 0, hi = tiles_of(r) - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (pages_before(r, mid) <= rel)
-                    lo = mid;
-                else
-                    hi = mid - 1;
-            }
-            ctl->b0 = fb;
-            ctl->t0 = lo;
-            ctl->j0 = static_cast<int>(rel - pages_before(r, lo));
-            ctl->units = u1 - u0;
-        }
+        return;
+    }
+    int b0, t0, j0, b1, t1, j1;
+    locate_unit(p, u0, lane, b0, t0, j0);
+    locate_unit(p, u1 - 1, lane, b1, t1, j1);
+    if (lane == 0) {
+        ctl->b0 = b0;
+        ctl->t0 = t0;
+        ctl->j0 = j0;
+        ctl->b1 = b1;
+        ctl->t1 = t1;
+        ctl->j1 = j1 + 1;
+        ctl->units = u1 - u0;
     }
 }
 
@@ -358,17 +384,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
     tc_fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
     const int sb = ctl->b0, st = ctl->t0, sj = ctl->j0;
+    const int eb = ctl->b1, et = ctl->t1, ej = ctl->j1;
 
     if (warp == 0) {
         // ---------------- producer ----------------
         Cursor c;
-        c.load(p, sb, st, sj);
+        c.load(p, sb, st, sj, eb, et, ej);
         long long left = units;
         uint32_t kc = 0, seg = 0;
         bool ok_run = true;
         while (left > 0 && ok_run) {
-            const int nb = tile_pages(c.r, c.t);
-            const int je = static_cast<int>(min(static_cast<long long>(nb), c.j + left));
+            const int je = c.je;
             if (lane == 0) {
                 if (seg > 0 && !mbar_wait(smem_addr(&ctl->q_empty), (seg - 1) & 1u)) {
                     give_up(p, ctl);
@@ -440,13 +466,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
         // ---------------- MMA issue (one thread) ----------------
         if (lane == 0) {
             Cursor c;
-            c.load(p, sb, st, sj);
+            c.load(p, sb, st, sj, eb, et, ej);
             long long left = units;
             uint32_t kc = 0, ac = 0, seg = 0;
             bool ok_run = true;
             while (left > 0 && ok_run) {
-                const int nb = tile_pages(c.r, c.t);
-                const int je = static_cast<int>(min(static_cast<long long>(nb), c.j + left));
+                const int je = c.je;
                 if (!mbar_wait(smem_addr(&ctl->q_full), seg & 1u)) {
                     give_up(p, ctl);
                     break;
@@ -480,13 +505,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
                                    static_cast<uint32_t>(mt * kPage);
         const float neg_inf = -__int_as_float(0x7f800000);
         Cursor c;
-        c.load(p, sb, st, sj);
+        c.load(p, sb, st, sj, eb, et, ej);
         long long left = units;
         uint32_t ac = 0;
         bool ok_run = true;
         while (left > 0 && ok_run) {
-            const int nb = tile_pages(c.r, c.t);
-            const int je = static_cast<int>(min(static_cast<long long>(nb), c.j + left));
+            const int je = c.je;
             const int tl = kTileTokens * c.t + (row_in_tile >> 2);  // token within the request's new ones
             const int head = row_in_tile & 3;
             const bool live = tl < c.r.n;

@@ -59,7 +59,8 @@ struct F8Smem {
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
-    int b0, t0, j0;
+    int b0, t0, j0;  // the range's first unit
+    int b1, t1, j1;  // its last unit + 1 page
     long long units;
 };
 
@@ -197,17 +198,17 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
     tc_fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
     const int sb = ctl->b0, st = ctl->t0, sj = ctl->j0;
+    const int eb = ctl->b1, et = ctl->t1, ej = ctl->j1;
 
     if (warp == 0) {
         // ---------------- producer: query tiles and raw pages ----------------
         Cursor c;
-        c.load(p, sb, st, sj);
+        c.load(p, sb, st, sj, eb, et, ej);
         long long left = units;
         uint32_t kc = 0, seg = 0;
         bool ok_run = true;
         while (left > 0 && ok_run) {
-            const int nb = tile_pages(c.r, c.t);
-            const int je = static_cast<int>(min(static_cast<long long>(nb), c.j + left));
+            const int je = c.je;
             if (lane == 0) {
                 if (seg > 0 && !mbar_wait(smem_addr(&ctl->q_empty), (seg - 1) & 1u)) {
                     give_up(p, ctl);
@@ -280,13 +281,12 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
         // ---------------- MMA issue (one thread) ----------------
         if (lane == 0) {
             Cursor c;
-            c.load(p, sb, st, sj);
+            c.load(p, sb, st, sj, eb, et, ej);
             long long left = units;
             uint32_t kc = 0, ac = 0, seg = 0;
             bool ok_run = true;
             while (left > 0 && ok_run) {
-                const int nb = tile_pages(c.r, c.t);
-                const int je = static_cast<int>(min(static_cast<long long>(nb), c.j + left));
+                const int je = c.je;
                 if (!mbar_wait(smem_addr(&ctl->q_conv), seg & 1u)) {
                     give_up(p, ctl);
                     break;
@@ -402,13 +402,12 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(row0) << 16) + static_cast<uint32_t>(mt * kPage);
         const float neg_inf = -__int_as_float(0x7f800000);
         Cursor c;
-        c.load(p, sb, st, sj);
+        c.load(p, sb, st, sj, eb, et, ej);
         long long left = units;
         uint32_t ac = 0, seg = 0;
         bool ok_run = true;
         while (left > 0 && ok_run) {
-            const int nb = tile_pages(c.r, c.t);
-            const int je = static_cast<int>(min(static_cast<long long>(nb), c.j + left));
+            const int je = c.je;
             // this row of the segment's query tile to f16, scaled by 2^sh
             bool qready = !aborted(ctl) && mbar_wait(smem_addr(&ctl->q_full), seg & 1u);
             qready = __all_sync(0xffffffffu, qready);

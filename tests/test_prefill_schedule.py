@@ -2,9 +2,12 @@
 
 The tensor-core prefill kernel cuts the batch's (tile of 64 new tokens, page)
 units into one equal range per CTA, using a closed form for the pages that
-tiles [0, t) of a request see, then walks tiles in order from its start.
+tiles [0, t) of a request see, locates the range's first and last units, and
+walks the range's tiles last one first (pages within a tile in order), so
+that the CTAs scoring one request's tiles read its pages nearly together.
 This replays that arithmetic (restated from the kernel) and checks that the
-ranges of any grid cover every unit exactly once.
+ranges of any grid cover every unit exactly once, and that on a long chunked
+prefill the pages in flight form at most two compact fronts per request.
 """
 
 import numpy as np
@@ -42,18 +45,13 @@ def req_units(n, L, ok=True):
     return pages_before(n, L, T - 1) + tile_pages(n, L, T - 1)
 
 
-def plan(reqs, G, g):
-    """(b, t, j, units) for CTA g, as the kernel's planning warp computes them."""
-    units = [req_units(n, L, ok) for n, L, ok in reqs]
-    W = sum(units)
-    u0, u1 = W * g // G, W * (g + 1) // G
-    if u1 <= u0:
-        return None
+def locate(reqs, units, u):
+    """(b, t, j) of unit u of the batch's units in order."""
     cum = 0
     for b, v in enumerate(units):
-        if cum + v > u0:
+        if cum + v > u:
             n, L, _ = reqs[b]
-            rel = u0 - cum
+            rel = u - cum
             lo, hi = 0, tiles_of(n) - 1
             while lo < hi:
                 mid = (lo + hi + 1) >> 1
@@ -61,28 +59,45 @@ def plan(reqs, G, g):
                     lo = mid
                 else:
                     hi = mid - 1
-            return b, lo, rel - pages_before(n, L, lo), u1 - u0
+            return b, lo, rel - pages_before(n, L, lo)
         cum += v
-    raise AssertionError("range start past the last unit")
+    raise AssertionError("unit past the last one")
+
+
+def plan(reqs, G, g):
+    """(first (b, t, j), last (b, t, j + 1), units) for CTA g, as the kernel's
+    planning warp computes them."""
+    units = [req_units(n, L, ok) for n, L, ok in reqs]
+    W = sum(units)
+    u0, u1 = W * g // G, W * (g + 1) // G
+    if u1 <= u0:
+        return None
+    b1, t1, j1 = locate(reqs, units, u1 - 1)
+    return locate(reqs, units, u0), (b1, t1, j1 + 1), u1 - u0
 
 
 def walk(reqs, start):
-    b, t, j, left = start
+    """The kernel cursor's order: segments from the range's last tile back to
+    its first, each segment's pages in order."""
+    (fb, ft, fj), (b, t, je), left = start
+    j = fj if (b, t) == (fb, ft) else 0
     out = []
     while left > 0:
-        n, L, _ = reqs[b]
-        nb = tile_pages(n, L, t)
-        je = min(nb, j + left)
         out.extend((b, t, x) for x in range(j, je))
         left -= je - j
         if left > 0:
-            t, j = t + 1, 0
-            if t >= tiles_of(n):
-                t = 0
-                b += 1
-                while b < len(reqs) and (not reqs[b][2] or reqs[b][0] == 0):
-                    b += 1
-                assert b < len(reqs), "walked past the batch"
+            assert (b, t) != (fb, ft), "walked past the range"
+            if t > 0:
+                t -= 1
+            else:
+                b -= 1
+                while b > fb and (not reqs[b][2] or reqs[b][0] == 0):
+                    b -= 1
+                t = tiles_of(reqs[b][0]) - 1
+            n, L, _ = reqs[b]
+            je = tile_pages(n, L, t)
+            j = fj if (b, t) == (fb, ft) else 0
+    assert left == 0 and (b, t) == (fb, ft)
     return out
 
 
@@ -129,7 +144,7 @@ def test_ranges_cover_every_unit_once(seed):
                 start = plan(reqs, G, g)
                 if start is not None:
                     got.extend(walk(reqs, start))
-            assert got == expect, (reqs, G)
+            assert sorted(got) == expect, (reqs, G)
 
 
 def test_named_prefill_shapes():
@@ -140,4 +155,59 @@ def test_named_prefill_shapes():
             s = plan(reqs, 148, g)
             if s is not None:
                 got.extend(walk(reqs, s))
-        assert got == all_units(reqs)
+        assert sorted(got) == all_units(reqs)
+
+
+def test_long_prefill_reads_pages_on_two_fronts():
+    """4 requests x 2048 new tokens at 128K on 152 CTAs, each CTA taking one
+    unit per step: at every step at least 90 % of the pages of one request
+    being read lie in two windows of 32 pages (a page leaves DRAM about twice,
+    not once per tile as with a first-tile-first walk; the few CTAs whose
+    range straddles two requests read a third, small window)."""
+    reqs = [(2048, 131072, True)] * 4
+    G = 152
+    walks = [walk(reqs, plan(reqs, G, g)) for g in range(G)]
+    assert sorted(u for w in walks for u in w) == all_units(reqs)
+
+    def windows(pages):
+        """sizes of the groups of pages no more than 32 apart, largest first"""
+        pages = sorted(pages)
+        sizes = [1]
+        for a, b in zip(pages, pages[1:]):
+            if b - a > 32:
+                sizes.append(1)
+            else:
+                sizes[-1] += 1
+        return sorted(sizes, reverse=True)
+
+    def fronts(pages):
+        return len(windows(pages))
+
+    worst = 1.0
+    for step in range(max(len(w) for w in walks)):
+        by_req = {}
+        for w in walks:
+            if step < len(w):
+                b, _, page = w[step]
+                by_req.setdefault(b, []).append(page)
+        for v in by_req.values():
+            if len(v) >= 8:
+                worst = min(worst, sum(windows(v)[:2]) / len(v))
+    assert worst >= 0.9, worst
+
+    # first tile first, the same ranges: pages scattered over the whole context
+    fwd = []
+    for g in range(G):
+        (b, t, j), _, left = plan(reqs, G, g)
+        seq = []
+        while left > 0:
+            n, L, _ = reqs[b]
+            je = min(tile_pages(n, L, t), j + left)
+            seq.extend((b, x) for x in range(j, je))
+            left -= je - j
+            t, j = t + 1, 0
+            if t >= tiles_of(n):
+                b, t = b + 1, 0
+        fwd.append(seq)
+    spread = max(fronts([w[0][1] for w in fwd if w[0][0] == b]) for b in range(4))
+    assert spread > 8
