@@ -70,15 +70,17 @@ __device__ __forceinline__ uint64_t merge32(uint64_t run, uint64_t key, int lane
 }
 
 // One warp per (token, head) row of the prefill: pins and top-k of its
-// blocks, 512 blocks (16 per lane) at a time.  Filtering runs on 32-bit
-// coarse keys: the KMAX-th largest of the 32 lane maxima is a lower bound on
-// the coarse key of the group's KMAX-th largest key (KMAX lanes hold one at
-// least that large), and so is the running list's last key; only blocks at
-// or above the larger bound can enter the list.  Their packed keys are
-// compacted into shared memory (without ties at most KMAX lanes x 16 keys;
-// a group whose ties overflow that is merged whole instead), sorted 32 at a
-// time and merged into the running list, which ends as the descending
-// top-KMAX of all keys.
+// blocks.  The pins enter the running list first; then the blocks go 512 (16
+// per lane) at a time through a filter on 32-bit coarse keys (the order bits
+// of the score): the KMAX-th largest of the 32 lane maxima is a lower bound
+// on the coarse key of the group's KMAX-th largest block (KMAX lanes hold one
+// at least that large, and a pin ranks above its coarse key), and so is the
+// running list's last key; only blocks at or above the larger bound can enter
+// the list.  They are compacted into shared memory (without ties at most KMAX
+// lanes x 16; a group whose ties overflow that is merged whole instead),
+// pins and out-of-range blocks dropped, and inserted one at a time when there
+// are few, else sorted 32 at a time and merged.  The list ends as the
+// descending top-KMAX of all keys.
 template <int KMAX>
 __global__ void __launch_bounds__(32 * rows_per_cta<KMAX>()) rows_topk_kernel(
     const float *scores, int64_t bs_stride, const int32_t *cu_q, const int32_t *seq_lens, int batch,
@@ -114,7 +116,19 @@ __global__ void __launch_bounds__(32 * rows_per_cta<KMAX>()) rows_topk_kernel(
     const float neg_inf = -__int_as_float(0x7f800000);
     float *buf_s = cand_s[wid];
     int *buf_j = cand_j[wid];
-    uint64_t run = 0;
+    // The pins (the first n_sink and the last n_window visible blocks, ids
+    // ascending) go into the list first: their ids are known, and a block
+    // whose page was out of range (-inf) is left out.
+    const int ns = min(n_sink, nb);
+    const int w0 = max(ns, nb - n_window);  // first window block that is not a sink
+    const int npin = ns + (nb - w0);        // <= n_sink + n_window <= k <= KMAX
+    uint64_t pk = 0;
+    if (lane < npin) {
+        const int id = lane < ns ? lane : w0 + (lane - ns);
+        const float sv = srow[id];
+        pk = sv == neg_inf ? 0ull : pack_key(sv, id, true);
+    }
+    uint64_t run = npin > 0 ? merge32<KMAX>(0ull, pk, lane) : 0ull;
     for (int g0 = 0; g0 < nb; g0 += 32 * kKeysPerLane) {
         float v[kKeysPerLane];
 #pragma unroll
@@ -122,24 +136,23 @@ __global__ void __launch_bounds__(32 * rows_per_cta<KMAX>()) rows_topk_kernel(
             const int j = g0 + 32 * i + lane;
             v[i] = j < nb ? srow[j] : neg_inf;
         }
+        // coarse keys of every block as a free one (-0 as +0, as pack_key);
+        // pins and -inf are sorted out among the few candidates
         uint32_t ck[kKeysPerLane];
         uint32_t cmx = 0;
 #pragma unroll
         for (int i = 0; i < kKeysPerLane; ++i) {
-            const int j = g0 + 32 * i + lane;
-            // -inf marks a block whose page was out of range (and pads the tail)
-            const float sv = v[i] + 0.0f;  // -0 -> +0, as pack_key
-            ck[i] = (v[i] == neg_inf) ? 0u
-                    : (j < n_sink || j >= nb - n_window) ? 0xFFFFFFFFu
-                    : float_order_bits(sv);
+            ck[i] = float_order_bits(v[i] + 0.0f);
             cmx = max(cmx, ck[i]);
         }
-        const uint32_t bound = max(__shfl_sync(0xffffffffu, sort32_desc_u32(cmx, lane), KMAX - 1),
-                                   coarse_of(__shfl_sync(0xffffffffu, run, KMAX - 1)));
+        // above -inf's coarse key, so padding and out-of-range blocks never qualify
+        const uint32_t bound = max(max(__shfl_sync(0xffffffffu, sort32_desc_u32(cmx, lane), KMAX - 1),
+                                       coarse_of(__shfl_sync(0xffffffffu, run, KMAX - 1))),
+                                   float_order_bits(neg_inf) + 1u);
         int cnt = 0;
 #pragma unroll
         for (int i = 0; i < kKeysPerLane; ++i)
-            cnt += (ck[i] != 0 && ck[i] >= bound) ? 1 : 0;
+            cnt += ck[i] >= bound ? 1 : 0;
         int off = cnt;  // inclusive prefix over the lanes
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -152,29 +165,39 @@ __global__ void __launch_bounds__(32 * rows_per_cta<KMAX>()) rows_topk_kernel(
         if (total <= kCandCap) {
 #pragma unroll
             for (int i = 0; i < kKeysPerLane; ++i) {
-                if (ck[i] != 0 && ck[i] >= bound) {
+                if (ck[i] >= bound) {
                     buf_s[off] = v[i];
                     buf_j[off] = g0 + 32 * i + lane;
                     ++off;
                 }
             }
             __syncwarp();
-            for (int c0 = 0; c0 < total; c0 += 32) {
-                uint64_t key = 0;
-                if (c0 + lane < total) {
-                    const int j = buf_j[c0 + lane];
-                    key = pack_key(buf_s[c0 + lane], j, j < n_sink || j >= nb - n_window);
+            if (total <= 8) {
+                // a few candidates: insert them one at a time
+                for (int c = 0; c < total; ++c) {
+                    const int j = buf_j[c];
+                    const uint64_t key = (j < ns || j >= w0) ? 0ull : pack_key(buf_s[c], j, false);
+                    run = insert_desc<KMAX>(run, key, lane);
                 }
-                run = merge32<KMAX>(run, key, lane);
+            } else {
+                for (int c0 = 0; c0 < total; c0 += 32) {
+                    uint64_t key = 0;
+                    if (c0 + lane < total) {
+                        const int j = buf_j[c0 + lane];
+                        if (j >= ns && j < w0)
+                            key = pack_key(buf_s[c0 + lane], j, false);
+                    }
+                    run = merge32<KMAX>(run, key, lane);
+                }
             }
             __syncwarp();
         } else {
-            // many ties at the bound: merge every key of the group
+            // many ties at the bound: merge every free block of the group
 #pragma unroll
             for (int i = 0; i < kKeysPerLane; ++i) {
                 const int j = g0 + 32 * i + lane;
-                run = merge32<KMAX>(run, ck[i] != 0 ? pack_key(v[i], j, j < n_sink || j >= nb - n_window) : 0,
-                                    lane);
+                const bool free_ok = j < nb && j >= ns && j < w0 && v[i] != neg_inf;
+                run = merge32<KMAX>(run, free_ok ? pack_key(v[i], j, false) : 0ull, lane);
             }
         }
     }
