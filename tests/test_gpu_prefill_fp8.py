@@ -179,3 +179,28 @@ def test_prefill_score_fp8_entry_matches(msa):
                                       max_model_len=w8.max_model_len)
     assert msa.msa_indexer_get_error(ws) == 0
     np.testing.assert_array_equal(out.cpu().numpy(), got[2])
+
+
+def test_prefill_fp8_bench_workload_sampled_rows(msa, orc):
+    """The benchmarked prefill on the E4M3 cache (4 x 2048 new tokens at 128K,
+    the launch `bench.py --path prefill --cache fp8` times) on the GPU; sampled
+    rows checked one by one against the oracle."""
+    import bench
+    w, q, cu = bench.prefill_workload()
+    w8 = wl.to_fp8(w)
+    got = run_prefill_fp8(msa, w8, q, cu)
+    assert got[3] == 0
+    total = q.shape[0]
+    rng = np.random.default_rng(401)
+    firsts, lasts = cu[:-1], cu[1:] - 1
+    rows = np.unique(np.concatenate([firsts, lasts, rng.choice(total, 16, replace=False)]))
+    req = np.searchsorted(cu, rows, side="right") - 1
+    lens = (w8.seq_lens[req] - np.diff(cu)[req] + (rows - cu[req]) + 1).astype(np.int32)
+    bt_rows = w8.block_table[req]
+    s = orc.block_scores_fp8(q[rows], w8.pool8, w8.kscale, bt_rows, lens)
+    o_ids, _ = orc.select(s, lens, w8.k, w8.n_sink, w8.n_window)
+    sub = wl.Workload(name="bench_prefill_fp8_rows", q=q[rows], pool=None, block_table=bt_rows,
+                      seq_lens=lens, k=w8.k, n_sink=w8.n_sink, n_window=w8.n_window,
+                      max_model_len=w8.max_model_len)
+    st = sub.bt_stride
+    parity.check(sub, s[:, :, :st], o_ids, got[0][rows], got[1][rows], got[2][rows][:, :, :st])
