@@ -25,8 +25,8 @@
 //   warps 6-21   epilogue, four per TMEM lane quarter (2 M tiles x 2 halves of
 //                the quarter's 32 rows): first its 16 query rows to f16 in
 //                place (per segment), then per page their scaled, masked
-//                block max.  Sixteen warps of 16 rows keep the per-page work
-//                of each short enough to follow the tensor pipe.
+//                block max (sixteen warps of 16 rows: half the per-page
+//                work of each, against eight of 32).
 // (22 warps: up to six on one SM sub-partition, whose 16K-register file then
 // allows 80 registers a thread; the register cap keeps the kernel there.)
 #pragma once
@@ -39,6 +39,8 @@ constexpr int kF8Ring = 8;                   // scale slots, one page each
 constexpr int kF8ConvWarps = 4;              // one key row per thread, one warp per SM sub-partition
 constexpr int kF8FirstEpiWarp = 2 + kF8ConvWarps;
 constexpr int kF8EpiWarps = 16;             // four per TMEM lane quarter: 2 M tiles x 2 row halves
+static_assert(kF8EpiWarps == 4 * 2 * kMTiles && kMTiles == 2,
+              "the epilogue maps warp e to M tile e / 8 and row half (e / 4) % 2");
 constexpr int kF8Threads = 32 * (kF8FirstEpiWarp + kF8EpiWarps);
 constexpr uint32_t kF8RawBytes = kPage * kDim;  // 16 KiB of codes
 constexpr uint32_t kF8ScaleBytes = kPage * 4;   // 512 B
