@@ -72,11 +72,11 @@ __device__ __forceinline__ uint64_t merge32(uint64_t run, uint64_t key, int lane
 // One warp per (token, head) row of the prefill: pins and top-k of its
 // blocks.  The pins enter the running list first; then the blocks go 512 (16
 // per lane) at a time through a filter on 32-bit coarse keys (the order bits
-// of the score): the KMAX-th largest of the 32 lane maxima is a lower bound
-// on the coarse key of the group's KMAX-th largest block (KMAX lanes hold one
-// at least that large, and a pin ranks above its coarse key), and so is the
-// running list's last key; only blocks at or above the larger bound can enter
-// the list.  They are compacted into shared memory (without ties at most KMAX
+// of the score): until the running list is full, the KMAX-th largest of the
+// 32 lane maxima is a lower bound on the coarse key of the group's KMAX-th
+// largest block (KMAX lanes hold one at least that large, and a pin ranks
+// above its coarse key); once it is full, its last key is the bound.  Only
+// blocks at or above the bound can enter the list.  They are compacted into shared memory (without ties at most KMAX
 // lanes x 16; a group whose ties overflow that is merged whole instead),
 // pins and out-of-range blocks dropped, and inserted one at a time when there
 // are few, else sorted 32 at a time and merged.  The list ends as the
@@ -128,7 +128,11 @@ __global__ void __launch_bounds__(32 * rows_per_cta<KMAX>()) rows_topk_kernel(
         const float sv = srow[id];
         pk = sv == neg_inf ? 0ull : pack_key(sv, id, true);
     }
-    uint64_t run = npin > 0 ? merge32<KMAX>(0ull, pk, lane) : 0ull;
+    // lanes hold the pins in id order, which is their key order: already the
+    // sorted list unless a pin was dropped (-inf), which a merge compacts
+    const unsigned pin_lanes = __ballot_sync(0xffffffffu, pk != 0ull);
+    const unsigned all_pins = npin >= 32 ? 0xffffffffu : ((1u << npin) - 1u);
+    uint64_t run = pin_lanes == all_pins ? pk : merge32<KMAX>(0ull, pk, lane);
     for (int g0 = 0; g0 < nb; g0 += 32 * kKeysPerLane) {
         float v[kKeysPerLane];
 #pragma unroll
@@ -145,10 +149,13 @@ __global__ void __launch_bounds__(32 * rows_per_cta<KMAX>()) rows_topk_kernel(
             ck[i] = float_order_bits(v[i] + 0.0f);
             cmx = max(cmx, ck[i]);
         }
-        // above -inf's coarse key, so padding and out-of-range blocks never qualify
-        const uint32_t bound = max(max(__shfl_sync(0xffffffffu, sort32_desc_u32(cmx, lane), KMAX - 1),
-                                       coarse_of(__shfl_sync(0xffffffffu, run, KMAX - 1))),
-                                   float_order_bits(neg_inf) + 1u);
+        // Once the list is full its last key is the bound (nothing below it can
+        // enter); before that, the KMAX-th largest lane maximum.  Always above
+        // -inf's coarse key, so padding and out-of-range blocks never qualify.
+        const uint64_t tail = __shfl_sync(0xffffffffu, run, KMAX - 1);
+        const uint32_t lane_bound =
+            tail != 0ull ? 0u : __shfl_sync(0xffffffffu, sort32_desc_u32(cmx, lane), KMAX - 1);
+        const uint32_t bound = max(max(lane_bound, coarse_of(tail)), float_order_bits(neg_inf) + 1u);
         int cnt = 0;
 #pragma unroll
         for (int i = 0; i < kKeysPerLane; ++i)
