@@ -72,3 +72,14 @@ def test_fp8_matches_bf16_when_codes_are_exact(lib):
     b = parity.run_gpu(w8)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_fp8_max_batch(lib, orc):
+    """MSA_MAX_BATCH requests on the E4M3 cache, short ragged lengths with
+    empty requests."""
+    rng = np.random.default_rng(4097)
+    seq = rng.integers(0, 400, 4096)
+    seq[rng.random(4096) < 0.05] = 0
+    w = wl.random_workload(seq, seed=4097, q_scale=1 / np.sqrt(128), max_model_len=512,
+                           name="max_batch_fp8")
+    _compare(orc, wl.to_fp8(w))

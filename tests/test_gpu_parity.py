@@ -186,3 +186,15 @@ def test_decode_pages_fused_matches_separate(lib, orc, page_tokens):
         e_pages, e_num = orc.expand_pages(outs[1][0], w.seq_lens, kvb.cpu().numpy(), page_tokens)
         np.testing.assert_array_equal(outs[1][2], e_pages)
         np.testing.assert_array_equal(outs[1][3], e_num)
+
+
+def test_max_batch(lib, orc):
+    """The largest batch the library accepts (MSA_MAX_BATCH = 4096 requests),
+    short ragged lengths with empty requests: the per-request prefix in shared
+    memory, chunks spanning many requests and the merge grid at their limits."""
+    rng = np.random.default_rng(4096)
+    seq = rng.integers(0, 400, 4096)
+    seq[rng.random(4096) < 0.05] = 0
+    w = wl.random_workload(seq, seed=4096, q_scale=1 / np.sqrt(128), max_model_len=512,
+                           name="max_batch")
+    _compare(orc, w)
