@@ -290,3 +290,21 @@ def test_prefill_bench_workload_sampled_rows(msa, orc):
                       max_model_len=w.max_model_len)
     st = sub.bt_stride
     parity.check(sub, s[:, :, :st], o_ids, got[0][rows], got[1][rows], got[2][rows][:, :, :st])
+
+
+def _many_pairs(seed, count=200, max_new=24, max_len=2000):
+    rng = np.random.default_rng(seed)
+    pairs = []
+    for _ in range(count):
+        n = int(rng.integers(0, max_new + 1))
+        pairs.append((n, int(rng.integers(max(n, 1), max_len + 1))))
+    return pairs
+
+
+def test_prefill_many_requests(msa, orc):
+    """200 short ragged requests (some with no new tokens): most CTA ranges
+    cross request boundaries, walked last tile first."""
+    w, q, cu = prefill_case(_many_pairs(500), seed=501, max_model_len=2048)
+    got = run_prefill(msa, w, q, cu)
+    assert got[3] == 0
+    check_prefill(orc, w, q, cu, got)

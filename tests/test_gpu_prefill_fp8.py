@@ -204,3 +204,13 @@ def test_prefill_fp8_bench_workload_sampled_rows(msa, orc):
                       max_model_len=w8.max_model_len)
     st = sub.bt_stride
     parity.check(sub, s[:, :, :st], o_ids, got[0][rows], got[1][rows], got[2][rows][:, :, :st])
+
+
+def test_prefill_fp8_many_requests(msa, orc):
+    """200 short ragged requests on the E4M3 cache."""
+    from test_gpu_prefill import _many_pairs
+    w, q, cu = prefill_case(_many_pairs(502), seed=503, max_model_len=2048)
+    w8 = wl.to_fp8(w)
+    got = run_prefill_fp8(msa, w8, q, cu)
+    assert got[3] == 0
+    check_fp8(orc, w8, q, cu, got)
