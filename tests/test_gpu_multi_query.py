@@ -221,3 +221,23 @@ def test_multi_query_fp8_bad_page_is_reported(msa):
                                   max_model_len=w8.max_model_len)
     assert msa.msa_indexer_get_error(ws) & msa.MSA_FAULT_PAGE_ID
     assert not (ids[1].cpu().numpy() == 4).any()
+
+
+def _max_batch_lens(seed):
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(0, 400, 4096)
+    lens[rng.random(4096) < 0.05] = 0
+    return lens
+
+
+def test_multi_query_max_batch(msa, orc):
+    """q_len 4 at the largest accepted batch (4096 short ragged requests)."""
+    w, q = multi_workload(_max_batch_lens(4098), 4, seed=4098, max_model_len=512)
+    check_rows(orc, w, q, 4, run_mq(msa, w, q, 4))
+
+
+def test_multi_query_fp8_max_batch(msa, orc):
+    """q_len 4 on the E4M3 cache at the largest accepted batch."""
+    w, q = multi_workload(_max_batch_lens(4099), 4, seed=4099, max_model_len=512)
+    w8 = wl.to_fp8(w)
+    check_rows_fp8(orc, w8, q, 4, run_mq_fp8(msa, w8, q, 4))
