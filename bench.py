@@ -418,7 +418,7 @@ def run_ours(args):
     clocks = sampler.stop()
     score_ms = s0.elapsed_time(s1) / args.steps
     ms = max_over_ranks(dist, local_ms, device)
-    gpu_launches = 2 * args.steps
+    gpu_launches = 2 * args.steps  # score + merge per decode call
     assert msa.msa_indexer_get_error(ws, stream=stream) == 0
 
     # eager calls through the binding, for comparison (not the headline)
@@ -732,6 +732,19 @@ def graph_median_us(fn, stream, device, calls=20, replays=50, rounds=7):
     return statistics.median(per), e0.elapsed_time(e1) * 1e3 / calls
 
 
+def parity_verdict(w, o_scores, o_ids, ids, sc):
+    """The tests' comparison (tests/parity.py) of one call's selection with the
+    oracle's: rows compared, pass or the first disagreement, band exchanges."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import parity
+    rows = w.batch * 4
+    try:
+        swaps = parity.check(w, o_scores, o_ids, ids.cpu().numpy(), sc.cpu().numpy())
+    except AssertionError as e:
+        return {"rows": rows, "pass": False, "first_failure": str(e)[:200]}
+    return {"rows": rows, "pass": True, "band_exchanges": swaps}
+
+
 def run_configs(args):
     """Every named workload: CUDA-graph median us/call, eager us/call, index-K GB/s,
     and the oracle on all host cores and on one (one JSON line per config and variant)."""
@@ -763,12 +776,12 @@ def run_configs(args):
         variants = [("auto", 0, [pool])]
         if name == "adversarial":
             variants.append(("W=64", 64, [pool]))
-        if name == "decode_point":
+        if name in ("decode_point", "ragged"):
             copies = math.ceil(2 * L2_BYTES / w.index_k_bytes) + 1
             variants.append((f"L2-cold ({copies} pool copies, rotated)", 0,
                              [pool] + [pool.clone() for _ in range(copies - 1)]))
         t0 = time.perf_counter()
-        orc.run(w)
+        o_scores, o_ids, _ = orc.run(w)
         oracle_all = time.perf_counter() - t0
         orc.set_num_threads(1)
         t0 = time.perf_counter()
@@ -785,6 +798,8 @@ def run_configs(args):
 
             us, eager = graph_median_us(call, stream, device)
             assert msa.msa_indexer_get_error(ws, stream=stream) == 0
+            # the selection of this variant's last call against the oracle output above
+            verdict = parity_verdict(w, o_scores, o_ids, ids, sc)
             gbs = w.index_k_bytes / (us * 1e-6) / 1e9
             lines.append({
                 "config": name, "variant": label, "batch": B,
@@ -794,6 +809,8 @@ def run_configs(args):
                 "timing": "graph of 20 calls, 50 replays x 7 rounds, median; eager: 20 calls",
                 "oracle_s": {"all_cores": round(oracle_all, 4), "cores": cores,
                              "one_core": round(oracle_one, 4)},
+                "gpu_launches_per_call": 2,
+                "parity": verdict,
             })
             del ws
         del q, pool, bt, seq, variants

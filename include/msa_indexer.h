@@ -45,7 +45,11 @@
  * request empty (ids -1 / scores -inf); a block-table entry outside
  * [0, num_pages) makes that block score -inf and excludes it from the
  * selection.  Both set a bit in the workspace fault word, read (and cleared)
- * by msa_indexer_get_error().  No kernel traps or waits without bound.
+ * by msa_indexer_get_error().  No kernel traps or waits without bound: every
+ * wait inside a kernel gives up after a fixed number of polls and sets
+ * MSA_FAULT_TIMEOUT; the merge of a pass in which that happened writes -1 /
+ * -inf to every output row, and the workspace stays usable for the next
+ * call.
  *
  * Concurrency.  The library keeps no state between calls except in the
  * caller's workspace.  Calls that may overlap on the GPU need separate
@@ -79,7 +83,7 @@ typedef enum msa_status {
 /* Bits of the workspace fault word (see msa_indexer_get_error). */
 #define MSA_FAULT_SEQ_LEN 0x1u /* a seq_len outside [0, min(max_model_len, 128*bt_stride)] */
 #define MSA_FAULT_PAGE_ID 0x2u /* a block-table entry outside [0, num_pages) */
-#define MSA_FAULT_TIMEOUT 0x4u /* a bounded wait inside a kernel ran out (work was skipped) */
+#define MSA_FAULT_TIMEOUT 0x4u /* a bounded wait inside a kernel ran out (the call's rows are -1 / -inf) */
 #define MSA_FAULT_SLOTS 0x8u   /* the workspace held fewer candidate slots than needed */
 
 /*
@@ -91,6 +95,13 @@ typedef enum msa_status {
  * The workspace must be zero-filled once before its first use (for example
  * cudaMemset or torch.zeros); afterwards the library keeps it consistent.
  * It is 256-byte aligned storage owned by the caller.
+ *
+ * No passage of the pages defines this call; it is this library's own.  It
+ * follows from two things the pages do fix: buffers are persistent and
+ * allocated once (vLLM PR #57832, "CUDA graph capture": the indexer keeps
+ * persistent buffers; TensorRT-LLM PR #17008, "Changes": graph-safe plan
+ * buffers sized for the maximum work), and shapes come from bounds such as
+ * max_model_len, never from the live lengths (vLLM PR #57832, same section).
  */
 size_t msa_indexer_workspace_bytes(int max_batch, int max_model_len, int k, int split_blocks);
 
@@ -366,8 +377,30 @@ msa_status msa_indexer_prefill(const void *q, const int32_t *cu_seqlens_q, int t
  * Reads the workspace fault word (MSA_FAULT_* bits) into *flags and clears
  * it.  Synchronises `stream`.  Returns MSA_ERR_INVALID_ARG for null
  * pointers, MSA_ERR_CUDA if a CUDA call fails.
+ *
+ * No passage of the pages defines this call; it is this library's own way
+ * of reporting bad device data without a host read inside the decode call.
+ * The pages treat unsupported configurations as start-up errors (vLLM PR
+ * #57832, "Solution": enabling the path with a non-bf16 index cache fails at
+ * start-up) and a short plan mirror after capture as a hard error
+ * (TensorRT-LLM PR #17008, "Changes"); device
+ * data cannot be checked on the host without a synchronisation, so it is
+ * flagged here instead.
  */
 msa_status msa_indexer_get_error(void *workspace, void *stream, uint32_t *flags);
+
+/*
+ * Test hook for the bounded waits.  No passage of the pages corresponds; it
+ * exists so that a test can make the decode kernel's waits run out without
+ * any fault: while `on` is non-zero, decode and score passes enqueued
+ * afterwards load no index-K page and never signal one, so every consumer's
+ * first page wait runs out after a short poll limit (about 2^14 polls)
+ * instead of the normal one; no asynchronous copy is in flight at any time.
+ * The pass then sets MSA_FAULT_TIMEOUT and its merge writes -1 / -inf to
+ * every output row.  Set it back to 0 for normal operation.  Not thread-safe with
+ * concurrent decode calls in other threads (the flag is process-wide).
+ */
+void msa_indexer_test_withhold_pages(int on);
 
 /*
  * msa_indexer_decode without a caller-supplied workspace.  The pages describe
@@ -378,23 +411,28 @@ msa_status msa_indexer_get_error(void *workspace, void *stream, uint32_t *flags)
  *
  * The scratch lives in one fixed array of MSA_NOALLOC_WORKSPACE_BYTES in the
  * library's device memory (every GPU that loads the library keeps it until
- * the process exits).  The call allocates and frees nothing.  Its first call
- * on a device does a one-time set-up with that device current: it looks up
- * the array's device address and zero-fills the array's 256-byte header
- * (a blocking cudaMemset); make that first call before any stream capture.
+ * the process exits).  The call allocates and frees nothing.  Each call looks
+ * up the array's device address in the current context (a host-side query
+ * that enqueues nothing), so a caller's own context, or a new one after
+ * cudaDeviceReset, gets its own copy.  Loading the library's module into a
+ * context can happen on the first call in it; make that first call before
+ * any stream capture.
  *
  * Arguments are those of msa_indexer_decode with max_batch = batch and the
- * automatic split.  A batch whose scratch would not fit
- * (256 + round_up(4*(batch+1), 256) + (7*CTAs + batch) * 4 * kmax * 8 bytes,
- * CTAs <= the SM count, kmax = 16 for k <= 16 else 32) returns
- * MSA_ERR_UNSUPPORTED before anything is enqueued; on GB300 (152 SMs) every
- * batch up to 1024 fits for any k.  Every call uses the same array and leaves
- * its contents behind; the only words that must start at zero (two ticket
- * counters in the header) are zeroed at set-up and returned to zero by every
- * call, and everything else a call reads it wrote earlier on the GPU.  Calls
- * that can overlap on the GPU (different streams, different threads) race on
- * the array: serialise them.  Data faults are handled as in
- * msa_indexer_decode but are not reported.
+ * automatic split.  A batch whose scratch would not fit returns
+ * MSA_ERR_UNSUPPORTED before anything is enqueued; the scratch a batch needs
+ * is what msa_indexer_decode checks a caller's workspace against, with the
+ * grid of this GPU (at most its SM count of score CTAs) in place of
+ * MSA_MAX_GRID:
+ *   256 + round_up(4*(batch+1), 256) + (7*CTAs + batch) * 4 * kmax * 8 bytes,
+ * kmax = 16 for k <= 16 else 32.  On GB300 (152 SMs) every batch up to 1024
+ * fits for any k.  Every call uses the same array and leaves its contents
+ * behind.  The words that must start at zero (two ticket counters in the
+ * header) are zero when the module is loaded into a context and every call
+ * returns them to zero; everything else a call reads it wrote earlier on the
+ * GPU.  Calls that can overlap on the GPU (different streams,
+ * different threads) race on the array: serialise them.  Data faults are
+ * handled as in msa_indexer_decode but are not reported.
  */
 #define MSA_NOALLOC_WORKSPACE_BYTES (4u * 1024u * 1024u)
 msa_status msa_indexer_decode_noalloc(const void *q, const void *kcache_pool, int64_t num_pages,
@@ -403,7 +441,10 @@ msa_status msa_indexer_decode_noalloc(const void *q, const void *kcache_pool, in
                                       int n_sink, int n_window, int32_t *out_ids,
                                       float *out_scores, float *out_block_scores, void *stream);
 
-/* A static, human-readable name for a status code. */
+/*
+ * A static, human-readable name for a status code.  No passage of the pages
+ * defines it; it belongs to this library's status codes (above).
+ */
 const char *msa_status_string(int status);
 
 #ifdef __cplusplus

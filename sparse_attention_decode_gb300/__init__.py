@@ -42,6 +42,7 @@ from ._binding import (  # noqa: F401
     msa_indexer_get_error,
     msa_indexer_merge,
     msa_indexer_score,
+    msa_indexer_test_withhold_pages,
     msa_indexer_workspace_bytes,
     msa_status_string,
     new_workspace,

@@ -52,6 +52,7 @@ EXPORTED = (
     "msa_indexer_prefill_score",
     "msa_indexer_prefill_score_fp8",
     "msa_indexer_prefill_workspace_bytes",
+    "msa_indexer_test_withhold_pages",
 )
 
 _lib = None
@@ -122,6 +123,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.msa_indexer_prefill_score_fp8.argtypes = [P, P, c_int, P, P, c_i64, P, c_i64, P, c_int,
                                                   c_int, P, P, c_size, P]
     lib.msa_indexer_prefill_score_fp8.restype = c_int
+    lib.msa_indexer_test_withhold_pages.argtypes = [c_int]
+    lib.msa_indexer_test_withhold_pages.restype = None
     lib.msa_status_string.argtypes = [c_int]
     lib.msa_status_string.restype = ctypes.c_char_p
     if path is None:
@@ -421,6 +424,11 @@ def msa_indexer_prefill_score_fp8(q, cu_seqlens_q, kcache_fp8, kscale, block_tab
         int(seq_lens.shape[0]), max_model_len, _ptr(out_block_scores), _ptr(workspace),
         int(workspace.numel() * workspace.element_size()), _stream_ptr(stream))
     _check(st, "msa_indexer_prefill_score_fp8")
+
+
+def msa_indexer_test_withhold_pages(on: bool) -> None:
+    """Test hook: while set, decode passes load no page and their waits run out (see the C header)."""
+    load().msa_indexer_test_withhold_pages(1 if on else 0)
 
 
 def msa_indexer_get_error(workspace, *, stream=None) -> int:

@@ -181,7 +181,9 @@ struct WorkspaceHeader {
     uint32_t done;       // CTAs of the running pass done claiming; 0 between passes
     int32_t batch;       // batch of the last score pass
     int32_t kmax;        // list length of the last score pass
-    int32_t reserved0[3];
+    uint32_t epoch;      // score passes completed on this workspace (wraps)
+    uint32_t aborted;    // 1 + the count at the start of the last pass in which a wait ran out
+    int32_t reserved0;
     Partition part;      // chunking of the last score pass (read by the merge)
     uint32_t reserved[(kHeaderBytes - 32 - sizeof(Partition)) / 4];
 };

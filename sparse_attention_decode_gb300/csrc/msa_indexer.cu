@@ -31,7 +31,6 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
-#include <mutex>
 
 #include "../../include/msa_indexer.h"
 #include "keys.cuh"
@@ -130,6 +129,8 @@ struct ScoreParams {
     int n_window;
     int split_blocks;
     int slot_capacity;
+    uint32_t spin_limit;  // polls before a barrier wait gives up
+    int withhold;         // test hook: the producer loads no page and never signals one
 };
 
 constexpr int kChunkQueue = 8;  // chunk ids the producer may post ahead of the consumers
@@ -146,6 +147,7 @@ struct SmemCtl {
     int chunk_q[kChunkQueue];
     int warp_sums[F::kConsumers + 1];
     volatile int abort_flag;
+    uint32_t epoch;  // the workspace's pass count when this pass started
     Partition part;  // this pass's chunking, the same in every CTA
 };
 
@@ -197,6 +199,8 @@ __device__ void build_prefix(const ScoreParams &p, int *prefix, SmemCtl<F> *ctl,
     const int B = p.batch;
     const int per = (B + kThreads - 1) / kThreads;
     const int r0 = min(B, tid * per), r1 = min(B, r0 + per);
+    // the pass count, loaded beside the lengths (it is needed only if a wait runs out)
+    const uint32_t epoch = tid == 0 ? __ldcg(&hdr->epoch) : 0u;
     int local = 0;
     for (int b = r0; b < r1; ++b) {
         const int L = p.seq_lens[b];
@@ -224,6 +228,8 @@ __device__ void build_prefix(const ScoreParams &p, int *prefix, SmemCtl<F> *ctl,
     }
     if (tid == kThreads - 1)
         prefix[B] = before + x;
+    if (tid == 0)
+        ctl->epoch = epoch;
     __syncthreads();
 }
 
@@ -293,19 +299,36 @@ __device__ __forceinline__ void score_page(uint32_t stage,
     }
 }
 
+// Wait for phase `parity` of barrier `bar`, polling at most `limit` times.
+__device__ __forceinline__ bool mbar_wait_n(uint32_t bar, uint32_t parity, uint32_t limit)
+{
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity))
+            return true;
+    return false;
+}
+
+// A wait of this CTA ran out: the fault bit for the caller, and the pass is
+// marked so that the merge empties every output row (its lists are incomplete).
+template <class F>
+__device__ __forceinline__ void give_up(SmemCtl<F> *ctl, WorkspaceHeader *hdr)
+{
+    atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
+    atomicExch(&hdr->aborted, ctl->epoch + 1u);
+    ctl->abort_flag = 1;
+}
+
 // Bounded wait for the whole warp; false (and the CTA's abort flag set) when
 // the wait ran out or another warp already gave up.
 template <class F>
 __device__ __forceinline__ bool warp_wait(SmemCtl<F> *ctl, WorkspaceHeader *hdr, uint32_t bar,
-                                          uint32_t parity)
+                                          uint32_t parity, uint32_t limit)
 {
     bool ok = false;
     if (!ctl->abort_flag) {
-        ok = mbar_wait(bar, parity);
-        if (!ok) {
-            atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
-            ctl->abort_flag = 1;
-        }
+        ok = mbar_wait_n(bar, parity, limit);
+        if (!ok)
+            give_up(ctl, hdr);
     }
     return __all_sync(0xffffffffu, ok);
 }
@@ -490,7 +513,7 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
     for (uint32_t n = 0;; ++n) {
         // next chunk id from the producer
         const int qs = static_cast<int>(n % kChunkQueue);
-        if (!warp_wait(ctl, hdr, smem_addr(&ctl->cq_full[qs]), (n / kChunkQueue) & 1u))
+        if (!warp_wait(ctl, hdr, smem_addr(&ctl->cq_full[qs]), (n / kChunkQueue) & 1u, p.spin_limit))
             break;
         const int c = ctl->chunk_q[qs];
         __syncwarp();
@@ -529,7 +552,8 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
                     q_row = b;
                 }
 
-                const bool ready = warp_wait(ctl, hdr, smem_addr(&ctl->full[s]), P::use_of(my) & 1u);
+                const bool ready =
+                    warp_wait(ctl, hdr, smem_addr(&ctl->full[s]), P::use_of(my) & 1u, p.spin_limit);
                 const int2 meta = ctl->meta[s];
                 float mk[NF][2];  // the page's column maxima (-inf when skipped)
 #pragma unroll
@@ -622,7 +646,7 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
             }
             mbar_arrive(smem_addr(&ctl->list_bar[buf]));  // every consumer thread
             const bool lists_ready =
-                warp_wait(ctl, hdr, smem_addr(&ctl->list_bar[buf]), (segments >> 1) & 1u);
+                warp_wait(ctl, hdr, smem_addr(&ctl->list_bar[buf]), (segments >> 1) & 1u, p.spin_limit);
             ++segments;
             if (!lists_ready)
                 continue;
@@ -733,10 +757,9 @@ __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_
         if (lane == 0) {
             const int qs = static_cast<int>(n % kChunkQueue);
             if (n >= kChunkQueue && !ctl->abort_flag &&
-                !mbar_wait(smem_addr(&ctl->cq_empty[qs]), ((n / kChunkQueue) - 1) & 1u)) {
-                atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
-                ctl->abort_flag = 1;
-            }
+                !mbar_wait_n(smem_addr(&ctl->cq_empty[qs]), ((n / kChunkQueue) - 1) & 1u,
+                             p.spin_limit))
+                give_up(ctl, hdr);
             ctl->chunk_q[qs] = c;
             mbar_arrive(smem_addr(&ctl->cq_full[qs]));
         }
@@ -768,12 +791,14 @@ __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_
                 const int s = P::stage_of(it);
                 const uint32_t full = smem_addr(&ctl->full[s]);
                 if (it >= P::kStages && !ctl->abort_flag) {
-                    if (!mbar_wait(smem_addr(&ctl->empty[s]), (P::use_of(it) - 1) & 1u)) {
-                        atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
-                        ctl->abort_flag = 1;
-                    }
+                    if (!mbar_wait_n(smem_addr(&ctl->empty[s]), (P::use_of(it) - 1) & 1u,
+                                     p.spin_limit))
+                        give_up(ctl, hdr);
                 }
-                const bool issue = ok && !ctl->abort_flag;
+                // with the test hook set nothing is loaded or signalled until a
+                // wait has run out: every stage stays empty, no copy is in flight
+                const bool withheld = p.withhold && !ctl->abort_flag;
+                const bool issue = ok && !ctl->abort_flag && !withheld;
                 ctl->meta[s] = make_int2(valid, issue ? 1 : 0);
                 if (issue) {
                     const uint32_t dst = stage0 + s * F::kDataBytes;
@@ -788,7 +813,7 @@ __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_
                         tma_load_2d_hint(dst + kHalfPageBytes, &p.tmap, 64, page * kPage, full,
                                          stream_policy);
                     }
-                } else {
+                } else if (!withheld) {
                     mbar_arrive(full);
                 }
             }
@@ -809,22 +834,26 @@ __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_
     post(-1);  // no more chunks
 
     // This CTA takes no more tickets; the last CTA to get here resets the
-    // counters for the next pass (every other CTA has stopped claiming).
-    // Without a pool no ticket was taken and the counters stay at zero.
-    if (lane == 0 && part.pool > 0) {
+    // ticket counters for the next pass (every other CTA has stopped claiming)
+    // and counts the pass: every CTA read the pass count at its start, before
+    // its own arrival here.
+    if (lane == 0) {
         __threadfence();
         if (atomicAdd(&hdr->done, 1u) == gridDim.x - 1) {
             atomicExch(&hdr->pool_next, 0u);
             atomicExch(&hdr->done, 0u);
+            atomicAdd(&hdr->epoch, 1u);
         }
     }
     // Drain: no copy may still be landing in shared memory when the CTA exits.
-    if (lane == 0) {
+    // (With the test hook no copy was ever issued.)
+    if (lane == 0 && !p.withhold) {
         const uint32_t cnt = it < P::kStages ? it : P::kStages;
         for (uint32_t i = 0; i < cnt; ++i) {
             const uint32_t q = it - 1 - i;
-            if (!mbar_wait(smem_addr(&ctl->full[P::stage_of(q)]), P::use_of(q) & 1u))
-                atomicOr(&hdr->fault, MSA_FAULT_TIMEOUT);
+            if (!mbar_wait_n(smem_addr(&ctl->full[P::stage_of(q)]), P::use_of(q) & 1u,
+                             p.spin_limit))
+                give_up(ctl, hdr);
         }
     }
 }
@@ -975,8 +1004,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const uint8_t *ws,
 
     const Partition &part = hdr->part;
     const int p0 = prefix[b], p1 = prefix[b + 1];
+    // a wait of the score pass ran out: its lists are incomplete, every row is left empty
+    const bool pass_ok = hdr->aborted != hdr->epoch;
     int c_first = 0, n_lists = 0;
-    if (p1 > p0 && part.unit > 0 && p1 <= part.total) {
+    if (pass_ok && p1 > p0 && part.unit > 0 && p1 <= part.total) {
         c_first = part.chunk_of(p0);
         n_lists = min(part.chunk_of(p1 - 1) - c_first + 1, slot_capacity);
     }
@@ -1111,6 +1142,12 @@ static int score_grid(int sms, int batch, int64_t max_blocks, int split_blocks)
     return static_cast<int>(g < 1 ? 1 : g);
 }
 
+// Test hook for the bounded waits (msa_indexer_test_withhold_pages): passes
+// launched while it is set load no page and give up each wait after
+// kTestSpinLimit polls.
+static std::atomic<int> g_withhold_pages{0};
+constexpr uint32_t kTestSpinLimit = 1u << 14;
+
 // The pool as a 2-D tensor map: rows = num_pages * 128 tokens, 128 elements
 // per row, 128-byte swizzle.  bf16: 64x128 boxes (two per page); fp8
 // (unsigned bytes): one 128x128 box per page.
@@ -1142,6 +1179,9 @@ static msa_status launch_score(const void *q, const void *kcache_pool, const flo
 {
     ScoreParams p;
     std::memset(&p, 0, sizeof p);
+    const bool withhold = g_withhold_pages.load(std::memory_order_relaxed) != 0;
+    p.withhold = withhold ? 1 : 0;
+    p.spin_limit = withhold ? kTestSpinLimit : kSpinLimit;
     if (!make_pool_map<F>(&p.tmap, kcache_pool, num_pages))
         return MSA_ERR_CUDA;
     p.q = static_cast<const uint16_t *>(q);
@@ -1348,29 +1388,20 @@ namespace msa {
 
 static __device__ __align__(256) uint8_t g_noalloc_workspace[MSA_NOALLOC_WORKSPACE_BYTES];
 
-// Device address of g_noalloc_workspace on device `dev` (the current device),
-// looked up once per device.  In host code the array's name only stands in
-// for it; the kernels must be given this address.  The same set-up clears
-// the header once: its ticket counters must start at zero (the score kernel
-// returns them to zero at the end of every pass).
-static void *noalloc_workspace(int dev)
+// Device address of g_noalloc_workspace in the current context.  In host code
+// the array's name only stands in for it; the kernels must be given this
+// address.  It is looked up on every call (a host-side query that allocates
+// nothing and enqueues nothing): each context that loads the library (the
+// primary one, a framework's own, a new one after cudaDeviceReset) holds its
+// own copy of the array at its own address.  Each copy is zero-filled when
+// the module is loaded into its context, which is what the words that must
+// start at zero (the header's ticket counters) need; the score kernel
+// returns them to zero at the end of every pass.
+static void *noalloc_workspace()
 {
-    static std::atomic<void *> addr[kMaxDevices];
-    static std::mutex setup;
-    if (dev < 0 || dev >= kMaxDevices)
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess)
         return nullptr;
-    void *p = addr[dev].load(std::memory_order_acquire);
-    if (p != nullptr)
-        return p;
-    std::lock_guard<std::mutex> lock(setup);
-    p = addr[dev].load(std::memory_order_acquire);
-    if (p != nullptr)
-        return p;
-    if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || p == nullptr)
-        return nullptr;
-    if (cudaMemset(p, 0, kHeaderBytes) != cudaSuccess)
-        return nullptr;
-    addr[dev].store(p, std::memory_order_release);
     return p;
 }
 
@@ -1392,20 +1423,14 @@ extern "C" msa_status msa_indexer_decode_noalloc(const void *q, const void *kcac
                              reinterpret_cast<const void *>(uintptr_t{256}), 0);
     if (st != MSA_OK || batch == 0)
         return st;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return MSA_ERR_CUDA;
-    const int sms = device_sms(dev);
-    if (sms <= 0)
-        return MSA_ERR_CUDA;
-    const int grid = score_grid(sms, batch, blocks_for(max_model_len), 0);
-    const size_t need = slots_offset(batch) +
-                        static_cast<size_t>(chunk_bound(batch, blocks_for(max_model_len), 0, grid) +
-                                            batch) *
-                            slot_bytes(kmax_for(k));
-    if (need > MSA_NOALLOC_WORKSPACE_BYTES)
+    // the same sizing msa_indexer_decode applies to a caller's workspace
+    Plan pl;
+    st = plan(batch, max_batch, max_model_len, k, 0, MSA_NOALLOC_WORKSPACE_BYTES, pl);
+    if (st == MSA_ERR_WORKSPACE_TOO_SMALL)
         return MSA_ERR_UNSUPPORTED;
-    void *ws = noalloc_workspace(dev);
+    if (st != MSA_OK)
+        return st;
+    void *ws = noalloc_workspace();
     if (ws == nullptr)
         return MSA_ERR_CUDA;
     return msa_indexer_decode(q, kcache_pool, num_pages, block_table, bt_stride, seq_lens, batch,
@@ -1552,6 +1577,11 @@ extern "C" msa_status msa_indexer_decode_fp8(const void *q, const void *kcache_f
     if (st != MSA_OK || batch == 0)
         return st;
     return msa_indexer_merge(batch, k, out_ids, out_scores, workspace, workspace_bytes, stream);
+}
+
+extern "C" void msa_indexer_test_withhold_pages(int on)
+{
+    g_withhold_pages.store(on != 0 ? 1 : 0, std::memory_order_relaxed);
 }
 
 extern "C" msa_status msa_indexer_get_error(void *workspace, void *stream, uint32_t *flags)

@@ -35,6 +35,13 @@ def test_header_declares_the_binding_names():
     assert declared_functions() == sorted(msa.EXPORTED)
 
 
+def test_the_package_binds_every_declared_call():
+    import sparse_attention_decode_gb300 as msa
+    for name in declared_functions():
+        if name != "msa_status_string":
+            assert callable(getattr(msa, name, None)), name
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
@@ -44,9 +51,10 @@ def test_workspace_bytes(lib):
     import sparse_attention_decode_gb300 as msa
     n = msa.msa_indexer_workspace_bytes(32, 131072, 16)
     # header 256 + prefix (33 ints -> 256) + (7 chunks x 1024 CTAs + 32) slots x 4 heads x 16 keys x 8 B
-    assert n == 256 + 256 + (7 * 1024 + 32) * 4 * 16 * 8
-    assert msa.msa_indexer_workspace_bytes(32, 131072, 16, 64) == 256 + 256 + (512 + 32) * 512
-    assert msa.msa_indexer_workspace_bytes(32, 131072, 17) == 256 + 256 + (7 * 1024 + 32) * 4 * 32 * 8
+    fixed = 256 + 256
+    assert n == fixed + (7 * 1024 + 32) * 4 * 16 * 8
+    assert msa.msa_indexer_workspace_bytes(32, 131072, 16, 64) == fixed + (512 + 32) * 512
+    assert msa.msa_indexer_workspace_bytes(32, 131072, 17) == fixed + (7 * 1024 + 32) * 4 * 32 * 8
     for bad in [(0, 1024, 16, 0), (32, 0, 16, 0), (32, 1024, 0, 0), (32, 1024, 33, 0),
                 (32, 1024, 16, -1), (5000, 1024, 16, 0)]:
         assert msa.msa_indexer_workspace_bytes(*bad) == 0, bad

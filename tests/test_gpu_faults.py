@@ -93,3 +93,29 @@ def test_argument_errors(msa):
         msa.msa_indexer_decode(q, pool, bt, seq, 16, 1, 2, ids, sc, ws, max_batch=1,
                                max_model_len=1024)
     assert e.value.status == msa.MSA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("split", [0, 2])
+def test_waits_that_run_out_end_the_call_and_leave_the_workspace_usable(msa, orc, split):
+    """The bounded-wait path, made without any fault: with the test hook set,
+    the producer loads no page and signals none (no copy is ever in flight),
+    so every consumer's first page wait runs out after its short poll limit.
+    The call must return, report MSA_FAULT_TIMEOUT and leave every row empty;
+    the next call on the same workspace must match the oracle, which shows the
+    ticket and arrival counters were returned to zero.  split=2 makes the
+    producers claim pool chunks through the ticket counter."""
+    w = wl.decode_point()
+    tensors = parity.to_device(w)
+    ws = msa.new_workspace(w.batch, w.max_model_len, w.k, split)
+    msa.msa_indexer_test_withhold_pages(True)
+    try:
+        ids, sc, blk, fault = parity.run_gpu(w, tensors=tensors, ws=ws, split_blocks=split)
+    finally:
+        msa.msa_indexer_test_withhold_pages(False)
+    assert fault & msa.MSA_FAULT_TIMEOUT
+    assert (ids == -1).all() and np.isneginf(sc).all()
+    o_scores, o_ids, _ = orc.run(w)
+    for _ in range(2):
+        ids, sc, blk, fault = parity.run_gpu(w, tensors=tensors, ws=ws, split_blocks=split)
+        assert fault == 0
+        parity.check(w, o_scores, o_ids, ids, sc, blk)

@@ -198,3 +198,63 @@ def test_max_batch(lib, orc):
     w = wl.random_workload(seq, seed=4096, q_scale=1 / np.sqrt(128), max_model_len=512,
                            name="max_batch")
     _compare(orc, w)
+
+
+@pytest.mark.parametrize("case", ["decode_point", "ragged", "k32", "split1", "max_batch"])
+def test_decode_equals_its_two_stages(lib, case):
+    """msa_indexer_decode and msa_indexer_score followed by msa_indexer_merge
+    must give bitwise-identical ids, scores and block scores, alternating on
+    one workspace (split 1 gives the long request up to 1024 lists)."""
+    import torch
+    k, split = 16, 0
+    if case in ("decode_point", "ragged"):
+        w = wl.make(case)
+    elif case == "k32":
+        w, k = wl.decode_point(), 32
+    elif case == "split1":
+        w, split = wl.ragged(), 1  # up to 1024 lists for the long request
+    else:
+        rng = np.random.default_rng(7)
+        seq = rng.integers(0, 3000, 1500)
+        seq[rng.random(1500) < 0.05] = 0
+        w = wl.random_workload(seq, seed=7, q_scale=1 / np.sqrt(128), max_model_len=4096)
+    q, pool, bt, seq = parity.to_device(w)
+    B, S = w.batch, w.bt_stride
+    ws = lib.new_workspace(B, w.max_model_len, k, split)
+    outs = []
+    for fused in (True, False, True):
+        ids = torch.full((B, 4, k), -7, dtype=torch.int32, device="cuda")
+        sc = torch.full((B, 4, k), 7.0, dtype=torch.float32, device="cuda")
+        blk = torch.full((B, 4, S), float("nan"), dtype=torch.float32, device="cuda")
+        if fused:
+            lib.msa_indexer_decode(q, pool, bt, seq, k, 1, 2, ids, sc, ws,
+                                   max_model_len=w.max_model_len, out_block_scores=blk,
+                                   split_blocks=split)
+        else:
+            lib.msa_indexer_score(q, pool, bt, seq, k, 1, 2, ws, max_model_len=w.max_model_len,
+                                  out_block_scores=blk, split_blocks=split)
+            lib.msa_indexer_merge(B, k, ids, sc, ws)
+        outs.append([t.cpu().numpy() for t in (ids, sc, blk)])
+    assert lib.msa_indexer_get_error(ws) == 0
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            np.testing.assert_array_equal(a, b)
+
+
+def test_one_workspace_across_changing_batches(lib):
+    """A serving loop calls the indexer with a different batch every step on
+    one workspace sized for the largest.  The state one call leaves for the
+    next (ticket and arrival counters) must not depend on where the batch-sized
+    regions of the workspace fall, so each call equals the same call on a fresh
+    workspace, bit for bit."""
+    max_batch, max_len, k = 300, 4096, 16
+    ws = lib.new_workspace(max_batch, max_len, k)
+    rng = np.random.default_rng(11)
+    for step, B in enumerate([16, 3, 300, 1, 77, 300, 16]):
+        seq = rng.integers(0, max_len + 1, B)
+        w = wl.random_workload(seq, seed=500 + step, q_scale=1 / np.sqrt(128), max_model_len=max_len)
+        shared = parity.run_gpu(w, ws=ws, max_batch=max_batch)
+        fresh = parity.run_gpu(w, max_batch=max_batch)
+        assert shared[3] == 0 and fresh[3] == 0
+        for a, b in zip(shared[:3], fresh[:3]):
+            np.testing.assert_array_equal(a, b, err_msg=f"step {step} B={B}")

@@ -190,11 +190,18 @@ def replay(seq, max_model_len, bt_stride, split_blocks, sms, rng, fmt=FORMATS["b
             q, h = divmod(u, fmt[2])
             assert use_of(q, h, fmt) == uses[stage_of(q, h, fmt)]
     assert len(seen) == total
+    segments = [0] * B
+    for (c, b) in written.values():
+        segments[b] += 1
     for b in range(B):
         if prefix[b + 1] > prefix[b]:
             first, last = part.chunk_of(prefix[b]), part.chunk_of(prefix[b + 1] - 1)
             for c in range(first, last + 1):
                 assert written[c + b] == (c, b)
+            # one list per (chunk, request) segment: the merge reads exactly these
+            assert segments[b] == last - first + 1
+        else:
+            assert segments[b] == 0
     return grid, part
 
 
