@@ -101,16 +101,20 @@ struct Req {
     bool ok;
 };
 
+// A request from its row range [c0, c1) and length.
+__device__ __forceinline__ Req make_req(int c0, int c1, int len, int total_q, int seq_limit)
+{
+    Req r;
+    r.c0 = c0;
+    r.n = c1 - c0;
+    r.len = len;
+    r.ok = c0 >= 0 && c1 <= total_q && r.n >= 0 && len >= 0 && len <= seq_limit && r.n <= len;
+    return r;
+}
 __device__ __forceinline__ Req req_info(const int32_t *cu_q, const int32_t *seq_lens, int total_q,
                                         int seq_limit, int b)
 {
-    Req r;
-    r.c0 = cu_q[b];
-    const int c1 = cu_q[b + 1];
-    r.n = c1 - r.c0;
-    r.len = seq_lens[b];
-    r.ok = r.c0 >= 0 && c1 <= total_q && r.n >= 0 && r.len >= 0 && r.len <= seq_limit && r.n <= r.len;
-    return r;
+    return make_req(cu_q[b], cu_q[b + 1], seq_lens[b], total_q, seq_limit);
 }
 
 __device__ __forceinline__ int tiles_of(const Req &r) { return (r.n + kTileTokens - 1) / kTileTokens; }
@@ -742,10 +746,27 @@ static msa_status prefill_entry(const void *q, const int32_t *cu_seqlens_q, int 
         return s;
     const int64_t rows = static_cast<int64_t>(total_q) * kHeads;
     const bool k16 = kmax_for(k) == 16;
-    const int per = k16 ? rows_per_cta<16>() : rows_per_cta<32>();
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return MSA_ERR_CUDA;
+    static std::atomic<bool> topk_attr_done[kMaxDevices];
+    if (dev >= 0 && dev < kMaxDevices && !topk_attr_done[dev].load(std::memory_order_acquire)) {
+        if (cudaFuncSetAttribute(rows_topk_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kTopkSmemBytes)) != cudaSuccess ||
+            cudaFuncSetAttribute(rows_topk_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kTopkSmemBytes)) != cudaSuccess)
+            return MSA_ERR_CUDA;
+        topk_attr_done[dev].store(true, std::memory_order_release);
+    }
+    // persistent: every warp walks rows a grid's worth of warps apart
+    const int64_t ctas = (rows + kTopkRowsPerCta - 1) / kTopkRowsPerCta;
+    const int sms = device_sms(dev);
+    if (sms <= 0)
+        return MSA_ERR_CUDA;
+    const int64_t resident = static_cast<int64_t>(sms) * kTopkCtasPerSm;
     cudaLaunchAttribute attr2[1];
-    cudaLaunchConfig_t cfg2 = pdl_config(dim3(static_cast<unsigned>((rows + per - 1) / per)),
-                                         dim3(32 * per), 0, st, attr2);
+    cudaLaunchConfig_t cfg2 = pdl_config(dim3(static_cast<unsigned>(ctas < resident ? ctas : resident)),
+                                         dim3(32 * kTopkRowsPerCta), kTopkSmemBytes, st, attr2);
     cudaError_t e = k16 ? cudaLaunchKernelEx(&cfg2, rows_topk_kernel<16>, static_cast<const float *>(p.scores),
                                              p.bs_stride, cu_seqlens_q, seq_lens, batch, total_q,
                                              p.seq_limit, k, n_sink, n_window, out_ids, out_scores)

@@ -3,20 +3,28 @@
 The kernel keeps, per (token, head) row, the pins (the first n_sink and the
 last n_window visible blocks) and the highest-scoring free blocks, ties to
 the lower block id, blocks whose page was out of range (-inf) left out.  It
-seeds its running list with the pins, then passes the row's blocks 512 at a
-time (lane l holds blocks g0 + 32 i + l) through a bound on 32-bit coarse
-keys: the KMAX-th largest lane maximum until the list is full, the list's
-last key after.  Only blocks at or above the bound are merged.  This replays
+seeds its running list with the pins, then reads the row's blocks 1024 at a
+time (lane l holds blocks g0 + 128 i + 4 l + e, i < 8, e < 4) and keeps only
+those whose fp32 score is at or above one bound: the KMAX-th largest lane
+maximum while the list is not full, the score of the list's last key after
+(+inf when that key is a pin), and never -inf.  Up to 64 candidates are
+merged; a group with more (ties) merges all its free blocks.  This replays
 those steps (restated from the kernel) on rows built to stress them (ties,
--0, -inf, sorted rows that overflow the candidate space, short rows) and
-checks every row against a brute-force sort of all its keys.
+-0, -inf, sorted rows, short rows, pins that fill the list) and checks every
+row against a brute-force sort of all its keys.
 """
 
 import numpy as np
 import pytest
 
-GROUP, LANES, PER_LANE = 512, 32, 16
+GROUP, LANES, PER_LANE, CAP = 1024, 32, 32, 64
 NEG_INF = np.float32(-np.inf)
+FLT_LOWEST = np.float32(-3.402823466e38)
+
+
+def lane_of(j_in_group):
+    """Lane holding block g0 + j of a group (16-byte loads: 4 blocks a lane, 128 a row of lanes)."""
+    return (j_in_group % 128) // 4
 
 
 def order_bits(x):
@@ -45,6 +53,27 @@ def top(keys, width):
     return out + [0] * (width - len(out))
 
 
+def tail_bound(key):
+    if key == 0:
+        return NEG_INF
+    if key >> 63:
+        return np.float32(np.inf)
+    o = (key >> 31) & 0xFFFFFFFF
+    u = (o & 0x7FFFFFFF) if o & 0x80000000 else (~o & 0xFFFFFFFF)
+    return np.uint32(u).view(np.float32)
+
+
+def group_bound(vals, kmax):
+    """kmax 16: the 16th largest lane maximum; 32: the 32nd largest of the lane
+    maxima and second maxima."""
+    per_lane = [[] for _ in range(LANES)]
+    for off, v in enumerate(vals):
+        per_lane[lane_of(off)].append(v)
+    take = 1 if kmax == 16 else 2
+    pool = [x for lane in per_lane for x in sorted(lane, reverse=True)[:take]]
+    return sorted(pool, reverse=True)[kmax - 1]
+
+
 def kernel_row(scores, nb, k, n_sink, n_window, kmax):
     """The kernel's steps for one row; returns its descending key list (k)."""
     ns = min(n_sink, nb)
@@ -55,20 +84,17 @@ def kernel_row(scores, nb, k, n_sink, n_window, kmax):
         j = lane if lane < ns else w0 + (lane - ns)
         pins.append(0 if scores[j] == NEG_INF else pack(scores[j], j, True))
     run = top(pins, kmax)  # in id order already, or compacted by a merge
-    cap = kmax * PER_LANE
-    floor = order_bits(NEG_INF) + 1
     for g0 in range(0, nb, GROUP):
         js = np.arange(g0, g0 + GROUP)
-        vals = [scores[j] if j < nb else NEG_INF for j in js]
-        ck = [order_bits(v) for v in vals]
+        vals = np.array([scores[j] if j < nb else NEG_INF for j in js], dtype=np.float32)
         tail = run[kmax - 1]
-        lane_bound = 0
         if tail == 0:
-            lane_max = [max(ck[LANES * i + lane] for i in range(PER_LANE)) for lane in range(LANES)]
-            lane_bound = sorted(lane_max, reverse=True)[kmax - 1]
-        bound = max(lane_bound, coarse(tail), floor)
-        cand = [(int(j), v) for j, v, c in zip(js, vals, ck) if c >= bound]
-        if len(cand) <= cap:
+            bound = group_bound(vals, kmax)
+        else:
+            bound = tail_bound(tail)
+        bound = max(np.float32(bound), FLT_LOWEST)
+        cand = [(int(j), v) for j, v in zip(js, vals) if v >= bound]
+        if len(cand) <= CAP:
             keys = [0 if (j < ns or j >= w0) else pack(v, j, False) for j, v in cand]
         else:  # ties overflow the candidate space: every free block of the group
             keys = [pack(v, int(j), False) for j, v in zip(js, vals)
@@ -117,23 +143,21 @@ def test_filter_matches_brute_force(kmax, kind):
         assert got == brute_row(s, nb, k, n_sink, n_window), (kind, nb, k, n_sink, n_window)
 
 
+def test_pins_that_fill_the_list_admit_no_free_block():
+    s = np.random.default_rng(9).standard_normal(300).astype(np.float32)
+    got = kernel_row(s, 300, 16, 8, 8, 16)
+    assert got == brute_row(s, 300, 16, 8, 8)
+    assert all(key >> 63 for key in got)
+
+
 def test_bound_prunes_on_long_rows():
-    """On a long row of random scores the bound keeps the merges small."""
+    """On a row of random scores the bound leaves a few dozen candidates."""
     rng = np.random.default_rng(5)
-    nb, kmax = 1024, 16
-    s = rng.standard_normal(nb).astype(np.float32)
-    ns, w0 = 1, nb - 2
-    run = top([pack(s[0], 0, True), pack(s[nb - 2], nb - 2, True), pack(s[nb - 1], nb - 1, True)], kmax)
     sizes = []
-    for g0 in range(0, nb, GROUP):
-        ck = [order_bits(s[j]) for j in range(g0, g0 + GROUP)]
-        tail = run[kmax - 1]
-        lane_bound = 0
-        if tail == 0:
-            lane_max = [max(ck[LANES * i + lane] for i in range(PER_LANE)) for lane in range(LANES)]
-            lane_bound = sorted(lane_max, reverse=True)[kmax - 1]
-        bound = max(lane_bound, coarse(tail))
-        cand = [g0 + i for i, c in enumerate(ck) if c >= bound]
-        sizes.append(len(cand))
-        run = top(run + [pack(s[j], j, False) for j in cand if ns <= j < w0], kmax)
-    assert sizes[0] <= 64 and sizes[1] <= 32, sizes
+    for kmax in (16, 32):
+        for _ in range(20):
+            s = rng.standard_normal(GROUP).astype(np.float32)
+            bound = group_bound(s, kmax)
+            sizes.append(int((s >= bound).sum()))
+            assert sizes[-1] >= kmax
+    assert max(sizes) <= CAP, sizes
