@@ -36,11 +36,11 @@ if ROOT not in sys.path:
 METRIC = "indexer decode µs/call and index-K HBM GB/s (B=32, 128K ctx) vs GB300 peak"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = {"bf16": os.path.join(ROOT, "profiles", "score_kernel_long_context.md"),
-                   "fp8": os.path.join(ROOT, "profiles", "score_kernel_fp8_long_context.md"),
-                   "prefill": os.path.join(ROOT, "profiles", "prefill_kernel_chunked_128k.md"),
-                   "prefill_fp8": os.path.join(ROOT, "profiles",
-                                               "prefill_fp8_kernel_chunked_128k.md")}
+# Machine-written ncu records (bench.py --record-profile) behind roofline.traffic,
+# by the path the bench line reports: name of profiles/<name>.json.
+PROFILE_RECORDS = {"bf16": "score_kernel_long_context", "fp8": "score_kernel_fp8_long_context",
+                   "prefill": "prefill_kernel_chunked_128k",
+                   "prefill_fp8": "prefill_fp8_kernel_chunked_128k"}
 PREFILL_METRIC = "prefill index-score TFLOP/s (4 x 2048 new tokens at 128K ctx) vs GB300 bf16 peak"
 PREFILL_PAIRS = [(2048, 131072)] * 4  # (new tokens, tokens) per request
 CSRC = os.path.join(ROOT, "sparse_attention_decode_gb300", "csrc")
@@ -62,6 +62,18 @@ def parse_args(argv=None):
                     help="time the SGLang page's batch x context shapes (bf16 and fp8 caches)")
     ap.add_argument("--configs", action="store_true",
                     help="time every named workload (one JSON line each) instead of the headline")
+    ap.add_argument("--profile-workload", choices=["tiny", "decode_point", "long_context", "ragged",
+                                                   "adversarial"],
+                    help="run --steps eager decode calls on this workload and exit (for ncu)")
+    ap.add_argument("--record-profile", metavar="NAME",
+                    help="write profiles/NAME.json from --ncu-report and exit (no GPU needed)")
+    ap.add_argument("--ncu-report", help="the .ncu-rep --record-profile reads")
+    ap.add_argument("--source-path", choices=["decode", "prefill", "prefill_fp8", "rows_topk"],
+                    default="decode",
+                    help="which kernel sources the recorded capture was taken on")
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="factor from the captured launch's traffic to the full workload's")
+    ap.add_argument("--command", default="", help="the capture command, stored in the record")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args(argv)
@@ -136,16 +148,21 @@ DECODE_SOURCES = ("host_util.cuh", "keys.cuh", "layout.cuh", "msa_indexer.cu", "
                   os.path.join("..", "..", "include", "msa_indexer.h"))
 
 
+# The prefill translation unit's kernels: the bf16 score kernel, the E4M3 one
+# (its own header) and the per-row top-k (its own header).
 PREFILL_SOURCES = ("host_util.cuh", "keys.cuh", "layout.cuh", "prefill.cu", "ptx.cuh",
                    "tcgen05.cuh", os.path.join("..", "..", "include", "msa_indexer.h"))
-
 PREFILL_FP8_SOURCES = PREFILL_SOURCES + ("prefill_fp8.cuh",)
+ROWS_TOPK_SOURCES = ("host_util.cuh", "keys.cuh", "layout.cuh", "prefill.cu", "ptx.cuh",
+                     "rows_topk.cuh", os.path.join("..", "..", "include", "msa_indexer.h"))
+SOURCE_SETS = {"decode": DECODE_SOURCES, "prefill": PREFILL_SOURCES,
+               "prefill_fp8": PREFILL_FP8_SOURCES, "rows_topk": ROWS_TOPK_SOURCES}
 
 
 def kernel_source_hash(path: str = "decode") -> str:
-    """Hash of a path's kernel sources: a profile taken at another hash is stale."""
+    """Hash of a kernel's sources: a profile taken at another hash is stale."""
     h = hashlib.sha256()
-    names = {"prefill": PREFILL_SOURCES, "prefill_fp8": PREFILL_FP8_SOURCES}.get(path, DECODE_SOURCES)
+    names = SOURCE_SETS[path]
     for name in names:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
@@ -154,17 +171,98 @@ def kernel_source_hash(path: str = "decode") -> str:
 
 
 def profiled_traffic(batch: int, cache: str = "bf16"):
-    """DRAM bytes per score launch from the committed ncu summary, if it is current."""
+    """DRAM bytes per launch of the path's dominant kernel from its committed ncu
+    record (profiles/<name>.json), scaled to `batch` requests of 32, or None
+    when the record is missing or was taken on other kernel sources."""
     try:
-        text = open(PROFILE_SUMMARY[cache]).read()
-    except OSError:
+        with open(os.path.join(ROOT, "profiles", PROFILE_RECORDS[cache] + ".json")) as f:
+            rec = json.load(f)
+    except (OSError, KeyError, ValueError):
         return None
-    m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
-    m_bytes = re.search(r"dram_bytes_per_launch_full_batch:\s*([0-9]+)", text)
-    path = cache if cache.startswith("prefill") else "decode"
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(path):
+    if rec.get("source_sha256_16") != kernel_source_hash(rec.get("source_path", "")):
         return None
-    return int(m_bytes.group(1)) * batch // 32
+    if rec["source_path"] != ("decode" if cache in ("bf16", "fp8") else cache):
+        return None
+    return int(rec["dram_bytes_per_launch_full_batch"]) * batch // 32
+
+
+_NCU_SCALE = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12,
+              "ns": 1e-9, "us": 1e-6, "usecond": 1e-6, "ms": 1e-3, "msecond": 1e-3, "s": 1.0}
+NCU_FIELDS = ("gpu__time_duration.sum", "dram__bytes_read.sum", "dram__bytes_write.sum",
+              "gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed",
+              "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_active",
+              "smsp__issue_active.avg.pct_of_peak_sustained_active",
+              "sm__warps_active.avg.pct_of_peak_sustained_active",
+              "smsp__inst_executed.sum", "launch__registers_per_thread", "launch__grid_size",
+              "launch__block_size", "launch__shared_mem_per_block_dynamic")
+
+
+def read_ncu_report(report: str):
+    """Every launch in an ncu report (ncu -i ... --page raw --csv): kernel name and
+    the NCU_FIELDS present, bytes in bytes, times in seconds."""
+    import csv
+    out = subprocess.run(["ncu", "-i", report, "--page", "raw", "--csv"], check=True,
+                         capture_output=True, text=True).stdout
+    rows = [r for r in csv.reader(out.splitlines()) if r]
+    head, units = rows[0], rows[1]
+    launches = []
+    for r in rows[2:]:
+        rec = {"kernel": r[head.index("Kernel Name")]}
+        for name in NCU_FIELDS:
+            if name in head:
+                i = head.index(name)
+                v = float(r[i].replace(",", ""))
+                rec[name] = v * _NCU_SCALE.get(units[i].split("/")[0], 1)
+        launches.append(rec)
+    return launches
+
+
+def record_profile(name: str, report: str, path: str, scale: float, command: str):
+    """Writes profiles/<name>.json from an ncu report of one launch: the counters,
+    DRAM read + write per launch scaled by `scale` to the full workload, and the
+    hash of the kernel sources it was taken on."""
+    launches = read_ncu_report(report)
+    if not launches:
+        raise SystemExit(f"{report}: no launch")
+    first = launches[0]
+    traffic = first["dram__bytes_read.sum"] + first["dram__bytes_write.sum"]
+    rec = {"profile": name, "report": os.path.basename(report), "command": command,
+           "source_path": path, "source_sha256_16": kernel_source_hash(path),
+           "launches": launches, "dram_bytes_per_launch": int(traffic),
+           "scale_to_full_workload": scale,
+           "dram_bytes_per_launch_full_batch": int(round(traffic * scale))}
+    out = os.path.join(ROOT, "profiles", name + ".json")
+    with open(out, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    return out
+
+
+def run_profile_workload(args):
+    """A few eager decode calls on one named workload: the command put under ncu
+    to capture that workload's launches (no timing, no JSON line)."""
+    import numpy as np
+    import torch
+
+    import sparse_attention_decode_gb300 as msa
+    import workloads as wl
+
+    device = torch.device("cuda", 0)
+    msa.load()
+    w = wl.make(args.profile_workload)
+    q = torch.from_numpy(w.q.view(np.int16)).view(torch.bfloat16).to(device)
+    pool = torch.from_numpy(w.pool.view(np.int16)).view(torch.bfloat16).to(device)
+    bt = torch.from_numpy(w.block_table).to(device)
+    seq = torch.from_numpy(w.seq_lens).to(device)
+    ids = torch.empty((w.batch, 4, w.k), dtype=torch.int32, device=device)
+    sc = torch.empty((w.batch, 4, w.k), dtype=torch.float32, device=device)
+    ws = msa.new_workspace(w.batch, w.max_model_len, w.k, device=device)
+    for _ in range(args.steps):
+        msa.msa_indexer_decode(q, pool, bt, seq, w.k, w.n_sink, w.n_window, ids, sc, ws,
+                               max_model_len=w.max_model_len)
+    torch.cuda.synchronize(device)
+    print(json.dumps({"profile_workload": w.name, "calls": args.steps,
+                      "index_k_bytes": w.index_k_bytes, "fault": msa.msa_indexer_get_error(ws)}))
 
 
 class ClockSampler:
@@ -995,6 +1093,13 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.record_profile:
+        print(record_profile(args.record_profile, args.ncu_report, args.source_path, args.scale,
+                             args.command))
+        return
+    if args.profile_workload and args.impl != "reference":
+        run_profile_workload(args)
+        return
     if args.configs and args.impl != "reference":
         for line in run_configs(args):
             print(json.dumps(line), flush=True)

@@ -392,13 +392,15 @@ msa_status msa_indexer_get_error(void *workspace, void *stream, uint32_t *flags)
 /*
  * Test hook for the bounded waits.  No passage of the pages corresponds; it
  * exists so that a test can make the decode kernel's waits run out without
- * any fault: while `on` is non-zero, decode and score passes enqueued
- * afterwards load no index-K page and never signal one, so every consumer's
- * first page wait runs out after a short poll limit (about 2^14 polls)
+ * any fault: while `on` is non-zero, bf16 one-position decode and score
+ * passes with k <= 16 enqueued afterwards run a separately built copy of the
+ * score kernel that loads no index-K page and never signals one, so every
+ * consumer's first page wait runs out after a short poll limit (2^14 polls)
  * instead of the normal one; no asynchronous copy is in flight at any time.
  * The pass then sets MSA_FAULT_TIMEOUT and its merge writes -1 / -inf to
- * every output row.  Set it back to 0 for normal operation.  Not thread-safe with
- * concurrent decode calls in other threads (the flag is process-wide).
+ * every output row.  Other shapes return MSA_ERR_UNSUPPORTED while it is
+ * set.  Set it back to 0 for normal operation.  The flag is process-wide:
+ * do not set it while other threads run decode calls.
  */
 void msa_indexer_test_withhold_pages(int on);
 

@@ -31,6 +31,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 
 #include "../../include/msa_indexer.h"
 #include "keys.cuh"
@@ -129,11 +130,18 @@ struct ScoreParams {
     int n_window;
     int split_blocks;
     int slot_capacity;
-    uint32_t spin_limit;  // polls before a barrier wait gives up
-    int withhold;         // test hook: the producer loads no page and never signals one
 };
 
 constexpr int kChunkQueue = 8;  // chunk ids the producer may post ahead of the consumers
+
+// Polls before a barrier wait gives up.  TH selects the kernel built for the
+// bounded-wait test hook (msa_indexer_test_withhold_pages): its producer
+// loads and signals no page, and its waits give up after far fewer polls.
+// Both are compile-time: a wait bound read at run time slowed the E4M3
+// kernel's page waits by ~11 %.
+constexpr uint32_t kTestSpinLimit = 1u << 14;
+template <bool TH>
+constexpr uint32_t kWaitPolls = TH ? kTestSpinLimit : kSpinLimit;
 
 template <class F>
 struct SmemCtl {
@@ -469,7 +477,7 @@ __device__ __forceinline__ void load_query(const ScoreParams &p, int b, int lane
     }
 }
 
-template <int KMAX, class F, int NQ>
+template <int KMAX, class F, int NQ, bool TH>
 __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_t *smem,
                              SmemCtl<F> *ctl, const int *prefix, WorkspaceHeader *hdr,
                              uint64_t *g_slots)
@@ -513,7 +521,7 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
     for (uint32_t n = 0;; ++n) {
         // next chunk id from the producer
         const int qs = static_cast<int>(n % kChunkQueue);
-        if (!warp_wait(ctl, hdr, smem_addr(&ctl->cq_full[qs]), (n / kChunkQueue) & 1u, p.spin_limit))
+        if (!warp_wait(ctl, hdr, smem_addr(&ctl->cq_full[qs]), (n / kChunkQueue) & 1u, kWaitPolls<TH>))
             break;
         const int c = ctl->chunk_q[qs];
         __syncwarp();
@@ -553,7 +561,7 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
                 }
 
                 const bool ready =
-                    warp_wait(ctl, hdr, smem_addr(&ctl->full[s]), P::use_of(my) & 1u, p.spin_limit);
+                    warp_wait(ctl, hdr, smem_addr(&ctl->full[s]), P::use_of(my) & 1u, kWaitPolls<TH>);
                 const int2 meta = ctl->meta[s];
                 float mk[NF][2];  // the page's column maxima (-inf when skipped)
 #pragma unroll
@@ -646,7 +654,8 @@ __device__ void run_consumer(const ScoreParams &p, const Partition &part, uint8_
             }
             mbar_arrive(smem_addr(&ctl->list_bar[buf]));  // every consumer thread
             const bool lists_ready =
-                warp_wait(ctl, hdr, smem_addr(&ctl->list_bar[buf]), (segments >> 1) & 1u, p.spin_limit);
+                warp_wait(ctl, hdr, smem_addr(&ctl->list_bar[buf]), (segments >> 1) & 1u,
+                          kWaitPolls<TH>);
             ++segments;
             if (!lists_ready)
                 continue;
@@ -741,7 +750,7 @@ __device__ __forceinline__ int resolve_ticket(const Partition &part, WorkspaceHe
     return c;
 }
 
-template <int KMAX, class F, int NQ>
+template <int KMAX, class F, int NQ, bool TH>
 __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_t *smem,
                              SmemCtl<F> *ctl, const int *prefix, WorkspaceHeader *hdr)
 {
@@ -758,7 +767,7 @@ __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_
             const int qs = static_cast<int>(n % kChunkQueue);
             if (n >= kChunkQueue && !ctl->abort_flag &&
                 !mbar_wait_n(smem_addr(&ctl->cq_empty[qs]), ((n / kChunkQueue) - 1) & 1u,
-                             p.spin_limit))
+                             kWaitPolls<TH>))
                 give_up(ctl, hdr);
             ctl->chunk_q[qs] = c;
             mbar_arrive(smem_addr(&ctl->cq_full[qs]));
@@ -792,12 +801,12 @@ __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_
                 const uint32_t full = smem_addr(&ctl->full[s]);
                 if (it >= P::kStages && !ctl->abort_flag) {
                     if (!mbar_wait_n(smem_addr(&ctl->empty[s]), (P::use_of(it) - 1) & 1u,
-                                     p.spin_limit))
+                                     kWaitPolls<TH>))
                         give_up(ctl, hdr);
                 }
                 // with the test hook set nothing is loaded or signalled until a
                 // wait has run out: every stage stays empty, no copy is in flight
-                const bool withheld = p.withhold && !ctl->abort_flag;
+                const bool withheld = TH && !ctl->abort_flag;
                 const bool issue = ok && !ctl->abort_flag && !withheld;
                 ctl->meta[s] = make_int2(valid, issue ? 1 : 0);
                 if (issue) {
@@ -847,18 +856,18 @@ __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_
     }
     // Drain: no copy may still be landing in shared memory when the CTA exits.
     // (With the test hook no copy was ever issued.)
-    if (lane == 0 && !p.withhold) {
+    if (lane == 0 && !TH) {
         const uint32_t cnt = it < P::kStages ? it : P::kStages;
         for (uint32_t i = 0; i < cnt; ++i) {
             const uint32_t q = it - 1 - i;
             if (!mbar_wait_n(smem_addr(&ctl->full[P::stage_of(q)]), P::use_of(q) & 1u,
-                             p.spin_limit))
+                             kWaitPolls<TH>))
                 give_up(ctl, hdr);
         }
     }
 }
 
-template <int KMAX, class F, int NQ>
+template <int KMAX, class F, int NQ, bool TH = false>
 __global__ void __launch_bounds__(Pipe<F>::kThreads, 1)
     score_kernel(const __grid_constant__ ScoreParams p)
 {
@@ -912,9 +921,9 @@ __global__ void __launch_bounds__(Pipe<F>::kThreads, 1)
     }
 
     if (warp == P::kProducerWarp)
-        run_producer<KMAX, F, NQ>(p, part, smem, ctl, prefix, hdr);
+        run_producer<KMAX, F, NQ, TH>(p, part, smem, ctl, prefix, hdr);
     else
-        run_consumer<KMAX, F, NQ>(p, part, smem, ctl, prefix, hdr, g_slots);
+        run_consumer<KMAX, F, NQ, TH>(p, part, smem, ctl, prefix, hdr, g_slots);
 }
 
 // Selected blocks -> small KV pages for one (request, head) row, by one full
@@ -1071,14 +1080,14 @@ __global__ void __launch_bounds__(128) expand_pages_kernel(const int32_t *ids, i
 // host side
 // ---------------------------------------------------------------------------
 
-template <int KMAX, class F, int NQ>
+template <int KMAX, class F, int NQ, bool TH = false>
 static bool ensure_smem_attr(int dev)
 {
     static std::atomic<bool> done[kMaxDevices];
     if (dev >= 0 && dev < kMaxDevices && done[dev].load(std::memory_order_acquire))
         return true;
     const size_t bytes = SmemLayout<KMAX, F, NQ>::bytes(MSA_MAX_BATCH);
-    if (cudaFuncSetAttribute(score_kernel<KMAX, F, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(score_kernel<KMAX, F, NQ, TH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(bytes)) != cudaSuccess)
         return false;
     if (dev >= 0 && dev < kMaxDevices)
@@ -1142,11 +1151,10 @@ static int score_grid(int sms, int batch, int64_t max_blocks, int split_blocks)
     return static_cast<int>(g < 1 ? 1 : g);
 }
 
-// Test hook for the bounded waits (msa_indexer_test_withhold_pages): passes
-// launched while it is set load no page and give up each wait after
-// kTestSpinLimit polls.
+// Test hook for the bounded waits (msa_indexer_test_withhold_pages): while it
+// is set, bf16 one-position passes with k <= 16 run score_kernel<16, Bf16Fmt,
+// 1, true> (no page loaded, short waits); other shapes are refused.
 static std::atomic<int> g_withhold_pages{0};
-constexpr uint32_t kTestSpinLimit = 1u << 14;
 
 // The pool as a 2-D tensor map: rows = num_pages * 128 tokens, 128 elements
 // per row, 128-byte swizzle.  bf16: 64x128 boxes (two per page); fp8
@@ -1180,8 +1188,8 @@ static msa_status launch_score(const void *q, const void *kcache_pool, const flo
     ScoreParams p;
     std::memset(&p, 0, sizeof p);
     const bool withhold = g_withhold_pages.load(std::memory_order_relaxed) != 0;
-    p.withhold = withhold ? 1 : 0;
-    p.spin_limit = withhold ? kTestSpinLimit : kSpinLimit;
+    if (withhold && !(KMAX == 16 && NQ == 1 && std::is_same<F, Bf16Fmt>::value))
+        return MSA_ERR_UNSUPPORTED;
     if (!make_pool_map<F>(&p.tmap, kcache_pool, num_pages))
         return MSA_ERR_CUDA;
     p.q = static_cast<const uint16_t *>(q);
@@ -1199,11 +1207,20 @@ static msa_status launch_score(const void *q, const void *kcache_pool, const flo
     p.n_window = n_window;
     p.split_blocks = split_blocks;
     p.slot_capacity = slot_capacity;
-    if (!ensure_smem_attr<KMAX, F, NQ>(dev))
-        return MSA_ERR_CUDA;
     const size_t smem = SmemLayout<KMAX, F, NQ>::bytes(batch);
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(Pipe<F>::kThreads), smem, st, attr);
+    if constexpr (KMAX == 16 && NQ == 1 && std::is_same<F, Bf16Fmt>::value) {
+        if (withhold) {
+            if (!ensure_smem_attr<16, Bf16Fmt, 1, true>(dev))
+                return MSA_ERR_CUDA;
+            return cudaLaunchKernelEx(&cfg, score_kernel<16, Bf16Fmt, 1, true>, p) == cudaSuccess
+                       ? MSA_OK
+                       : MSA_ERR_CUDA;
+        }
+    }
+    if (!ensure_smem_attr<KMAX, F, NQ>(dev))
+        return MSA_ERR_CUDA;
     return cudaLaunchKernelEx(&cfg, score_kernel<KMAX, F, NQ>, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 

@@ -1,5 +1,6 @@
 """bench.py's host logic: rank aggregation under gloo (world size 2) and helpers."""
 
+import json
 import os
 import socket
 
@@ -63,15 +64,32 @@ def test_clock_sampler_parses_nvidia_smi_rows():
     assert c["reasons"] == ["sw_power_cap"]
 
 
-def test_profiled_traffic_requires_a_current_summary(tmp_path, monkeypatch):
-    path = tmp_path / "summary.md"
-    monkeypatch.setattr(bench, "PROFILE_SUMMARY", {"bf16": str(path)})
+def test_profiled_traffic_requires_a_current_record(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    path = tmp_path / "profiles" / (bench.PROFILE_RECORDS["bf16"] + ".json")
     assert bench.profiled_traffic(32) is None
-    path.write_text(f"source_sha256_16: {bench.kernel_source_hash()}\n"
-                    "dram_bytes_per_launch_full_batch: 1000\n")
-    assert bench.profiled_traffic(32) == 1000
-    path.write_text("source_sha256_16: 0000000000000000\ndram_bytes_per_launch_full_batch: 1000\n")
+    rec = {"source_path": "decode", "source_sha256_16": bench.kernel_source_hash("decode"),
+           "dram_bytes_per_launch_full_batch": 1000}
+    path.write_text(json.dumps(rec))
+    assert bench.profiled_traffic(32) == 1000 and bench.profiled_traffic(8) == 250
+    path.write_text(json.dumps(dict(rec, source_sha256_16="0000000000000000")))
     assert bench.profiled_traffic(32) is None
+    # a record of the prefill sources does not stand for the decode kernel
+    path.write_text(json.dumps(dict(rec, source_path="prefill",
+                                    source_sha256_16=bench.kernel_source_hash("prefill"))))
+    assert bench.profiled_traffic(32) is None
+
+
+def test_committed_records_are_machine_written():
+    """Every profiles/*.json has the fields --record-profile writes."""
+    import glob
+    for f in glob.glob(os.path.join(bench.ROOT, "profiles", "*.json")):
+        rec = json.load(open(f))
+        for key in ("profile", "report", "command", "source_path", "source_sha256_16",
+                    "launches", "dram_bytes_per_launch", "dram_bytes_per_launch_full_batch"):
+            assert key in rec, (f, key)
+        assert rec["source_path"] in bench.SOURCE_SETS
 
 
 def test_peak_falls_back_when_no_measurement(monkeypatch, tmp_path):
@@ -80,10 +98,12 @@ def test_peak_falls_back_when_no_measurement(monkeypatch, tmp_path):
     assert v == bench.FALLBACK_HBM_GBS and src.startswith("fallback")
 
 
-def test_fp8_prefill_profile_hash_covers_its_kernel():
-    """The fp8 prefill kernel lives in its own header: a change there must
-    invalidate its profile and not the bf16 prefill one."""
+def test_prefill_profile_hashes_cover_their_kernels():
+    """The E4M3 prefill kernel and the per-row top-k live in their own headers:
+    a change there must invalidate their profiles and not the bf16 prefill one."""
     assert "prefill_fp8.cuh" in bench.PREFILL_FP8_SOURCES
     assert "prefill_fp8.cuh" not in bench.PREFILL_SOURCES
-    assert bench.kernel_source_hash("prefill_fp8") != bench.kernel_source_hash("prefill")
-    assert bench.kernel_source_hash("prefill") != bench.kernel_source_hash("decode")
+    assert "rows_topk.cuh" in bench.ROWS_TOPK_SOURCES
+    assert "rows_topk.cuh" not in bench.PREFILL_SOURCES
+    hashes = {p: bench.kernel_source_hash(p) for p in bench.SOURCE_SETS}
+    assert len(set(hashes.values())) == len(hashes)
