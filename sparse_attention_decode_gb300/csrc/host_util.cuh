@@ -68,6 +68,20 @@ static int device_sms(int dev)
     return v;
 }
 
+// L2 size of device `dev` in bytes (0 when the query fails).
+static int64_t device_l2_bytes(int dev)
+{
+    static std::atomic<int> cache[kMaxDevices];
+    int v = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (v > 0)
+        return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess || v <= 0)
+        return 0;
+    if (dev >= 0 && dev < kMaxDevices)
+        cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
 static int64_t blocks_for(int max_model_len) { return (static_cast<int64_t>(max_model_len) + kPage - 1) / kPage; }
 
 }  // namespace msa

@@ -130,6 +130,7 @@ struct ScoreParams {
     int n_window;
     int split_blocks;
     int slot_capacity;
+    int l2_keep_pages;  // passes of at most this many pages keep them in L2
 };
 
 constexpr int kChunkQueue = 8;  // chunk ids the producer may post ahead of the consumers
@@ -760,7 +761,10 @@ __device__ void run_producer(const ScoreParams &p, const Partition &part, uint8_
     const uint32_t scale0 = smem_addr(smem + SmemLayout<KMAX, F, NQ>::scales);
     uint32_t it = 0;  // pages issued
     uint32_t n = 0;   // chunk ids posted
-    const uint64_t stream_policy = l2_evict_first_policy();  // K is read once per pass
+    // K is read once per pass: evicted first, unless the whole pass fits in
+    // half of L2, where repeated calls on the same pages can find them there
+    const uint64_t stream_policy =
+        part.total <= p.l2_keep_pages ? l2_evict_normal_policy() : l2_evict_first_policy();
 
     auto post = [&](int c) {
         if (lane == 0) {
@@ -1207,6 +1211,7 @@ static msa_status launch_score(const void *q, const void *kcache_pool, const flo
     p.n_window = n_window;
     p.split_blocks = split_blocks;
     p.slot_capacity = slot_capacity;
+    p.l2_keep_pages = static_cast<int>(device_l2_bytes(dev) / 2 / (F::kDataBytes + F::kScaleBytes));
     const size_t smem = SmemLayout<KMAX, F, NQ>::bytes(batch);
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pdl_config(dim3(grid), dim3(Pipe<F>::kThreads), smem, st, attr);

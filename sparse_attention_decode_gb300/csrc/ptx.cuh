@@ -97,6 +97,13 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy()
     return pol;
 }
 
+__device__ __forceinline__ uint64_t l2_evict_normal_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 // 2-D tiled TMA load with an L2 cache policy.
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, int x, int y,
                                                  uint32_t bar, uint64_t policy)
