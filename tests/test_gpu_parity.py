@@ -258,3 +258,12 @@ def test_one_workspace_across_changing_batches(lib):
         assert shared[3] == 0 and fresh[3] == 0
         for a, b in zip(shared[:3], fresh[:3]):
             np.testing.assert_array_equal(a, b, err_msg=f"step {step} B={B}")
+
+
+def test_million_token_request(lib, orc):
+    """One request of 2^20 tokens beside short and empty ones: its 8192 pages
+    spread over every CTA, so the merge folds more lists than one staged tile
+    holds."""
+    w = wl.random_workload([1 << 20, 3000, 0, 129], seed=77, q_scale=1 / np.sqrt(128),
+                           max_model_len=1 << 20)
+    _compare(orc, w)

@@ -308,3 +308,16 @@ def test_prefill_many_requests(msa, orc):
     got = run_prefill(msa, w, q, cu)
     assert got[3] == 0
     check_prefill(orc, w, q, cu, got)
+
+
+@pytest.mark.parametrize("max_len,k", [(300032, 16), (300160, 16), (300032, 32)])
+def test_prefill_rows_longer_than_one_group(msa, orc, max_len, k):
+    """Rows of more than 1024 blocks (contexts past 128K tokens): the per-row
+    top-k takes them 1024 at a time, the first group copied ahead into shared
+    memory and later ones loaded in place.  A row stride of 2345 blocks (not a
+    multiple of four) takes the plain-load path instead of 16-byte copies."""
+    pairs = [(24, 300000), (8, 140001), (4, 1000)]
+    w, q, cu = prefill_case(pairs, seed=290 + k + max_len % 7, max_model_len=max_len)
+    got = run_prefill(msa, w, q, cu, k=k)
+    assert got[3] == 0
+    check_prefill(orc, w, q, cu, got, k=k)
