@@ -23,7 +23,10 @@
 //              (tiles of 32 tokens would allow four buffers but load every
 //              page for half as many rows: 1.3x slower when measured)
 //   warps 2-9  read their rows' 128 accumulators per page from TMEM and
-//              write the masked block max (keys <= the row's position).
+//              write the masked block max (keys <= the row's position);
+//   warp 10    waits, page by page, for the stage to be full and the
+//              accumulator buffer to be free, and counts the pages that may
+//              be multiplied in a shared word the issuing thread polls.
 //
 // rows_topk_kernel (rows_topk.cuh): one warp per (token, head) row: pins and
 // top-k over the row's block scores.
@@ -49,7 +52,8 @@ constexpr int kMRows = 128;                           // rows per MMA: 32 tokens
 constexpr int kMTiles = kTileTokens * kHeads / kMRows;  // 2
 constexpr int kTcStages = 4;
 constexpr int kEpiWarps = 4 * kMTiles;                // one per (TMEM lane quarter, M tile)
-constexpr int kTcThreads = 32 * (2 + kEpiWarps);
+constexpr int kWaiterWarp = 2 + kEpiWarps;
+constexpr int kTcThreads = 32 * (3 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;                   // the whole tensor memory
 constexpr int kAccBufs = kTmemCols / (kMTiles * kPage);  // accumulator buffers (pages in flight)
 static_assert(kPage % kTileTokens == 0 && kAccBufs >= 2, "tile geometry");
@@ -84,6 +88,7 @@ struct TcSmem {
     uint64_t acc_empty[kAccBufs];
     uint64_t mma_done;
     uint32_t tmem_base;
+    uint32_t ready;  // pages whose operands and accumulator buffer the issuing thread may use
     int abort;
     int b0, t0, j0;  // the range's first unit
     int b1, t1, j1;  // its last unit + 1 page
@@ -302,6 +307,24 @@ __device__ __forceinline__ void give_up(const TcParams &p, Ctl *ctl)
     *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
 }
 
+// The issuing thread's wait for page `need - 1` of its range: the waiter
+// warp raises `ready` to n once pages 0 .. n-1 have their stage full and
+// their accumulator buffer free.  Two mbarrier waits per page in the issuing
+// thread cost it ~500 of the ~1700 cycles a page took; one acquire load of a
+// counter that is usually already there leaves it free to issue.
+template <class Ctl>
+__device__ __forceinline__ bool wait_ready(Ctl *ctl, uint32_t need)
+{
+    const uint32_t addr = smem_addr(&ctl->ready);
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (ld_acquire_shared_u32(addr) >= need)
+            return true;
+        if (aborted(ctl))
+            return false;
+    }
+    return false;
+}
+
 // The MMAs of pages [j0, je) of one segment, by the issuing thread: per page,
 // NMT M tiles of 8 tcgen05.mma each.  NMT = 1 for a tile whose second M tile
 // holds no new token (its epilogue writes nothing); the choice is made once
@@ -315,8 +338,7 @@ __device__ __forceinline__ bool mma_pages(const TcParams &p, TcSmem *ctl, uint32
     for (int j = j0; j < je; ++j) {
         const int s = static_cast<int>(kc % kTcStages);
         const int a = static_cast<int>(ac % kAccBufs);
-        if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->k_full[s]), (kc / kTcStages) & 1u) ||
-            (ac >= kAccBufs && !mbar_wait(smem_addr(&ctl->acc_empty[a]), ((ac / kAccBufs) - 1) & 1u))) {
+        if (!wait_ready(ctl, kc + 1)) {
             give_up(p, ctl);
             return false;
         }
@@ -369,6 +391,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
         }
         mbar_init(smem_addr(&ctl->mma_done), 1);
         ctl->abort = 0;
+        ctl->ready = 0;
         fence_barrier_init();
     }
     griddep_wait();
@@ -497,6 +520,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
             umma_commit(smem_addr(&ctl->mma_done));
             if (!mbar_wait(smem_addr(&ctl->mma_done), 0))
                 give_up(p, ctl);
+        }
+        __syncwarp();
+    } else if (warp == kWaiterWarp) {
+        // ---------------- waiter: page kc may be multiplied ----------------
+        // (pages are issued in order; page kc uses stage kc mod S and
+        // accumulator buffer kc mod A)
+        if (lane == 0) {
+            const uint32_t addr = smem_addr(&ctl->ready);
+            for (uint32_t kc = 0; kc < static_cast<uint32_t>(units); ++kc) {
+                const int s = static_cast<int>(kc % kTcStages);
+                const int a = static_cast<int>(kc % kAccBufs);
+                if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->k_full[s]), (kc / kTcStages) & 1u) ||
+                    (kc >= kAccBufs && !mbar_wait(smem_addr(&ctl->acc_empty[a]), ((kc / kAccBufs) - 1) & 1u))) {
+                    give_up(p, ctl);
+                    break;
+                }
+                st_release_shared_u32(addr, kc + 1);
+            }
         }
         __syncwarp();
     } else {

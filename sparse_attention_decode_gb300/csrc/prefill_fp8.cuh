@@ -26,8 +26,11 @@
 //                the quarter's 32 rows): first its 16 query rows to f16 in
 //                place (per segment), then per page their scaled, masked
 //                block max (sixteen warps of 16 rows: half the per-page
-//                work of each, against eight of 32).
-// (22 warps: up to six on one SM sub-partition, whose 16K-register file then
+//                work of each, against eight of 32);
+//   warp 22      waiter: per page, the converted stage full and the
+//                accumulator buffer free, counted in a shared word that the
+//                issuing thread polls (as in the bf16 kernel).
+// (23 warps: up to six on one SM sub-partition, whose 16K-register file then
 // allows 80 registers a thread; the register cap keeps the kernel there.)
 #pragma once
 
@@ -41,7 +44,8 @@ constexpr int kF8FirstEpiWarp = 2 + kF8ConvWarps;
 constexpr int kF8EpiWarps = 16;             // four per TMEM lane quarter: 2 M tiles x 2 row halves
 static_assert(kF8EpiWarps == 4 * 2 * kMTiles && kMTiles == 2,
               "the epilogue maps warp e to M tile e / 8 and row half (e / 4) % 2");
-constexpr int kF8Threads = 32 * (kF8FirstEpiWarp + kF8EpiWarps);
+constexpr int kF8WaiterWarp = kF8FirstEpiWarp + kF8EpiWarps;
+constexpr int kF8Threads = 32 * (kF8WaiterWarp + 1);
 constexpr uint32_t kF8RawBytes = kPage * kDim;  // 16 KiB of codes
 constexpr uint32_t kF8ScaleBytes = kPage * 4;   // 512 B
 constexpr uint32_t kIdescF16 = umma_idesc_f16_f32(kMRows, kPage);
@@ -60,6 +64,7 @@ struct F8Smem {
     uint64_t acc_empty[kAccBufs];
     uint64_t mma_done;
     uint32_t tmem_base;
+    uint32_t ready;  // pages the issuing thread may multiply (the waiter warp's count)
     int abort;
     int b0, t0, j0;  // the range's first unit
     int b1, t1, j1;  // its last unit + 1 page
@@ -141,8 +146,8 @@ __device__ __forceinline__ void scaled_max_frag(const uint32_t (&r)[16], const f
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// 22 warps leave six on two SM sub-partitions, whose 16K registers then hold
-// 80 a thread (a multiple of 8); the cap keeps the launch inside that.
+// 23 warps leave six on three SM sub-partitions, whose 16K registers then
+// hold 80 a thread (a multiple of 8); the cap keeps the launch inside that.
 constexpr int kF8MaxRegs = (16384 / (32 * ((kF8Threads / 32 + 3) / 4))) & ~7;
 static_assert(kF8MaxRegs >= 64, "too many warps for the register file");
 
@@ -181,6 +186,7 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
         }
         mbar_init(smem_addr(&ctl->mma_done), 1);
         ctl->abort = 0;
+        ctl->ready = 0;
         fence_barrier_init();
     }
     griddep_wait();
@@ -299,9 +305,7 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
                 for (int j = c.j; j < je; ++j) {
                     const int s = static_cast<int>(kc % kF8OpStages);
                     const int a = static_cast<int>(ac % kAccBufs);
-                    if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->op_full[s]), (kc / kF8OpStages) & 1u) ||
-                        (ac >= kAccBufs &&
-                         !mbar_wait(smem_addr(&ctl->acc_empty[a]), ((ac / kAccBufs) - 1) & 1u))) {
+                    if (!wait_ready(ctl, kc + 1)) {
                         give_up(p, ctl);
                         ok_run = false;
                         break;
@@ -389,6 +393,22 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
                 mbar_arrive(smem_addr(&ctl->sc_full[slot]));
             }
         }
+    } else if (warp == kF8WaiterWarp) {
+        // ---------------- waiter: page kc may be multiplied ----------------
+        if (lane == 0) {
+            const uint32_t addr = smem_addr(&ctl->ready);
+            for (uint32_t kc = 0; kc < static_cast<uint32_t>(units); ++kc) {
+                const int s = static_cast<int>(kc % kF8OpStages);
+                const int a = static_cast<int>(kc % kAccBufs);
+                if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->op_full[s]), (kc / kF8OpStages) & 1u) ||
+                    (kc >= kAccBufs && !mbar_wait(smem_addr(&ctl->acc_empty[a]), ((kc / kAccBufs) - 1) & 1u))) {
+                    give_up(p, ctl);
+                    break;
+                }
+                st_release_shared_u32(addr, kc + 1);
+            }
+        }
+        __syncwarp();
     } else {
         // ---------------- epilogue: query row to f16, then block scores ----------------
         const int e = warp - kF8FirstEpiWarp;

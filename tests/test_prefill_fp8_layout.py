@@ -1,8 +1,8 @@
 """CPU replay of the E4M3 prefill kernel's warp roles and row mappings.
 
-Restated from the kernel: 22 warps; warp 0 producer, warp 2 MMA issue,
+Restated from the kernel: 23 warps; warp 0 producer, warp 2 MMA issue,
 warps 1 and 3-5 convert one key row per thread, warps 6-21 are the
-epilogue.  Epilogue warp e (warp 6 + e) may read only the TMEM lanes of its
+epilogue and warp 22 waits on the barriers for the issuing thread.  Epilogue warp e (warp 6 + e) may read only the TMEM lanes of its
 quarter (warp % 4); it owns M tile e / 8 and the 16 rows 32 q + 16 ((e / 4)
 % 2) of that quarter.  Per page it reads those 16 rows in the mma-fragment
 layout (lane (g, c) holds rows g and g + 8, columns 8 i + 2 c + {0, 1}) and
@@ -13,7 +13,7 @@ a row, one half of its 128 dimensions each.
 from collections import Counter
 
 TILE_TOKENS, HEADS, M_ROWS, M_TILES, PAGE = 64, 4, 128, 2, 128
-FIRST_EPI, EPI_WARPS, WARPS = 6, 16, 22
+FIRST_EPI, EPI_WARPS, WAITER, WARPS = 6, 16, 22, 23
 CONVERTERS = (1, 3, 4, 5)
 
 
@@ -26,6 +26,8 @@ def roles():
             out[w] = "mma"
         elif w < FIRST_EPI:
             out[w] = "converter"
+        elif w == WAITER:
+            out[w] = "waiter"
         else:
             out[w] = "epilogue"
     return out
@@ -43,6 +45,7 @@ def test_roles_and_register_budget():
     r = roles()
     assert [w for w in r if r[w] == "converter"] == list(CONVERTERS)
     assert sum(v == "epilogue" for v in r.values()) == EPI_WARPS
+    assert [w for w in r if r[w] == "waiter"] == [WAITER] and WAITER == FIRST_EPI + EPI_WARPS
     # the MMA warp's SM sub-partition (warp % 4) holds no converter warp
     assert all(w % 4 != 2 % 4 for w in CONVERTERS)
     per_sub = Counter(w % 4 for w in range(WARPS))
