@@ -307,6 +307,20 @@ __device__ __forceinline__ void give_up(const TcParams &p, Ctl *ctl)
     *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
 }
 
+// A shared-memory word published by one thread (release) and polled by
+// another (acquire), CTA scope.
+__device__ __forceinline__ uint32_t ld_acquire_shared_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_shared_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // The issuing thread's wait for page `need - 1` of its range: the waiter
 // warp raises `ready` to n once pages 0 .. n-1 have their stage full and
 // their accumulator buffer free.  Two mbarrier waits per page in the issuing

@@ -127,20 +127,6 @@ __device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void *src, ui
         : "memory");
 }
 
-// A shared-memory word published by one thread (release) and polled by
-// another (acquire), CTA scope.
-__device__ __forceinline__ uint32_t ld_acquire_shared_u32(uint32_t addr)
-{
-    uint32_t v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release_shared_u32(uint32_t addr, uint32_t v)
-{
-    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr)
 {
     uint32_t v;
