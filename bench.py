@@ -882,7 +882,7 @@ def run_prefill_bench(args):
                   "no flush",
         },
         "roofline": {
-            "bound": "tensor", "kernel": "tc_prefill_fp8_kernel" if fp8 else "tc_prefill_score_kernel",
+            "bound": "tensor", "kernel": "tc_prefill_fp8_kernel" if fp8 else "tc_prefill_pair_kernel",
             "achieved": round(achieved, 1), "peak": peak, "peak_source": peak_src,
             "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
             "traffic": profiled_traffic(32, "prefill_fp8" if fp8 else "prefill"),

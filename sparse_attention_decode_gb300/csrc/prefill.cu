@@ -8,25 +8,15 @@
 // tokens, its last ones: new token t sits at position seq_len_b - n_b + t and
 // sees tokens [0, position].
 //
-// tc_prefill_score_kernel (persistent, one CTA per SM): the product of the
-// new tokens' query rows (token x head) with the keys is a dense contraction,
-// run on the 5th-generation tensor cores.  Work unit = (tile of 64 new tokens
-// of one request, one visible page of that tile); the units of the whole
-// batch, in order, are cut into one equal range per CTA (the page counts
-// have a closed form), which balances the causal triangle.  Per CTA:
-//   warp 0     TMA producer: the tile's 256 query rows (64 KiB, 128B swizzle)
-//              and the pages (32 KiB each) through a 4-stage ring;
-//   warp 1     owns the TMEM allocation; one thread issues tcgen05.mma
-//              (M = 128 rows, N = 128 keys, K = 16) for both 128-row halves
-//              of the tile against each page, fp32 accumulators in TMEM,
-//              double-buffered across pages (2 x 2 x 128 = 512 columns);
-//              (tiles of 32 tokens would allow four buffers but load every
-//              page for half as many rows: 1.3x slower when measured)
-//   warps 2-9  read their rows' 128 accumulators per page from TMEM and
-//              write the masked block max (keys <= the row's position);
-//   warp 10    waits, page by page, for the stage to be full and the
-//              accumulator buffer to be free, and counts the pages that may
-//              be multiplied in a shared word the issuing thread polls.
+// tc_prefill_pair_kernel (persistent, clusters of two CTAs, one CTA per SM):
+// the product of the new tokens' query rows (token x head) with the keys is a
+// dense contraction, run on the 5th-generation tensor cores, the two SMs of a
+// cluster multiplying as one (tcgen05 cta_group::2).  Work unit = (tile of 64
+// new tokens of one request, one visible page of that tile); the units of the
+// whole batch, in order, are cut into one equal range per pair of CTAs (the
+// page counts have a closed form), which balances the causal triangle.  The
+// kernel itself is described where it is defined; tc_prefill_fp8_kernel
+// (prefill_fp8.cuh) does the same on the E4M3 cache with one CTA per SM.
 //
 // rows_topk_kernel (rows_topk.cuh): one warp per (token, head) row: pins and
 // top-k over the row's block scores.
@@ -48,18 +38,14 @@
 namespace msa {
 
 constexpr int kTileTokens = 64;                       // new tokens per work tile
-constexpr int kMRows = 128;                           // rows per MMA: 32 tokens x 4 heads
+constexpr int kMRows = 128;                           // rows per M tile: 32 tokens x 4 heads
 constexpr int kMTiles = kTileTokens * kHeads / kMRows;  // 2
-constexpr int kTcStages = 4;
-constexpr int kEpiWarps = 4 * kMTiles;                // one per (TMEM lane quarter, M tile)
-constexpr int kWaiterWarp = 2 + kEpiWarps;
-constexpr int kTcThreads = 32 * (3 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;                   // the whole tensor memory
-constexpr int kAccBufs = kTmemCols / (kMTiles * kPage);  // accumulator buffers (pages in flight)
+// E4M3 kernel (one CTA per SM): accumulator buffers of both M tiles x 128 keys
+constexpr int kAccBufs = kTmemCols / (kMTiles * kPage);
 static_assert(kPage % kTileTokens == 0 && kAccBufs >= 2, "tile geometry");
 constexpr int kQTileBytes = kMRows * kDim * 2;        // 32 KiB per M tile
 constexpr uint32_t kQBytes = kMTiles * kQTileBytes;
-constexpr uint32_t kIdesc = umma_idesc_bf16_f32(kMRows, kPage);
 
 struct TcParams {
     CUtensorMap kmap;  // pool: bf16 [num_pages*128][128] in 64x128 boxes, or E4M3
@@ -78,25 +64,6 @@ struct TcParams {
     int seq_limit;
     int total_q;
 };
-
-struct TcSmem {
-    uint64_t k_full[kTcStages];
-    uint64_t k_empty[kTcStages];
-    uint64_t q_full;
-    uint64_t q_empty;
-    uint64_t acc_full[kAccBufs];
-    uint64_t acc_empty[kAccBufs];
-    uint64_t mma_done;
-    uint32_t tmem_base;
-    uint32_t ready;  // pages whose operands and accumulator buffer the issuing thread may use
-    int abort;
-    int b0, t0, j0;  // the range's first unit
-    int b1, t1, j1;  // its last unit + 1 page
-    long long units;
-};
-
-constexpr size_t kTcSmemBytes = 1024 /* alignment slack */ + kQBytes +
-                                static_cast<size_t>(kTcStages) * kPageBytes + sizeof(TcSmem);
 
 // One request as the kernels see it.  ok = false for a request they refuse:
 // rows outside [0, total_q) or out of order, a length past the limit or
@@ -260,7 +227,7 @@ __device__ __forceinline__ void locate_unit(const TcParams &p, long long u, int 
 // (tile, page) units in order.  Run by one warp; writes its first and last
 // positions and its unit count.
 template <class Ctl>
-__device__ void plan_range(const TcParams &p, Ctl *ctl, int lane)
+__device__ void plan_range(const TcParams &p, Ctl *ctl, int lane, long long G, long long g)
 {
     long long W = 0;
     for (int b0 = 0; b0 < p.batch; b0 += 32) {
@@ -273,7 +240,6 @@ __device__ void plan_range(const TcParams &p, Ctl *ctl, int lane)
         }
         W += warp_sum64(v);
     }
-    const long long G = gridDim.x, g = blockIdx.x;
     const long long u0 = W * g / G, u1 = W * (g + 1) / G;
     if (u1 <= u0) {
         if (lane == 0)
@@ -321,11 +287,13 @@ __device__ __forceinline__ void st_release_shared_u32(uint32_t addr, uint32_t v)
     asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-// The issuing thread's wait for page `need - 1` of its range: the waiter
-// warp raises `ready` to n once pages 0 .. n-1 have their stage full and
-// their accumulator buffer free.  Two mbarrier waits per page in the issuing
-// thread cost it ~500 of the ~1700 cycles a page took; one acquire load of a
-// counter that is usually already there leaves it free to issue.
+// The issuing thread's wait for its unit of work number need - 1 (a page, or
+// a pair of pages): the waiter warp raises `ready` to n once units 0 .. n-1
+// have their operands in shared memory and their accumulator buffer free.  An
+// mbarrier wait costs the thread that makes it ~250 cycles even when the
+// phase has long completed; two a page in the issuing thread cost it ~500 of
+// the ~1700 cycles a page took.  This load of a counter that is usually
+// already there is cheaper, and the waits happen on another warp.
 template <class Ctl>
 __device__ __forceinline__ bool wait_ready(Ctl *ctl, uint32_t need)
 {
@@ -339,69 +307,93 @@ __device__ __forceinline__ bool wait_ready(Ctl *ctl, uint32_t need)
     return false;
 }
 
-// The MMAs of pages [j0, je) of one segment, by the issuing thread: per page,
-// NMT M tiles of 8 tcgen05.mma each.  NMT = 1 for a tile whose second M tile
-// holds no new token (its epilogue writes nothing); the choice is made once
-// per segment so the per-page issue path carries no branch.  Returns false
-// when a wait ran out.
-template <int NMT>
-__device__ __forceinline__ bool mma_pages(const TcParams &p, TcSmem *ctl, uint32_t tmem,
-                                          uint32_t q_smem, uint32_t k_smem, int j0, int je,
-                                          uint32_t &kc, uint32_t &ac)
-{
-    for (int j = j0; j < je; ++j) {
-        const int s = static_cast<int>(kc % kTcStages);
-        const int a = static_cast<int>(ac % kAccBufs);
-        if (!wait_ready(ctl, kc + 1)) {
-            give_up(p, ctl);
-            return false;
-        }
-        tc_fence_after_sync();
-        // descriptors as base low words plus byte offsets >> 4: one integer add
-        // per operand keeps the single issuing thread ahead of the tensor pipe
-        const uint32_t a_lo = umma_desc_lo(q_smem);
-        const uint32_t b_lo = umma_desc_lo(k_smem + s * kPageBytes);
-        const uint32_t d0 = tmem + static_cast<uint32_t>(a * kMTiles * kPage);
-#pragma unroll
-        for (int mt = 0; mt < NMT; ++mt) {
-#pragma unroll
-            for (int ks = 0; ks < kDim / 16; ++ks) {
-                const uint32_t off = ((ks >> 2) * kHalfPageBytes + (ks & 3) * 32) >> 4;
-                const uint32_t qo = (mt * kQTileBytes) >> 4;
-                if (ks == 0)
-                    umma_f16<false>(d0 + mt * kPage, a_lo + qo + off, b_lo + off, kIdesc);
-                else
-                    umma_f16<true>(d0 + mt * kPage, a_lo + qo + off, b_lo + off, kIdesc);
-            }
-        }
-        umma_commit(smem_addr(&ctl->k_empty[s]));
-        umma_commit(smem_addr(&ctl->acc_full[a]));
-        ++kc;
-        ++ac;
-    }
-    return true;
-}
+// ---------------- pairs of SMs, two pages per MMA (bf16 cache) ----------------
+// tc_prefill_pair_kernel: the (tile, page) units split over clusters of two
+// CTAs that multiply as one (tcgen05 cta_group::2).  A tile's 256 query rows
+// are split 128 / 128 between the even and the odd CTA; its pages are taken
+// two at a time, the even CTA holding the first page of each pair and the odd
+// CTA the second (a segment's odd last page is paired with nothing).  One
+// thread of the even CTA issues 8 MMAs of M = 256 rows x N = 256 keys x
+// K = 16 per pair of pages; each SM's tensor core computes its own 128 rows x
+// 256 keys (128 cycles an MMA), into its own TMEM (two accumulator buffers of
+// 256 columns).  A single thread issues a tcgen05.mma in ~70 cycles whatever
+// its size, so with M = 128 x N = 128 MMAs (64 cycles of tensor work each)
+// the issuing thread, not the tensor pipe, set the pace (~1500 cycles a page
+// against 1024); here it issues a pair's 8 MMAs in ~700 cycles against 1024.
+// Each SM still reads one page from L2 or DRAM per 256 rows multiplied.
+// Per CTA:
+//   warp 0     TMA producer: its 128 query rows at each tile, its page of
+//              each pair through a 6-stage ring;
+//   warp 1     TMEM allocation (both CTAs, collectively); even CTA: one
+//              thread issues the MMAs; odd CTA: one thread tells the even CTA
+//              that its query rows and each of its pages have landed;
+//   warps 2-9  epilogue: warps 2-5 the pair's first page, 6-9 its second,
+//              one TMEM lane quarter each: all 128 columns of the warp's rows
+//              into registers, the accumulator buffer handed back to the even
+//              CTA at once, then the masked block max (reducing before the
+//              hand-back left the issuing thread waiting ~650 cycles a pair);
+//   warp 10    even CTA: waits for both pages of a pair and a free
+//              accumulator buffer and counts the pairs the issuing thread
+//              may multiply.
+// Every wait is bounded; a CTA that gives up still meets its partner at the
+// final cluster barrier, after which TMEM is freed.
+constexpr int kP2Stages = 6;
+constexpr int kP2AccBufs = 2;
+constexpr uint32_t kP2TmemCols = kP2AccBufs * 2 * kPage;  // 512
+constexpr uint32_t kP2QBytes = kMRows * kDim * 2;          // 32 KiB: 128 query rows
+constexpr uint32_t kP2QHalf = kP2QBytes / 2;               // 128 rows x 64 dims
+constexpr uint32_t kP2Idesc = umma_idesc_bf16_f32(2 * kMRows, 2 * kPage);
+constexpr int kP2EpiWarps = 8;
+constexpr int kP2WaiterWarp = 2 + kP2EpiWarps;
+constexpr int kP2Threads = 32 * (3 + kP2EpiWarps);
+static_assert(kP2TmemCols <= 512, "TMEM columns");
 
-__global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const __grid_constant__ TcParams p)
+struct P2Smem {
+    uint64_t k_full[kP2Stages];
+    uint64_t k_peer[kP2Stages];  // even CTA: the odd CTA's page of the stage has landed
+    uint64_t k_empty[kP2Stages];
+    uint64_t q_full;
+    uint64_t q_peer;             // even CTA: the odd CTA's query rows have landed
+    uint64_t q_empty;
+    uint64_t acc_full[kP2AccBufs];
+    uint64_t acc_empty[kP2AccBufs];  // even CTA: both CTAs' epilogue warps
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    uint32_t ready;  // even CTA: pairs of pages the issuing thread may multiply
+    int abort;
+    int b0, t0, j0;
+    int b1, t1, j1;
+    long long units;
+};
+
+constexpr size_t kP2SmemBytes = 1024 + kP2QBytes + static_cast<size_t>(kP2Stages) * kPageBytes + sizeof(P2Smem);
+static_assert(kP2SmemBytes <= 227 * 1024, "shared memory per CTA");
+
+__device__ __forceinline__ int pairs_of(int j, int je) { return (je - j + 1) / 2; }
+
+__global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __grid_constant__ TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t q_smem = smem_addr(smem);
-    const uint32_t k_smem = q_smem + kQBytes;
-    TcSmem *ctl = reinterpret_cast<TcSmem *>(smem + kQBytes + kTcStages * kPageBytes);
+    const uint32_t k_smem = q_smem + kP2QBytes;
+    P2Smem *ctl = reinterpret_cast<P2Smem *>(smem + kP2QBytes + kP2Stages * kPageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: the CTA that issues the MMAs
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kTcStages; ++s) {
+        for (int s = 0; s < kP2Stages; ++s) {
             mbar_init(smem_addr(&ctl->k_full[s]), 1);
+            mbar_init(smem_addr(&ctl->k_peer[s]), 1);
             mbar_init(smem_addr(&ctl->k_empty[s]), 1);
         }
         mbar_init(smem_addr(&ctl->q_full), 1);
+        mbar_init(smem_addr(&ctl->q_peer), 1);
         mbar_init(smem_addr(&ctl->q_empty), 1);
-        for (int a = 0; a < kAccBufs; ++a) {
+        for (int a = 0; a < kP2AccBufs; ++a) {
             mbar_init(smem_addr(&ctl->acc_full[a]), 1);
-            mbar_init(smem_addr(&ctl->acc_empty[a]), kEpiWarps);
+            mbar_init(smem_addr(&ctl->acc_empty[a]), 2 * kP2EpiWarps);
         }
         mbar_init(smem_addr(&ctl->mma_done), 1);
         ctl->abort = 0;
@@ -411,14 +403,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
     griddep_wait();
     griddep_launch_dependents();
     if (warp == 0)
-        plan_range(p, ctl, lane);
-    __syncthreads();
+        plan_range(p, ctl, lane, gridDim.x / 2, blockIdx.x / 2);
+    __syncwarp();
+    // both CTAs' barriers are initialised before either arrives on the other's
+    cluster_sync_all();
     const long long units = ctl->units;
     if (units <= 0)
-        return;  // uniform: no TMEM taken yet
+        return;  // the same for both CTAs of the pair: no TMEM taken yet
     if (warp == 1) {
-        tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
-        tmem_relinquish_alloc_permit();
+        tmem_alloc_pair(smem_addr(&ctl->tmem_base), kP2TmemCols);
+        tmem_relinquish_pair();
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -428,11 +422,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
     const int eb = ctl->b1, et = ctl->t1, ej = ctl->j1;
 
     if (warp == 0) {
-        // ---------------- producer ----------------
+        // ---------------- producer (both CTAs) ----------------
         Cursor c;
         c.load(p, sb, st, sj, eb, et, ej);
         long long left = units;
-        uint32_t kc = 0, seg = 0;
+        uint32_t gc = 0, seg = 0;
         bool ok_run = true;
         while (left > 0 && ok_run) {
             const int je = c.je;
@@ -442,37 +436,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
                     ok_run = false;
                 } else {
                     const uint32_t qf = smem_addr(&ctl->q_full);
-                    const int row0 = (c.r.c0 + kTileTokens * c.t) * kHeads;
-                    mbar_arrive_expect_tx(qf, kQBytes);
-#pragma unroll
-                    for (int mt = 0; mt < kMTiles; ++mt)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            tma_load_2d(q_smem + mt * kQTileBytes + h * kHalfPageBytes, &p.qmap, 64 * h,
-                                        row0 + mt * kMRows, qf);
+                    const int row0 = (c.r.c0 + kTileTokens * c.t) * kHeads + kMRows * static_cast<int>(rank);
+                    mbar_arrive_expect_tx(qf, kP2QBytes);
+                    tma_load_2d(q_smem, &p.qmap, 0, row0, qf);
+                    tma_load_2d(q_smem + kP2QHalf, &p.qmap, 64, row0, qf);
                 }
             }
             ok_run = __shfl_sync(0xffffffffu, ok_run ? 1 : 0, 0) != 0;
-            for (int jb = c.j; jb < je && ok_run; jb += 32) {
-                const int jl = jb + lane;
+            const int ng = pairs_of(c.j, je);
+            for (int gb = 0; gb < ng && ok_run; gb += 32) {
+                const int gl = gb + lane;
+                const int jl = c.j + 2 * gl + static_cast<int>(rank);  // this CTA's page of pair gl
                 int page = 0, ok = 0;
-                if (jl < je) {
+                if (gl < ng && jl < je) {
                     page = p.block_table[static_cast<int64_t>(c.b) * p.bt_stride + jl];
                     ok = (page >= 0 && page < p.num_pages) ? 1 : 0;
                     if (!ok)
                         atomicOr(p.fault, MSA_FAULT_PAGE_ID);
                 }
-                const int cnt = min(32, je - jb);
+                const int cnt = min(32, ng - gb);
                 for (int i = 0; i < cnt; ++i) {
                     const int pg = __shfl_sync(0xffffffffu, page, i);
                     const int pok = __shfl_sync(0xffffffffu, ok, i);
                     int good = 1;
                     if (lane == 0) {
-                        const int s = static_cast<int>(kc % kTcStages);
+                        const int s = static_cast<int>(gc % kP2Stages);
                         const uint32_t full = smem_addr(&ctl->k_full[s]);
                         if (aborted(ctl) ||
-                            (kc >= kTcStages &&
-                             !mbar_wait(smem_addr(&ctl->k_empty[s]), ((kc / kTcStages) - 1) & 1u))) {
+                            (gc >= kP2Stages &&
+                             !mbar_wait(smem_addr(&ctl->k_empty[s]), ((gc / kP2Stages) - 1) & 1u))) {
                             give_up(p, ctl);
                             good = 0;
                         } else if (pok) {
@@ -481,14 +473,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
                             tma_load_2d(dst, &p.kmap, 0, pg * kPage, full);
                             tma_load_2d(dst + kHalfPageBytes, &p.kmap, 64, pg * kPage, full);
                         } else {
-                            mbar_arrive(full);  // nothing to load; the epilogue writes -inf
+                            mbar_arrive(full);  // no page here (odd tail or bad id): nothing to load
                         }
                     }
                     if (__shfl_sync(0xffffffffu, good, 0) == 0) {
                         ok_run = false;
                         break;
                     }
-                    ++kc;
+                    ++gc;
                 }
             }
             ++seg;
@@ -497,87 +489,155 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
                 break;
         }
         if (lane == 0) {  // drain: no copy may land after the CTA exits
-            for (uint32_t i = kc > kTcStages ? kc - kTcStages : 0; i < kc; ++i)
-                if (!mbar_wait(smem_addr(&ctl->k_full[i % kTcStages]), (i / kTcStages) & 1u))
+            for (uint32_t i = gc > kP2Stages ? gc - kP2Stages : 0; i < gc; ++i)
+                if (!mbar_wait(smem_addr(&ctl->k_full[i % kP2Stages]), (i / kP2Stages) & 1u))
                     give_up(p, ctl);
             if (seg > 0 && !mbar_wait(smem_addr(&ctl->q_full), (seg - 1) & 1u))
                 give_up(p, ctl);
         }
     } else if (warp == 1) {
-        // ---------------- MMA issue (one thread) ----------------
         if (lane == 0) {
             Cursor c;
             c.load(p, sb, st, sj, eb, et, ej);
             long long left = units;
-            uint32_t kc = 0, ac = 0, seg = 0;
+            uint32_t gc = 0, seg = 0;
             bool ok_run = true;
-            while (left > 0 && ok_run) {
-                const int je = c.je;
-                if (!mbar_wait(smem_addr(&ctl->q_full), seg & 1u)) {
-                    give_up(p, ctl);
-                    break;
+            if (rank == 0) {
+                // ---------------- MMA issue for the pair ----------------
+                while (left > 0 && ok_run) {
+                    const int je = c.je;
+                    if (!mbar_wait(smem_addr(&ctl->q_full), seg & 1u) ||
+                        !mbar_wait(smem_addr(&ctl->q_peer), seg & 1u)) {
+                        give_up(p, ctl);
+                        break;
+                    }
+                    const int ng = pairs_of(c.j, je);
+                    for (int g = 0; g < ng; ++g) {
+                        const int s = static_cast<int>(gc % kP2Stages);
+                        const int a = static_cast<int>(gc % kP2AccBufs);
+                        if (!wait_ready(ctl, gc + 1)) {
+                            give_up(p, ctl);
+                            ok_run = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t a_lo = umma_desc_lo(q_smem);
+                        const uint32_t b_lo = umma_desc_lo(k_smem + s * kPageBytes);
+                        const uint32_t d = tmem + static_cast<uint32_t>(a * 2 * kPage);
+#pragma unroll
+                        for (int ks = 0; ks < kDim / 16; ++ks) {
+                            const uint32_t qo = ((ks >> 2) * kP2QHalf + (ks & 3) * 32) >> 4;
+                            const uint32_t ko = ((ks >> 2) * kHalfPageBytes + (ks & 3) * 32) >> 4;
+                            if (ks == 0)
+                                umma_pair_f16<false>(d, a_lo + qo, b_lo + ko, kP2Idesc);
+                            else
+                                umma_pair_f16<true>(d, a_lo + qo, b_lo + ko, kP2Idesc);
+                        }
+                        umma_commit_pair(smem_addr(&ctl->k_empty[s]));
+                        umma_commit_pair(smem_addr(&ctl->acc_full[a]));
+                        ++gc;
+                    }
+                    umma_commit_pair(smem_addr(&ctl->q_empty));
+                    ++seg;
+                    left -= je - c.j;
+                    if (left > 0 && !c.next(p))
+                        break;
                 }
-                tc_fence_after_sync();
-                // M tiles holding at least one of the tile's new tokens
-                const int live_tokens = min(kTileTokens, c.r.n - kTileTokens * c.t);
-                const int live_mtiles = (live_tokens * kHeads + kMRows - 1) / kMRows;
-                ok_run = live_mtiles == kMTiles
-                             ? mma_pages<kMTiles>(p, ctl, tmem, q_smem, k_smem, c.j, je, kc, ac)
-                             : mma_pages<1>(p, ctl, tmem, q_smem, k_smem, c.j, je, kc, ac);
-                umma_commit(smem_addr(&ctl->q_empty));
-                ++seg;
-                left -= je - c.j;
-                if (left > 0 && !c.next(p))
-                    break;
+                // every MMA issued has completed before TMEM is freed or either CTA exits
+                umma_commit_pair(smem_addr(&ctl->mma_done));
+            } else {
+                // ---------------- odd CTA: its query rows and pages have landed ----------------
+                const uint32_t q_peer = mapa_shared(smem_addr(&ctl->q_peer), 0);
+                while (left > 0 && ok_run) {
+                    const int je = c.je;
+                    if (!mbar_wait(smem_addr(&ctl->q_full), seg & 1u)) {
+                        give_up(p, ctl);
+                        break;
+                    }
+                    mbar_arrive_cluster(q_peer);
+                    const int ng = pairs_of(c.j, je);
+                    for (int g = 0; g < ng; ++g) {
+                        const int s = static_cast<int>(gc % kP2Stages);
+                        if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->k_full[s]), (gc / kP2Stages) & 1u)) {
+                            give_up(p, ctl);
+                            ok_run = false;
+                            break;
+                        }
+                        mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->k_peer[s]), 0));
+                        ++gc;
+                    }
+                    ++seg;
+                    left -= je - c.j;
+                    if (left > 0 && !c.next(p))
+                        break;
+                }
             }
-            // every MMA issued has completed before TMEM is freed
-            umma_commit(smem_addr(&ctl->mma_done));
             if (!mbar_wait(smem_addr(&ctl->mma_done), 0))
                 give_up(p, ctl);
         }
         __syncwarp();
-    } else if (warp == kWaiterWarp) {
-        // ---------------- waiter: page kc may be multiplied ----------------
-        // (pages are issued in order; page kc uses stage kc mod S and
-        // accumulator buffer kc mod A)
-        if (lane == 0) {
+    } else if (warp == kP2WaiterWarp) {
+        // ---------------- even CTA: pair gc may be multiplied ----------------
+        if (rank == 0 && lane == 0) {
             const uint32_t addr = smem_addr(&ctl->ready);
-            for (uint32_t kc = 0; kc < static_cast<uint32_t>(units); ++kc) {
-                const int s = static_cast<int>(kc % kTcStages);
-                const int a = static_cast<int>(kc % kAccBufs);
-                if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->k_full[s]), (kc / kTcStages) & 1u) ||
-                    (kc >= kAccBufs && !mbar_wait(smem_addr(&ctl->acc_empty[a]), ((kc / kAccBufs) - 1) & 1u))) {
-                    give_up(p, ctl);
-                    break;
+            Cursor c;
+            c.load(p, sb, st, sj, eb, et, ej);
+            long long left = units;
+            uint32_t gc = 0;
+            bool ok_run = true;
+            while (left > 0 && ok_run) {
+                const int je = c.je;
+                const int ng = pairs_of(c.j, je);
+                for (int g = 0; g < ng; ++g) {
+                    const int s = static_cast<int>(gc % kP2Stages);
+                    const int a = static_cast<int>(gc % kP2AccBufs);
+                    if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->k_full[s]), (gc / kP2Stages) & 1u) ||
+                        !mbar_wait(smem_addr(&ctl->k_peer[s]), (gc / kP2Stages) & 1u) ||
+                        (gc >= kP2AccBufs &&
+                         !mbar_wait(smem_addr(&ctl->acc_empty[a]), ((gc / kP2AccBufs) - 1) & 1u))) {
+                        give_up(p, ctl);
+                        ok_run = false;
+                        break;
+                    }
+                    st_release_shared_u32(addr, gc + 1);
+                    ++gc;
                 }
-                st_release_shared_u32(addr, kc + 1);
+                left -= je - c.j;
+                if (left > 0 && !c.next(p))
+                    break;
             }
         }
         __syncwarp();
     } else {
         // ---------------- epilogue: TMEM -> block scores ----------------
-        const int e = warp - 2;
-        const int quarter = warp & 3;        // TMEM lanes this warp may read
-        const int mt = e >> 2;               // M tile of this warp
-        const int row_in_tile = mt * kMRows + 32 * quarter + lane;  // 0..255
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16) +
-                                   static_cast<uint32_t>(mt * kPage);
+        const int h = (warp - 2) >> 2;  // 0: the pair's first page, 1: its second
+        const int quarter = warp & 3;
+        const int row_in_tile = kMRows * static_cast<int>(rank) + 32 * quarter + lane;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(h * kPage);
         const float neg_inf = -__int_as_float(0x7f800000);
         Cursor c;
         c.load(p, sb, st, sj, eb, et, ej);
         long long left = units;
-        uint32_t ac = 0;
+        uint32_t gc = 0;
         bool ok_run = true;
         while (left > 0 && ok_run) {
             const int je = c.je;
-            const int tl = kTileTokens * c.t + (row_in_tile >> 2);  // token within the request's new ones
+            const int tl = kTileTokens * c.t + (row_in_tile >> 2);
             const int head = row_in_tile & 3;
             const bool live = tl < c.r.n;
             const int pos = c.r.len - c.r.n + tl;
             float *out = p.scores + (static_cast<int64_t>(c.r.c0 + tl) * kHeads + head) * p.bs_stride;
-            for (int j = c.j; j < je; ++j) {
-                const int a = static_cast<int>(ac % kAccBufs);
-                bool ready = !aborted(ctl) && mbar_wait(smem_addr(&ctl->acc_full[a]), (ac / kAccBufs) & 1u);
+            const int32_t *bt_row = p.block_table + static_cast<int64_t>(c.b) * p.bt_stride;
+            const int ng = pairs_of(c.j, je);
+            // this warp's page of each pair, its block-table entry read a pair ahead
+            int page_next = c.j + h < je ? bt_row[c.j + h] : 0;
+            for (int g = 0; g < ng; ++g, ++gc) {
+                const int a = static_cast<int>(gc % kP2AccBufs);
+                const int j = c.j + 2 * g + h;
+                const int page = page_next;
+                if (j + 2 < je)
+                    page_next = bt_row[j + 2];
+                bool ready = !aborted(ctl) && mbar_wait(smem_addr(&ctl->acc_full[a]), (gc / kP2AccBufs) & 1u);
                 ready = __all_sync(0xffffffffu, ready);
                 if (!ready) {
                     if (lane == 0)
@@ -586,38 +646,50 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
                     break;
                 }
                 tc_fence_after_sync();
-                const int page = p.block_table[static_cast<int64_t>(c.b) * p.bt_stride + j];
                 const bool page_ok = page >= 0 && page < p.num_pages;
                 const int first_key = j * kPage;
-                const bool want = live && first_key <= pos;
-                if (page_ok && __any_sync(0xffffffffu, want)) {
-                    float mx = neg_inf;
-#pragma unroll
-                    for (int q4 = 0; q4 < kPage / 32; ++q4) {
-                        uint32_t r[32];
-                        tmem_ld32(lane_addr + static_cast<uint32_t>(a * kMTiles * kPage + 32 * q4), r);
-                        tmem_wait_ld(r);
-                        const int lim = pos - (first_key + 32 * q4);  // keys i <= lim are visible
-                        if (lim >= 31) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                mx = fmaxf(mx, __uint_as_float(r[i]));
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                mx = fmaxf(mx, i <= lim ? __uint_as_float(r[i]) : neg_inf);
-                        }
-                    }
-                    if (want)
-                        out[j] = mx;
-                } else if (!page_ok && want) {
-                    out[j] = neg_inf;
+                const bool want = j < je && live && first_key <= pos;
+                const bool math = j < je && page_ok && __any_sync(0xffffffffu, want);
+                // all 128 columns into registers, the buffer handed back at once,
+                // then the masked max
+                uint32_t r0[32], r1[32], r2[32], r3[32];
+                if (math) {
+                    const uint32_t col = lane_addr + static_cast<uint32_t>(a * 2 * kPage);
+                    tmem_ld32(col, r0);
+                    tmem_ld32(col + 32, r1);
+                    tmem_ld32(col + 64, r2);
+                    tmem_ld32(col + 96, r3);
+                    tmem_wait_ld(r0);
+                    tmem_regs_ready(r1);
+                    tmem_regs_ready(r2);
+                    tmem_regs_ready(r3);
                 }
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(smem_addr(&ctl->acc_empty[a]));
-                ++ac;
+                    mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->acc_empty[a]), 0));
+                if (math) {
+                    const int lim = pos - first_key;  // keys i <= lim of the page are visible
+                    float mx = neg_inf;
+                    if (lim >= kPage - 1) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            mx = fmaxf(fmaxf(mx, __uint_as_float(r0[i])),
+                                       fmaxf(__uint_as_float(r1[i]), fmaxf(__uint_as_float(r2[i]), __uint_as_float(r3[i]))));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            mx = fmaxf(mx, i <= lim ? __uint_as_float(r0[i]) : neg_inf);
+                            mx = fmaxf(mx, i + 32 <= lim ? __uint_as_float(r1[i]) : neg_inf);
+                            mx = fmaxf(mx, i + 64 <= lim ? __uint_as_float(r2[i]) : neg_inf);
+                            mx = fmaxf(mx, i + 96 <= lim ? __uint_as_float(r3[i]) : neg_inf);
+                        }
+                    }
+                    if (want)
+                        out[j] = mx;
+                } else if (j < je && !page_ok && want) {
+                    out[j] = neg_inf;
+                }
             }
             left -= je - c.j;
             if (left > 0 && !c.next(p))
@@ -625,11 +697,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_score_kernel(const _
         }
     }
 
+    // all of both CTAs' work is done (the issuing thread has seen its last MMA
+    // complete) before either frees TMEM or exits
     tc_fence_before_sync();
-    __syncthreads();
+    __syncwarp();
+    cluster_sync_all();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc_pair(tmem, kP2TmemCols);
     }
 }
 
@@ -670,6 +745,37 @@ static bool make_rows_map(CUtensorMap *map, const void *base, int64_t rows)
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Clusters of two the pair kernel runs: one per two SMs, fewer if the GPU
+// cannot hold that many at once (queried once per device).
+static int pair_clusters(int dev, int sms)
+{
+    static std::atomic<int> cache[kMaxDevices];
+    int v = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (v > 0)
+        return v;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(sms / 2 * 2));
+    cfg.blockDim = dim3(kP2Threads);
+    cfg.dynamicSmemBytes = kP2SmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_prefill_pair_kernel, &cfg) != cudaSuccess || n <= 0)
+        n = sms / 2;
+    v = n < sms / 2 ? n : sms / 2;
+    if (v < 1)
+        v = 1;
+    if (dev >= 0 && dev < kMaxDevices)
+        cache[dev].store(v, std::memory_order_relaxed);
+    return v;
 }
 
 }  // namespace msa
@@ -739,8 +845,8 @@ static msa_status prefill_score_launch(const void *q, const int32_t *cu_seqlens_
         const cudaError_t e =
             fp8 ? cudaFuncSetAttribute(tc_prefill_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kF8SmemBytes))
-                : cudaFuncSetAttribute(tc_prefill_score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kTcSmemBytes));
+                : cudaFuncSetAttribute(tc_prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kP2SmemBytes));
         if (e != cudaSuccess)
             return MSA_ERR_CUDA;
         attr_done[fp8][dev].store(true, std::memory_order_release);
@@ -749,13 +855,29 @@ static msa_status prefill_score_launch(const void *q, const int32_t *cu_seqlens_
                           : make_rows_map(&p.kmap, kcache_pool, num_pages * kPage);
     if (!maps || !make_rows_map(&p.qmap, q, static_cast<int64_t>(total_q) * kHeads))
         return MSA_ERR_CUDA;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(sms)),
-                                        dim3(fp8 ? kF8Threads : kTcThreads),
-                                        fp8 ? kF8SmemBytes : kTcSmemBytes, st, attr);
-    const cudaError_t e = fp8 ? cudaLaunchKernelEx(&cfg, tc_prefill_fp8_kernel, p)
-                              : cudaLaunchKernelEx(&cfg, tc_prefill_score_kernel, p);
-    return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+    if (fp8) {
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(sms)), dim3(kF8Threads), kF8SmemBytes, st,
+                                            attr);
+        return cudaLaunchKernelEx(&cfg, tc_prefill_fp8_kernel, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+    }
+    // clusters of two CTAs, with programmatic dependent launch
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pair_clusters(dev, sms)));
+    cfg.blockDim = dim3(kP2Threads);
+    cfg.dynamicSmemBytes = kP2SmemBytes;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, tc_prefill_pair_kernel, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 extern "C" msa_status msa_indexer_prefill_score(const void *q, const int32_t *cu_seqlens_q,

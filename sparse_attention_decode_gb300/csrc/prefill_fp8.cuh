@@ -192,7 +192,7 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
     griddep_wait();
     griddep_launch_dependents();
     if (warp == 0)
-        plan_range(p, ctl, lane);
+        plan_range(p, ctl, lane, gridDim.x, blockIdx.x);
     __syncthreads();
     const long long units = ctl->units;
     if (units <= 0)

@@ -2,10 +2,12 @@
 // sm_100a / sm_103a: tensor-memory (TMEM) allocation, shared-memory matrix
 // descriptors, MMA issue and completion, and TMEM loads.
 //
-// Conventions used by the kernels here: one CTA per SM (cta_group::1), A and
-// B both bf16 and K-major in shared memory in the 128-byte swizzle layout that
-// a TMA load with CU_TENSOR_MAP_SWIZZLE_128B produces (rows of 128 B, atoms of
-// 8 rows = 1024 B, every operand tile 1024-byte aligned), D in fp32 in TMEM.
+// Conventions used by the kernels here: A and B of one type (bf16, or f16 on
+// the E4M3 cache) and K-major in shared memory in the 128-byte swizzle layout
+// that a TMA load with CU_TENSOR_MAP_SWIZZLE_128B produces (rows of 128 B,
+// atoms of 8 rows = 1024 B, every operand tile 1024-byte aligned), D in fp32
+// in TMEM.  The E4M3 kernel runs one CTA per SM (cta_group::1); the bf16
+// kernel runs pairs of CTAs (cta_group::2, the wrappers at the end).
 #pragma once
 
 #include <cstdint>
@@ -161,6 +163,19 @@ __device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[16])
                    "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 
+// Marks r as written here (32 registers): placed after a tmem_wait_ld that
+// also covered r's load, it keeps r's uses after that wait.
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32])
+{
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31]));
+}
+
 // Waits for this thread's TMEM loads; the registers pass through the asm so
 // that no use of them can be scheduled before the wait.
 __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32])
@@ -174,6 +189,92 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32])
                    "+r"(r[30]), "+r"(r[31])
                  :
                  : "memory");
+}
+
+
+// ---- pairs of CTAs (a cluster of two, cta_group::2) ----
+// With cta_group::2 the two CTAs of a cluster act as one MMA unit: one thread
+// of the even CTA issues an M = 256 MMA whose A rows 0-127 come from the even
+// CTA's shared memory and rows 128-255 from the odd CTA's (the same offset in
+// both), whose B rows (the N keys) come half from each CTA (keys 0 .. N/2-1
+// from the even CTA, N/2 .. N-1 from the odd one, again the same offset), and
+// whose accumulator rows land in each CTA's own TMEM (rows 0-127 in the even
+// CTA's lanes, 128-255 in the odd CTA's, the same columns).  Allocation and
+// release are collective: one warp of each CTA executes them.  (Checked on
+// GB300 with a known-answer product before use: both CTAs receive the same
+// TMEM address, and B's rows split between the CTAs as stated.)
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of the variable at local shared address `addr`
+// in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Arrives on an mbarrier of another CTA of the cluster (default semantics:
+// release at CTA scope; with .release.cluster here and acquire.cluster on the
+// waiting side the pair kernel ran 1.36x slower).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Every thread of both CTAs: all writes before it are visible to all after it.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A * B^T over the pair (kind::f16, cta_group::2), issued by one
+// thread of the even CTA.
+template <bool ACC>
+__device__ __forceinline__ void umma_pair_f16(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc)
+{
+    asm volatile(
+        "{\n"
+        "  .reg .b64 ad, bd;\n"
+        "  mov.b64 ad, {%1, %5};\n"
+        "  mov.b64 bd, {%2, %5};\n"
+        "  tcgen05.mma.cta_group::2.kind::f16 [%0], ad, bd, %3, %4;\n"
+        "}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "n"(ACC ? 1 : 0), "r"(kUmmaDescHi)
+        : "memory");
+}
+
+// Arrives once on the mbarrier at local offset `bar` in both CTAs of the pair
+// when every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(static_cast<uint16_t>(0x3))
+        : "memory");
 }
 
 }  // namespace msa

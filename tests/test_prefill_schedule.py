@@ -1,4 +1,4 @@
-"""CPU replay of the prefill kernel's work split.
+"""CPU replay of the prefill kernels' work split.
 
 The tensor-core prefill kernel cuts the batch's (tile of 64 new tokens, page)
 units into one equal range per CTA, using a closed form for the pages that
@@ -8,6 +8,10 @@ that the CTAs scoring one request's tiles read its pages nearly together.
 This replays that arithmetic (restated from the kernel) and checks that the
 ranges of any grid cover every unit exactly once, and that on a long chunked
 prefill the pages in flight form at most two compact fronts per request.
+The bf16 kernel runs on pairs of CTAs (one range per pair) and multiplies a
+segment's pages two at a time: pair g of a segment [j, je) is pages j + 2 g
+(the even CTA's) and j + 2 g + 1 (the odd CTA's, absent past je); that
+grouping is replayed too.
 """
 
 import numpy as np
@@ -138,7 +142,7 @@ def test_ranges_cover_every_unit_once(seed):
     for _ in range(60):
         reqs = _random_batch(rng)
         expect = all_units(reqs)
-        for G in (1, 2, 7, 148, 152, 1000):
+        for G in (1, 2, 7, 76, 148, 152, 1000):
             got = []
             for g in range(G):
                 start = plan(reqs, G, g)
@@ -211,3 +215,68 @@ def test_long_prefill_reads_pages_on_two_fronts():
         fwd.append(seq)
     spread = max(fronts([w[0][1] for w in fwd if w[0][0] == b]) for b in range(4))
     assert spread > 8
+
+
+def pairs_of(j, je):
+    return (je - j + 1) // 2
+
+
+def pair_walk(reqs, start):
+    """The pair kernel's order: the cursor's segments, each cut into pairs of
+    pages; per pair (even CTA's page, odd CTA's page or None)."""
+    seq = walk(reqs, start)
+    segs = []
+    for b, t, x in seq:
+        if segs and segs[-1][0] == (b, t) and segs[-1][1][-1] == x - 1:
+            segs[-1][1].append(x)
+        else:
+            segs.append(((b, t), [x]))
+    out = []
+    for (b, t), pages in segs:
+        j, je = pages[0], pages[-1] + 1
+        for g in range(pairs_of(j, je)):
+            first = j + 2 * g
+            second = first + 1 if first + 1 < je else None
+            out.append((b, t, first, second))
+    return out
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_pairs_cover_every_page_once(seed):
+    """Every unit of a pair's range is the even or the odd CTA's page of
+    exactly one pair; only a segment's last pair can lack its second page;
+    stage (pair mod 6) and accumulator buffer (pair mod 2) follow the pairs."""
+    rng = np.random.default_rng(500 + seed)
+    for _ in range(40):
+        reqs = _random_batch(rng)
+        expect = all_units(reqs)
+        for G in (1, 3, 76):
+            got = []
+            for g in range(G):
+                start = plan(reqs, G, g)
+                if start is None:
+                    continue
+                pairs = pair_walk(reqs, start)
+                units = start[2]
+                segments = len({(b, t) for b, t, _, _ in pairs})
+                assert (units + 1) // 2 <= len(pairs) <= (units + segments) // 2 + segments
+                for i, (b, t, first, second) in enumerate(pairs):
+                    got.append((b, t, first))
+                    if second is not None:
+                        got.append((b, t, second))
+                    else:  # a missing second page ends its segment
+                        assert i + 1 == len(pairs) or pairs[i + 1][:2] != (b, t)
+            assert sorted(got) == expect, (reqs, G)
+
+
+def test_pair_counts_on_the_chunked_prefill():
+    """4 x 2048 new tokens at 128K on 76 pairs: ~878 pairs of pages per pair
+    of CTAs, at most a few half-empty ones."""
+    reqs = [(2048, 131072, True)] * 4
+    counts, halves = [], 0
+    for g in range(76):
+        pairs = pair_walk(reqs, plan(reqs, 76, g))
+        counts.append(len(pairs))
+        halves += sum(1 for p in pairs if p[3] is None)
+    assert max(counts) - min(counts) <= 2
+    assert halves <= 2 * 76
