@@ -223,11 +223,17 @@ __device__ __forceinline__ void locate_unit(const TcParams &p, long long u, int 
     uj = static_cast<int>(rel - pages_before(r, lo));
 }
 
-// This CTA's range of work units: [W*g/G, W*(g+1)/G) of the batch's
-// (tile, page) units in order.  Run by one warp; writes its first and last
-// positions and its unit count.
-template <class Ctl>
-__device__ void plan_range(const TcParams &p, Ctl *ctl, int lane, long long G, long long g)
+// A range of work units: its first (tile, page) unit, its last + 1 page, and
+// its unit count.
+struct UnitRange {
+    int b0, t0, j0;
+    int b1, t1, j1;
+    long long units;
+};
+
+// The batch's (tile, page) unit count W.  Run by one warp (every lane gets
+// it); the first CTA flags the requests the kernels refuse.
+__device__ long long batch_units(const TcParams &p, int lane)
 {
     long long W = 0;
     for (int b0 = 0; b0 < p.batch; b0 += 32) {
@@ -240,6 +246,15 @@ __device__ void plan_range(const TcParams &p, Ctl *ctl, int lane, long long G, l
         }
         W += warp_sum64(v);
     }
+    return W;
+}
+
+// Range g of the batch's W units, in order, cut G ways: [W*g/G, W*(g+1)/G).
+// Run by one warp; writes the range's first and last positions and its unit
+// count into *ctl (a UnitRange, or a control block with the same fields).
+template <class Ctl>
+__device__ void plan_range_of(const TcParams &p, Ctl *ctl, int lane, long long W, long long G, long long g)
+{
     const long long u0 = W * g / G, u1 = W * (g + 1) / G;
     if (u1 <= u0) {
         if (lane == 0)
@@ -258,6 +273,12 @@ __device__ void plan_range(const TcParams &p, Ctl *ctl, int lane, long long G, l
         ctl->j1 = j1 + 1;
         ctl->units = u1 - u0;
     }
+}
+
+template <class Ctl>
+__device__ void plan_range(const TcParams &p, Ctl *ctl, int lane, long long G, long long g)
+{
+    plan_range_of(p, ctl, lane, batch_units(p, lane), G, g);
 }
 
 template <class Ctl>
@@ -322,8 +343,8 @@ __device__ __forceinline__ bool wait_ready(Ctl *ctl, uint32_t need)
 // against 1024); here it issues a pair's 8 MMAs in ~700 cycles against 1024.
 // Each SM still reads one page from L2 or DRAM per 256 rows multiplied.
 // Per CTA:
-//   warp 0     TMA producer: its 128 query rows at each tile, its page of
-//              each pair through a 6-stage ring;
+//   warp 0     TMA producer: its 128 query rows at each tile (two tiles'
+//              rows resident), its page of each pair through a 5-stage ring;
 //   warp 1     TMEM allocation (both CTAs, collectively); even CTA: one
 //              thread issues the MMAs; odd CTA: one thread tells the even CTA
 //              that its query rows and each of its pages have landed;
@@ -337,7 +358,9 @@ __device__ __forceinline__ bool wait_ready(Ctl *ctl, uint32_t need)
 //              may multiply.
 // Every wait is bounded; a CTA that gives up still meets its partner at the
 // final cluster barrier, after which TMEM is freed.
-constexpr int kP2Stages = 6;
+constexpr int kP2Stages = 5;
+constexpr int kP2QBufs = 2;  // a tile's query rows load while the previous tile is multiplied
+constexpr long long kP2SplitUnits = 512;  // units a half-range needs for the two-range walk
 constexpr int kP2AccBufs = 2;
 constexpr uint32_t kP2TmemCols = kP2AccBufs * 2 * kPage;  // 512
 constexpr uint32_t kP2QBytes = kMRows * kDim * 2;          // 32 KiB: 128 query rows
@@ -352,24 +375,78 @@ struct P2Smem {
     uint64_t k_full[kP2Stages];
     uint64_t k_peer[kP2Stages];  // even CTA: the odd CTA's page of the stage has landed
     uint64_t k_empty[kP2Stages];
-    uint64_t q_full;
-    uint64_t q_peer;             // even CTA: the odd CTA's query rows have landed
-    uint64_t q_empty;
+    uint64_t q_full[kP2QBufs];
+    uint64_t q_peer[kP2QBufs];   // even CTA: the odd CTA's query rows have landed
+    uint64_t q_empty[kP2QBufs];
     uint64_t acc_full[kP2AccBufs];
     uint64_t acc_empty[kP2AccBufs];  // even CTA: both CTAs' epilogue warps
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t ready;  // even CTA: pairs of pages the issuing thread may multiply
     int abort;
-    int b0, t0, j0;
-    int b1, t1, j1;
-    long long units;
+    UnitRange rng[2];  // the pair's two ranges of units, walked one after the other
 };
 
-constexpr size_t kP2SmemBytes = 1024 + kP2QBytes + static_cast<size_t>(kP2Stages) * kPageBytes + sizeof(P2Smem);
+constexpr size_t kP2SmemBytes = 1024 + kP2QBufs * kP2QBytes + static_cast<size_t>(kP2Stages) * kPageBytes + sizeof(P2Smem);
 static_assert(kP2SmemBytes <= 227 * 1024, "shared memory per CTA");
 
 __device__ __forceinline__ int pairs_of(int j, int je) { return (je - j + 1) / 2; }
+
+// The segments of a pair's two ranges in walking order: each range from its
+// last tile back to its first, pages in order within a tile (as Cursor walks
+// one range); every role of the kernel walks the same ones.  The current
+// range's first unit stays in shared memory, which keeps the epilogue (a
+// row's 128 accumulators in registers) within its register budget.
+struct SegWalk {
+    int b, t, j, je;  // segment: pages [j, je) of tile t of request b
+    Req r;
+    long long left;   // units of the current range from this segment on
+    int k;            // the current range
+
+    __device__ __forceinline__ bool next_range(const TcParams &p, const UnitRange *rng)
+    {
+        while (++k < 2) {
+            const UnitRange &R = rng[k];
+            if (R.units > 0) {
+                b = R.b1;
+                t = R.t1;
+                r = req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, b);
+                je = R.j1;
+                j = (b == R.b0 && t == R.t0) ? R.j0 : 0;
+                left = R.units;
+                return true;
+            }
+        }
+        return false;
+    }
+    __device__ __forceinline__ bool start(const TcParams &p, const UnitRange *rng)
+    {
+        k = -1;
+        return next_range(p, rng);
+    }
+    // After the current segment: the next one; false when both ranges are done.
+    __device__ __forceinline__ bool next(const TcParams &p, const UnitRange *rng)
+    {
+        left -= je - j;
+        if (left <= 0)
+            return next_range(p, rng);
+        const UnitRange &R = rng[k];
+        if (b == R.b0 && t == R.t0)
+            return false;  // past the range's first tile (not reached: left counts its units)
+        if (t > 0) {
+            --t;
+        } else {
+            do {
+                --b;
+                r = req_info(p.cu_q, p.seq_lens, p.total_q, p.seq_limit, b);
+            } while (b > R.b0 && !(r.ok && r.n > 0));
+            t = tiles_of(r) - 1;
+        }
+        je = tile_pages(r, t);
+        j = (b == R.b0 && t == R.t0) ? R.j0 : 0;
+        return true;
+    }
+};
 
 __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __grid_constant__ TcParams p)
 {
@@ -377,8 +454,8 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     const uint32_t q_smem = smem_addr(smem);
-    const uint32_t k_smem = q_smem + kP2QBytes;
-    P2Smem *ctl = reinterpret_cast<P2Smem *>(smem + kP2QBytes + kP2Stages * kPageBytes);
+    const uint32_t k_smem = q_smem + kP2QBufs * kP2QBytes;
+    P2Smem *ctl = reinterpret_cast<P2Smem *>(smem + kP2QBufs * kP2QBytes + kP2Stages * kPageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();  // 0: the CTA that issues the MMAs
 
@@ -388,9 +465,11 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
             mbar_init(smem_addr(&ctl->k_peer[s]), 1);
             mbar_init(smem_addr(&ctl->k_empty[s]), 1);
         }
-        mbar_init(smem_addr(&ctl->q_full), 1);
-        mbar_init(smem_addr(&ctl->q_peer), 1);
-        mbar_init(smem_addr(&ctl->q_empty), 1);
+        for (int b = 0; b < kP2QBufs; ++b) {
+            mbar_init(smem_addr(&ctl->q_full[b]), 1);
+            mbar_init(smem_addr(&ctl->q_peer[b]), 1);
+            mbar_init(smem_addr(&ctl->q_empty[b]), 1);
+        }
         for (int a = 0; a < kP2AccBufs; ++a) {
             mbar_init(smem_addr(&ctl->acc_full[a]), 1);
             mbar_init(smem_addr(&ctl->acc_empty[a]), 2 * kP2EpiWarps);
@@ -402,13 +481,31 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
     }
     griddep_wait();
     griddep_launch_dependents();
-    if (warp == 0)
-        plan_range(p, ctl, lane, gridDim.x / 2, blockIdx.x / 2);
+    // On a large batch pair g of G takes ranges g and g + G of the units cut
+    // 2G ways.  The first ranges of all pairs cover the first half of the
+    // batch's units and the second ranges the rest, so at any time the pairs
+    // stream each request's pages on the few fronts a single-CTA split has: a
+    // pair walking one range of twice the length restarts at page 0
+    // mid-range, and on the chunked prefill of 4 x 2048 tokens at 128K each
+    // page then left DRAM ~5.6 times instead of about once.  A smaller batch
+    // (fewer than kP2SplitUnits units a half-range) takes range g of G: there
+    // the extra segments of the two-range walk cost more than L2 reuse gives.
+    if (warp == 0) {
+        const long long W = batch_units(p, lane);
+        const long long G = gridDim.x / 2, g = blockIdx.x / 2;
+        if (W >= 2 * G * kP2SplitUnits) {
+            plan_range_of(p, &ctl->rng[0], lane, W, 2 * G, g);
+            plan_range_of(p, &ctl->rng[1], lane, W, 2 * G, g + G);
+        } else {
+            plan_range_of(p, &ctl->rng[0], lane, W, G, g);
+            if (lane == 0)
+                ctl->rng[1].units = 0;
+        }
+    }
     __syncwarp();
     // both CTAs' barriers are initialised before either arrives on the other's
     cluster_sync_all();
-    const long long units = ctl->units;
-    if (units <= 0)
+    if (ctl->rng[0].units + ctl->rng[1].units <= 0)
         return;  // the same for both CTAs of the pair: no TMEM taken yet
     if (warp == 1) {
         tmem_alloc_pair(smem_addr(&ctl->tmem_base), kP2TmemCols);
@@ -418,28 +515,29 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
-    const int sb = ctl->b0, st = ctl->t0, sj = ctl->j0;
-    const int eb = ctl->b1, et = ctl->t1, ej = ctl->j1;
 
     if (warp == 0) {
         // ---------------- producer (both CTAs) ----------------
-        Cursor c;
-        c.load(p, sb, st, sj, eb, et, ej);
-        long long left = units;
+        SegWalk w;
+        bool more = w.start(p, ctl->rng);
+        const SegWalk &c = w;
         uint32_t gc = 0, seg = 0;
         bool ok_run = true;
-        while (left > 0 && ok_run) {
+        while (more && ok_run) {
             const int je = c.je;
             if (lane == 0) {
-                if (seg > 0 && !mbar_wait(smem_addr(&ctl->q_empty), (seg - 1) & 1u)) {
+                const int qb = static_cast<int>(seg % kP2QBufs);
+                if (seg >= kP2QBufs &&
+                    !mbar_wait(smem_addr(&ctl->q_empty[qb]), ((seg / kP2QBufs) - 1) & 1u)) {
                     give_up(p, ctl);
                     ok_run = false;
                 } else {
-                    const uint32_t qf = smem_addr(&ctl->q_full);
+                    const uint32_t qf = smem_addr(&ctl->q_full[qb]);
+                    const uint32_t qdst = q_smem + static_cast<uint32_t>(qb) * kP2QBytes;
                     const int row0 = (c.r.c0 + kTileTokens * c.t) * kHeads + kMRows * static_cast<int>(rank);
                     mbar_arrive_expect_tx(qf, kP2QBytes);
-                    tma_load_2d(q_smem, &p.qmap, 0, row0, qf);
-                    tma_load_2d(q_smem + kP2QHalf, &p.qmap, 64, row0, qf);
+                    tma_load_2d(qdst, &p.qmap, 0, row0, qf);
+                    tma_load_2d(qdst + kP2QHalf, &p.qmap, 64, row0, qf);
                 }
             }
             ok_run = __shfl_sync(0xffffffffu, ok_run ? 1 : 0, 0) != 0;
@@ -484,33 +582,34 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                 }
             }
             ++seg;
-            left -= je - c.j;
-            if (left > 0 && !c.next(p))
-                break;
+            more = w.next(p, ctl->rng);
         }
         if (lane == 0) {  // drain: no copy may land after the CTA exits
             for (uint32_t i = gc > kP2Stages ? gc - kP2Stages : 0; i < gc; ++i)
                 if (!mbar_wait(smem_addr(&ctl->k_full[i % kP2Stages]), (i / kP2Stages) & 1u))
                     give_up(p, ctl);
-            if (seg > 0 && !mbar_wait(smem_addr(&ctl->q_full), (seg - 1) & 1u))
-                give_up(p, ctl);
+            for (uint32_t i = seg > kP2QBufs ? seg - kP2QBufs : 0; i < seg; ++i)
+                if (!mbar_wait(smem_addr(&ctl->q_full[i % kP2QBufs]), (i / kP2QBufs) & 1u))
+                    give_up(p, ctl);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            Cursor c;
-            c.load(p, sb, st, sj, eb, et, ej);
-            long long left = units;
+            SegWalk w;
+            bool more = w.start(p, ctl->rng);
+            const SegWalk &c = w;
             uint32_t gc = 0, seg = 0;
             bool ok_run = true;
             if (rank == 0) {
                 // ---------------- MMA issue for the pair ----------------
-                while (left > 0 && ok_run) {
+                while (more && ok_run) {
                     const int je = c.je;
-                    if (!mbar_wait(smem_addr(&ctl->q_full), seg & 1u) ||
-                        !mbar_wait(smem_addr(&ctl->q_peer), seg & 1u)) {
+                    const int qb = static_cast<int>(seg % kP2QBufs);
+                    const uint32_t qph = (seg / kP2QBufs) & 1u;
+                    if (!mbar_wait(smem_addr(&ctl->q_full[qb]), qph) || !mbar_wait(smem_addr(&ctl->q_peer[qb]), qph)) {
                         give_up(p, ctl);
                         break;
                     }
+                    const uint32_t a_lo = umma_desc_lo(q_smem + static_cast<uint32_t>(qb) * kP2QBytes);
                     const int ng = pairs_of(c.j, je);
                     for (int g = 0; g < ng; ++g) {
                         const int s = static_cast<int>(gc % kP2Stages);
@@ -521,7 +620,6 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                             break;
                         }
                         tc_fence_after_sync();
-                        const uint32_t a_lo = umma_desc_lo(q_smem);
                         const uint32_t b_lo = umma_desc_lo(k_smem + s * kPageBytes);
                         const uint32_t d = tmem + static_cast<uint32_t>(a * 2 * kPage);
 #pragma unroll
@@ -537,24 +635,22 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                         umma_commit_pair(smem_addr(&ctl->acc_full[a]));
                         ++gc;
                     }
-                    umma_commit_pair(smem_addr(&ctl->q_empty));
+                    umma_commit_pair(smem_addr(&ctl->q_empty[qb]));
                     ++seg;
-                    left -= je - c.j;
-                    if (left > 0 && !c.next(p))
-                        break;
+                    more = w.next(p, ctl->rng);
                 }
                 // every MMA issued has completed before TMEM is freed or either CTA exits
                 umma_commit_pair(smem_addr(&ctl->mma_done));
             } else {
                 // ---------------- odd CTA: its query rows and pages have landed ----------------
-                const uint32_t q_peer = mapa_shared(smem_addr(&ctl->q_peer), 0);
-                while (left > 0 && ok_run) {
+                while (more && ok_run) {
                     const int je = c.je;
-                    if (!mbar_wait(smem_addr(&ctl->q_full), seg & 1u)) {
+                    const int qb = static_cast<int>(seg % kP2QBufs);
+                    if (!mbar_wait(smem_addr(&ctl->q_full[qb]), (seg / kP2QBufs) & 1u)) {
                         give_up(p, ctl);
                         break;
                     }
-                    mbar_arrive_cluster(q_peer);
+                    mbar_arrive_cluster(mapa_shared(smem_addr(&ctl->q_peer[qb]), 0));
                     const int ng = pairs_of(c.j, je);
                     for (int g = 0; g < ng; ++g) {
                         const int s = static_cast<int>(gc % kP2Stages);
@@ -567,9 +663,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                         ++gc;
                     }
                     ++seg;
-                    left -= je - c.j;
-                    if (left > 0 && !c.next(p))
-                        break;
+                    more = w.next(p, ctl->rng);
                 }
             }
             if (!mbar_wait(smem_addr(&ctl->mma_done), 0))
@@ -580,12 +674,12 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
         // ---------------- even CTA: pair gc may be multiplied ----------------
         if (rank == 0 && lane == 0) {
             const uint32_t addr = smem_addr(&ctl->ready);
-            Cursor c;
-            c.load(p, sb, st, sj, eb, et, ej);
-            long long left = units;
+            SegWalk w;
+            bool more = w.start(p, ctl->rng);
+            const SegWalk &c = w;
             uint32_t gc = 0;
             bool ok_run = true;
-            while (left > 0 && ok_run) {
+            while (more && ok_run) {
                 const int je = c.je;
                 const int ng = pairs_of(c.j, je);
                 for (int g = 0; g < ng; ++g) {
@@ -602,9 +696,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                     st_release_shared_u32(addr, gc + 1);
                     ++gc;
                 }
-                left -= je - c.j;
-                if (left > 0 && !c.next(p))
-                    break;
+                more = w.next(p, ctl->rng);
             }
         }
         __syncwarp();
@@ -615,12 +707,12 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
         const int row_in_tile = kMRows * static_cast<int>(rank) + 32 * quarter + lane;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + static_cast<uint32_t>(h * kPage);
         const float neg_inf = -__int_as_float(0x7f800000);
-        Cursor c;
-        c.load(p, sb, st, sj, eb, et, ej);
-        long long left = units;
+        SegWalk w;
+        bool more = w.start(p, ctl->rng);
+        const SegWalk &c = w;
         uint32_t gc = 0;
         bool ok_run = true;
-        while (left > 0 && ok_run) {
+        while (more && ok_run) {
             const int je = c.je;
             const int tl = kTileTokens * c.t + (row_in_tile >> 2);
             const int head = row_in_tile & 3;
@@ -691,9 +783,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                     out[j] = neg_inf;
                 }
             }
-            left -= je - c.j;
-            if (left > 0 && !c.next(p))
-                break;
+            more = w.next(p, ctl->rng);
         }
     }
 

@@ -11,7 +11,9 @@ prefill the pages in flight form at most two compact fronts per request.
 The bf16 kernel runs on pairs of CTAs (one range per pair) and multiplies a
 segment's pages two at a time: pair g of a segment [j, je) is pages j + 2 g
 (the even CTA's) and j + 2 g + 1 (the odd CTA's, absent past je); that
-grouping is replayed too.
+grouping is replayed too, with the pair kernel's ranges: on a batch of at
+least 2 G * 512 units pair g of G walks ranges g and then g + G of a 2G-way
+split, else range g of G.
 """
 
 import numpy as np
@@ -280,3 +282,65 @@ def test_pair_counts_on_the_chunked_prefill():
         halves += sum(1 for p in pairs if p[3] is None)
     assert max(counts) - min(counts) <= 2
     assert halves <= 2 * 76
+
+
+SPLIT_UNITS = 512
+
+
+def pair_ranges(reqs, G, g):
+    """The pair kernel's ranges for pair g of G, in walking order."""
+    W = sum(req_units(n, L, ok) for n, L, ok in reqs)
+    if W >= 2 * G * SPLIT_UNITS:
+        return [plan(reqs, 2 * G, g), plan(reqs, 2 * G, g + G)]
+    return [plan(reqs, G, g)]
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_pair_ranges_cover_every_unit_once(seed):
+    rng = np.random.default_rng(700 + seed)
+    batches = [_random_batch(rng) for _ in range(30)]
+    batches.append([(2048, 131072, True)] * 4)  # the chunked prefill: two ranges a pair
+    batches.append([(16, 8192, True)] * 256)    # short requests: one range a pair
+    for reqs in batches:
+        expect = all_units(reqs)
+        for G in (1, 5, 76):
+            got = []
+            for g in range(G):
+                for start in pair_ranges(reqs, G, g):
+                    if start is not None:
+                        got.extend(walk(reqs, start))
+            assert sorted(got) == expect, (reqs, G)
+    W = sum(req_units(n, L, ok) for n, L, ok in batches[-2])
+    assert W >= 2 * 76 * SPLIT_UNITS
+    W = sum(req_units(n, L, ok) for n, L, ok in batches[-1])
+    assert W < 2 * 76 * SPLIT_UNITS
+
+
+def test_two_ranges_keep_the_pages_of_a_request_together():
+    """Chunked prefill on 76 pairs, one unit a pair per step, an LRU cache of
+    1000 pages (31 MiB): with ranges g and g + 76 of 152 every page is missed
+    once; one range of twice the length per pair misses ~9 times as often."""
+    import collections
+    reqs = [(2048, 131072, True)] * 4
+
+    def misses(walks, cap=1000):
+        lru, miss, pos = collections.OrderedDict(), 0, [0] * len(walks)
+        while any(p < len(w) for p, w in zip(pos, walks)):
+            for i, w in enumerate(walks):
+                if pos[i] < len(w):
+                    b, _, j = w[pos[i]]
+                    pos[i] += 1
+                    if (b, j) in lru:
+                        lru.move_to_end((b, j))
+                    else:
+                        miss += 1
+                        lru[(b, j)] = 1
+                        if len(lru) > cap:
+                            lru.popitem(last=False)
+        return miss
+
+    two = [sum((walk(reqs, r) for r in pair_ranges(reqs, 76, g)), []) for g in range(76)]
+    one = [walk(reqs, plan(reqs, 76, g)) for g in range(76)]
+    pages = 4 * 1024
+    assert misses(two) == pages
+    assert misses(one) > 5 * pages
