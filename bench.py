@@ -878,8 +878,8 @@ def run_prefill_bench(args):
             "total_q": total, "useful_flops_per_step": flops, "parallelism": f"replicas x{world}",
             "timing": "one CUDA graph of K consecutive prefill calls (score + top-k kernels), "
                       "CUDA events on the stream",
-            "l2": "index-K pool 128 MiB + 128 MiB of block scores written per step vs 129 MB L2; "
-                  "no flush",
+            "l2": ("index-K pool 66 MiB (codes + scales)" if fp8 else "index-K pool 128 MiB")
+                  + " + 128 MiB of block scores written per step vs 129 MB L2; no flush",
         },
         "roofline": {
             "bound": "tensor", "kernel": "tc_prefill_fp8_kernel" if fp8 else "tc_prefill_pair_kernel",

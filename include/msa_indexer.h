@@ -47,9 +47,9 @@
  * selection.  Both set a bit in the workspace fault word, read (and cleared)
  * by msa_indexer_get_error().  No kernel traps or waits without bound: every
  * wait inside a kernel gives up after a fixed number of polls and sets
- * MSA_FAULT_TIMEOUT; the merge of a pass in which that happened writes -1 /
- * -inf to every output row, and the workspace stays usable for the next
- * call.
+ * MSA_FAULT_TIMEOUT; the merge (decode) or the top-k (prefill) of a pass in
+ * which that happened writes -1 / -inf to every output row, and the workspace
+ * stays usable for the next call.
  *
  * Concurrency.  The library keeps no state between calls except in the
  * caller's workspace.  Calls that may overlap on the GPU need separate
@@ -356,7 +356,8 @@ msa_status msa_indexer_prefill_score_fp8(const void *q, const int32_t *cu_seqlen
  * The block-score half of msa_indexer_prefill: writes out_block_scores
  * (required, fp32 [total_q, 4, ceil(max_model_len/128)], each token's
  * visible blocks only) and nothing else.  The workspace needs only its
- * 256-byte header (the fault word).  One kernel.
+ * 256-byte header (the fault word and pass count).  After MSA_FAULT_TIMEOUT
+ * the block scores of that pass are incomplete.  One kernel.
  */
 msa_status msa_indexer_prefill_score(const void *q, const int32_t *cu_seqlens_q, int total_q,
                                      const void *kcache_pool, int64_t num_pages,
@@ -391,16 +392,19 @@ msa_status msa_indexer_get_error(void *workspace, void *stream, uint32_t *flags)
 
 /*
  * Test hook for the bounded waits.  No passage of the pages corresponds; it
- * exists so that a test can make the decode kernel's waits run out without
- * any fault: while `on` is non-zero, bf16 one-position decode and score
- * passes with k <= 16 enqueued afterwards run a separately built copy of the
- * score kernel that loads no index-K page and never signals one, so every
+ * exists so that a test can make the kernels' waits run out without any
+ * fault: while `on` is non-zero, bf16 one-position decode and score passes
+ * with k <= 16 enqueued afterwards run a separately built copy of the score
+ * kernel that loads no index-K page and never signals one, so every
  * consumer's first page wait runs out after a short poll limit (2^14 polls)
- * instead of the normal one; no asynchronous copy is in flight at any time.
- * The pass then sets MSA_FAULT_TIMEOUT and its merge writes -1 / -inf to
- * every output row.  Other shapes return MSA_ERR_UNSUPPORTED while it is
- * set.  Set it back to 0 for normal operation.  The flag is process-wide:
- * do not set it while other threads run decode calls.
+ * instead of the normal one; bf16 prefill and prefill-score passes likewise
+ * run a copy of the prefill scoring kernel that loads no query row and no
+ * page.  No asynchronous copy is in flight at any time.  The pass then sets
+ * MSA_FAULT_TIMEOUT, and its merge or top-k writes -1 / -inf to every output
+ * row (a prefill-score pass leaves its block scores incomplete).  Other
+ * shapes, and the E4M3 prefill, return MSA_ERR_UNSUPPORTED while it is set.
+ * Set it back to 0 for normal operation.  The flag is process-wide: do not
+ * set it while other threads run calls.
  */
 void msa_indexer_test_withhold_pages(int on);
 

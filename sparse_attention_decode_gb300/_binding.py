@@ -427,7 +427,7 @@ def msa_indexer_prefill_score_fp8(q, cu_seqlens_q, kcache_fp8, kscale, block_tab
 
 
 def msa_indexer_test_withhold_pages(on: bool) -> None:
-    """Test hook: while set, decode passes load no page and their waits run out (see the C header)."""
+    """Test hook: while set, bf16 decode and prefill passes load nothing and their waits run out (see the C header)."""
     load().msa_indexer_test_withhold_pages(1 if on else 0)
 
 

@@ -1157,8 +1157,11 @@ static int score_grid(int sms, int batch, int64_t max_blocks, int split_blocks)
 
 // Test hook for the bounded waits (msa_indexer_test_withhold_pages): while it
 // is set, bf16 one-position passes with k <= 16 run score_kernel<16, Bf16Fmt,
-// 1, true> (no page loaded, short waits); other shapes are refused.
+// 1, true> (no page loaded, short waits) and bf16 prefill passes the pair
+// kernel's copy that loads nothing; other shapes are refused.
 static std::atomic<int> g_withhold_pages{0};
+
+bool test_withhold_pages() { return g_withhold_pages.load(std::memory_order_relaxed) != 0; }
 
 // The pool as a 2-D tensor map: rows = num_pages * 128 tokens, 128 elements
 // per row, 128-byte swizzle.  bf16: 64x128 boxes (two per page); fp8

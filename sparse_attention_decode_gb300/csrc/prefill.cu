@@ -57,6 +57,7 @@ struct TcParams {
     const int32_t *seq_lens;
     float *scores;  // [total_q, 4, bs_stride]
     uint32_t *fault;
+    WorkspaceHeader *hdr;  // fault word, pass count and aborted pass of the workspace
     int64_t bt_stride;
     int64_t bs_stride;
     int64_t num_pages;
@@ -294,6 +295,48 @@ __device__ __forceinline__ void give_up(const TcParams &p, Ctl *ctl)
     *reinterpret_cast<volatile int *>(&ctl->abort) = 1;
 }
 
+// Pass bookkeeping in the workspace header, as the decode kernels keep it:
+// thread 0 of each CTA reads the pass count once the previous kernel on the
+// stream has finished; at its exit a CTA that gave up records that count + 1
+// as the aborted pass, and the last CTA to finish bumps the count.  The top-k
+// kernel that follows compares the two and writes -1 / -inf to every row of a
+// pass that gave up (its block scores are incomplete).
+template <class Ctl>
+__device__ __forceinline__ void pass_start(const TcParams &p, Ctl *ctl)
+{
+    ctl->epoch = __ldcg(&p.hdr->epoch);
+}
+
+// Thread 0 of each CTA, after a barrier that every thread of the CTA reached
+// once all its waits had ended.
+template <class Ctl>
+__device__ __forceinline__ void pass_end(const TcParams &p, const Ctl *ctl)
+{
+    if (aborted(ctl))
+        atomicExch(&p.hdr->aborted, ctl->epoch + 1u);
+    __threadfence();
+    if (atomicAdd(&p.hdr->done, 1u) == gridDim.x - 1) {
+        atomicExch(&p.hdr->done, 0u);
+        atomicAdd(&p.hdr->epoch, 1u);
+    }
+}
+
+// Bounded waits.  The test copy of the pair kernel (TH = true, which loads
+// nothing) polls 2^14 times instead of the normal limit, so that its waits
+// run out quickly.
+constexpr uint32_t kTestSpinLimit = 1u << 14;
+template <bool TH>
+constexpr uint32_t kWaitPolls = TH ? kTestSpinLimit : kSpinLimit;
+
+template <bool TH>
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kWaitPolls<TH>; ++i)
+        if (mbar_try_wait(bar, parity))
+            return true;
+    return false;
+}
+
 // A shared-memory word published by one thread (release) and polled by
 // another (acquire), CTA scope.
 __device__ __forceinline__ uint32_t ld_acquire_shared_u32(uint32_t addr)
@@ -316,10 +359,10 @@ __device__ __forceinline__ void st_release_shared_u32(uint32_t addr, uint32_t v)
 // the ~1700 cycles a page took.  This load of a counter that is usually
 // already there is cheaper, and the waits happen on another warp.
 template <class Ctl>
-__device__ __forceinline__ bool wait_ready(Ctl *ctl, uint32_t need)
+__device__ __forceinline__ bool wait_ready(Ctl *ctl, uint32_t need, uint32_t limit = kSpinLimit)
 {
     const uint32_t addr = smem_addr(&ctl->ready);
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (ld_acquire_shared_u32(addr) >= need)
             return true;
         if (aborted(ctl))
@@ -383,6 +426,7 @@ struct P2Smem {
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t ready;  // even CTA: pairs of pages the issuing thread may multiply
+    uint32_t epoch;  // the workspace's pass count when this pass started
     int abort;
     UnitRange rng[2];  // the pair's two ranges of units, walked one after the other
 };
@@ -448,6 +492,7 @@ struct SegWalk {
     }
 };
 
+template <bool TH>
 __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __grid_constant__ TcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -481,6 +526,8 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
     }
     griddep_wait();
     griddep_launch_dependents();
+    if (threadIdx.x == 0)
+        pass_start(p, ctl);
     // On a large batch pair g of G takes ranges g and g + G of the units cut
     // 2G ways.  The first ranges of all pairs cover the first half of the
     // batch's units and the second ranges the rest, so at any time the pairs
@@ -505,8 +552,11 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
     __syncwarp();
     // both CTAs' barriers are initialised before either arrives on the other's
     cluster_sync_all();
-    if (ctl->rng[0].units + ctl->rng[1].units <= 0)
-        return;  // the same for both CTAs of the pair: no TMEM taken yet
+    if (ctl->rng[0].units + ctl->rng[1].units <= 0) {
+        if (threadIdx.x == 0)  // the same for both CTAs of the pair: no TMEM taken yet
+            pass_end(p, ctl);
+        return;
+    }
     if (warp == 1) {
         tmem_alloc_pair(smem_addr(&ctl->tmem_base), kP2TmemCols);
         tmem_relinquish_pair();
@@ -516,7 +566,10 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
     tc_fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
 
-    if (warp == 0) {
+    if (warp == 0 && TH) {
+        // test copy: no query row or page is loaded and no stage is signalled,
+        // so every wait on one runs out; no copy is ever in flight
+    } else if (warp == 0) {
         // ---------------- producer (both CTAs) ----------------
         SegWalk w;
         bool more = w.start(p, ctl->rng);
@@ -528,7 +581,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
             if (lane == 0) {
                 const int qb = static_cast<int>(seg % kP2QBufs);
                 if (seg >= kP2QBufs &&
-                    !mbar_wait(smem_addr(&ctl->q_empty[qb]), ((seg / kP2QBufs) - 1) & 1u)) {
+                    !bar_wait<TH>(smem_addr(&ctl->q_empty[qb]), ((seg / kP2QBufs) - 1) & 1u)) {
                     give_up(p, ctl);
                     ok_run = false;
                 } else {
@@ -562,7 +615,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                         const uint32_t full = smem_addr(&ctl->k_full[s]);
                         if (aborted(ctl) ||
                             (gc >= kP2Stages &&
-                             !mbar_wait(smem_addr(&ctl->k_empty[s]), ((gc / kP2Stages) - 1) & 1u))) {
+                             !bar_wait<TH>(smem_addr(&ctl->k_empty[s]), ((gc / kP2Stages) - 1) & 1u))) {
                             give_up(p, ctl);
                             good = 0;
                         } else if (pok) {
@@ -586,10 +639,10 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
         }
         if (lane == 0) {  // drain: no copy may land after the CTA exits
             for (uint32_t i = gc > kP2Stages ? gc - kP2Stages : 0; i < gc; ++i)
-                if (!mbar_wait(smem_addr(&ctl->k_full[i % kP2Stages]), (i / kP2Stages) & 1u))
+                if (!bar_wait<TH>(smem_addr(&ctl->k_full[i % kP2Stages]), (i / kP2Stages) & 1u))
                     give_up(p, ctl);
             for (uint32_t i = seg > kP2QBufs ? seg - kP2QBufs : 0; i < seg; ++i)
-                if (!mbar_wait(smem_addr(&ctl->q_full[i % kP2QBufs]), (i / kP2QBufs) & 1u))
+                if (!bar_wait<TH>(smem_addr(&ctl->q_full[i % kP2QBufs]), (i / kP2QBufs) & 1u))
                     give_up(p, ctl);
         }
     } else if (warp == 1) {
@@ -605,7 +658,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                     const int je = c.je;
                     const int qb = static_cast<int>(seg % kP2QBufs);
                     const uint32_t qph = (seg / kP2QBufs) & 1u;
-                    if (!mbar_wait(smem_addr(&ctl->q_full[qb]), qph) || !mbar_wait(smem_addr(&ctl->q_peer[qb]), qph)) {
+                    if (!bar_wait<TH>(smem_addr(&ctl->q_full[qb]), qph) || !bar_wait<TH>(smem_addr(&ctl->q_peer[qb]), qph)) {
                         give_up(p, ctl);
                         break;
                     }
@@ -614,7 +667,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                     for (int g = 0; g < ng; ++g) {
                         const int s = static_cast<int>(gc % kP2Stages);
                         const int a = static_cast<int>(gc % kP2AccBufs);
-                        if (!wait_ready(ctl, gc + 1)) {
+                        if (!wait_ready(ctl, gc + 1, kWaitPolls<TH>)) {
                             give_up(p, ctl);
                             ok_run = false;
                             break;
@@ -646,7 +699,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                 while (more && ok_run) {
                     const int je = c.je;
                     const int qb = static_cast<int>(seg % kP2QBufs);
-                    if (!mbar_wait(smem_addr(&ctl->q_full[qb]), (seg / kP2QBufs) & 1u)) {
+                    if (!bar_wait<TH>(smem_addr(&ctl->q_full[qb]), (seg / kP2QBufs) & 1u)) {
                         give_up(p, ctl);
                         break;
                     }
@@ -654,7 +707,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                     const int ng = pairs_of(c.j, je);
                     for (int g = 0; g < ng; ++g) {
                         const int s = static_cast<int>(gc % kP2Stages);
-                        if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->k_full[s]), (gc / kP2Stages) & 1u)) {
+                        if (aborted(ctl) || !bar_wait<TH>(smem_addr(&ctl->k_full[s]), (gc / kP2Stages) & 1u)) {
                             give_up(p, ctl);
                             ok_run = false;
                             break;
@@ -666,7 +719,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                     more = w.next(p, ctl->rng);
                 }
             }
-            if (!mbar_wait(smem_addr(&ctl->mma_done), 0))
+            if (!bar_wait<TH>(smem_addr(&ctl->mma_done), 0))
                 give_up(p, ctl);
         }
         __syncwarp();
@@ -685,10 +738,10 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                 for (int g = 0; g < ng; ++g) {
                     const int s = static_cast<int>(gc % kP2Stages);
                     const int a = static_cast<int>(gc % kP2AccBufs);
-                    if (aborted(ctl) || !mbar_wait(smem_addr(&ctl->k_full[s]), (gc / kP2Stages) & 1u) ||
-                        !mbar_wait(smem_addr(&ctl->k_peer[s]), (gc / kP2Stages) & 1u) ||
+                    if (aborted(ctl) || !bar_wait<TH>(smem_addr(&ctl->k_full[s]), (gc / kP2Stages) & 1u) ||
+                        !bar_wait<TH>(smem_addr(&ctl->k_peer[s]), (gc / kP2Stages) & 1u) ||
                         (gc >= kP2AccBufs &&
-                         !mbar_wait(smem_addr(&ctl->acc_empty[a]), ((gc / kP2AccBufs) - 1) & 1u))) {
+                         !bar_wait<TH>(smem_addr(&ctl->acc_empty[a]), ((gc / kP2AccBufs) - 1) & 1u))) {
                         give_up(p, ctl);
                         ok_run = false;
                         break;
@@ -729,7 +782,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
                 const int page = page_next;
                 if (j + 2 < je)
                     page_next = bt_row[j + 2];
-                bool ready = !aborted(ctl) && mbar_wait(smem_addr(&ctl->acc_full[a]), (gc / kP2AccBufs) & 1u);
+                bool ready = !aborted(ctl) && bar_wait<TH>(smem_addr(&ctl->acc_full[a]), (gc / kP2AccBufs) & 1u);
                 ready = __all_sync(0xffffffffu, ready);
                 if (!ready) {
                     if (lane == 0)
@@ -796,6 +849,8 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
         tc_fence_after_sync();
         tmem_dealloc_pair(tmem, kP2TmemCols);
     }
+    if (threadIdx.x == 0)
+        pass_end(p, ctl);
 }
 
 }  // namespace msa
@@ -804,6 +859,8 @@ __global__ void __launch_bounds__(kP2Threads, 1) tc_prefill_pair_kernel(const __
 #include "rows_topk.cuh"
 
 namespace msa {
+
+bool test_withhold_pages();  // msa_indexer.cu: the bounded-wait test hook is set
 
 // 2-D tensor map over the E4M3 codes: [num_pages*128 rows][128 B], one
 // 128x128-byte box per page, 128-byte swizzle.
@@ -858,7 +915,7 @@ static int pair_clusters(int dev, int sms)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_prefill_pair_kernel, &cfg) != cudaSuccess || n <= 0)
+    if (cudaOccupancyMaxActiveClusters(&n, tc_prefill_pair_kernel<false>, &cfg) != cudaSuccess || n <= 0)
         n = sms / 2;
     v = n < sms / 2 ? n : sms / 2;
     if (v < 1)
@@ -914,7 +971,8 @@ static msa_status prefill_score_launch(const void *q, const int32_t *cu_seqlens_
     p.seq_lens = seq_lens;
     p.scores = out_block_scores ? out_block_scores
                                 : reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kHeaderBytes);
-    p.fault = &static_cast<WorkspaceHeader *>(workspace)->fault;
+    p.hdr = static_cast<WorkspaceHeader *>(workspace);
+    p.fault = &p.hdr->fault;
     p.bt_stride = bt_stride;
     p.bs_stride = bs_stride;
     p.num_pages = num_pages;
@@ -930,12 +988,15 @@ static msa_status prefill_score_launch(const void *q, const int32_t *cu_seqlens_
     const int sms = device_sms(dev);
     if (sms <= 0)
         return MSA_ERR_CUDA;
+    const bool withhold = test_withhold_pages();
+    if (withhold && fp8)
+        return MSA_ERR_UNSUPPORTED;
     static std::atomic<bool> attr_done[2][kMaxDevices];
     if (dev >= 0 && dev < kMaxDevices && !attr_done[fp8][dev].load(std::memory_order_acquire)) {
         const cudaError_t e =
             fp8 ? cudaFuncSetAttribute(tc_prefill_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kF8SmemBytes))
-                : cudaFuncSetAttribute(tc_prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                : cudaFuncSetAttribute(tc_prefill_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kP2SmemBytes));
         if (e != cudaSuccess)
             return MSA_ERR_CUDA;
@@ -967,7 +1028,13 @@ static msa_status prefill_score_launch(const void *q, const int32_t *cu_seqlens_
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, tc_prefill_pair_kernel, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+    if (withhold) {
+        if (cudaFuncSetAttribute(tc_prefill_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kP2SmemBytes)) != cudaSuccess)
+            return MSA_ERR_CUDA;
+        return cudaLaunchKernelEx(&cfg, tc_prefill_pair_kernel<true>, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+    }
+    return cudaLaunchKernelEx(&cfg, tc_prefill_pair_kernel<false>, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 
 extern "C" msa_status msa_indexer_prefill_score(const void *q, const int32_t *cu_seqlens_q,
@@ -1036,10 +1103,12 @@ static msa_status prefill_entry(const void *q, const int32_t *cu_seqlens_q, int 
                                          dim3(32 * kTopkRowsPerCta), kTopkSmemBytes, st, attr2);
     cudaError_t e = k16 ? cudaLaunchKernelEx(&cfg2, rows_topk_kernel<16>, static_cast<const float *>(p.scores),
                                              p.bs_stride, cu_seqlens_q, seq_lens, batch, total_q,
-                                             p.seq_limit, k, n_sink, n_window, out_ids, out_scores)
+                                             p.seq_limit, k, n_sink, n_window, out_ids, out_scores,
+                                             static_cast<const WorkspaceHeader *>(p.hdr))
                         : cudaLaunchKernelEx(&cfg2, rows_topk_kernel<32>, static_cast<const float *>(p.scores),
                                              p.bs_stride, cu_seqlens_q, seq_lens, batch, total_q,
-                                             p.seq_limit, k, n_sink, n_window, out_ids, out_scores);
+                                             p.seq_limit, k, n_sink, n_window, out_ids, out_scores,
+                                             static_cast<const WorkspaceHeader *>(p.hdr));
     return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
 }
 

@@ -65,6 +65,7 @@ struct F8Smem {
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t ready;  // pages the issuing thread may multiply (the waiter warp's count)
+    uint32_t epoch;  // the workspace's pass count when this pass started
     int abort;
     int b0, t0, j0;  // the range's first unit
     int b1, t1, j1;  // its last unit + 1 page
@@ -191,12 +192,17 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
     }
     griddep_wait();
     griddep_launch_dependents();
+    if (threadIdx.x == 0)
+        pass_start(p, ctl);
     if (warp == 0)
         plan_range(p, ctl, lane, gridDim.x, blockIdx.x);
     __syncthreads();
     const long long units = ctl->units;
-    if (units <= 0)
-        return;  // uniform: no TMEM taken yet
+    if (units <= 0) {
+        if (threadIdx.x == 0)  // uniform: no TMEM taken yet
+            pass_end(p, ctl);
+        return;
+    }
     if (warp == 1) {
         tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
         tmem_relinquish_alloc_permit();
@@ -570,6 +576,8 @@ __global__ void __maxnreg__(kF8MaxRegs) tc_prefill_fp8_kernel(const __grid_const
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
+    if (threadIdx.x == 0)
+        pass_end(p, ctl);
 }
 
 }  // namespace msa

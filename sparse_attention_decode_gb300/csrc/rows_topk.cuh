@@ -169,13 +169,17 @@ __device__ __forceinline__ void fetch_group(float *dst, const float *srow, int g
 template <int KMAX>
 __global__ void __launch_bounds__(32 * kTopkRowsPerCta, kTopkCtasPerSm) rows_topk_kernel(
     const float *scores, int64_t bs_stride, const int32_t *cu_q, const int32_t *seq_lens, int batch,
-    int total_q, int seq_limit, int k, int n_sink, int n_window, int32_t *out_ids, float *out_scores)
+    int total_q, int seq_limit, int k, int n_sink, int n_window, int32_t *out_ids, float *out_scores,
+    const WorkspaceHeader *hdr)
 {
     extern __shared__ __align__(16) uint8_t topk_smem_raw[];
     TopkSmem &sm = *reinterpret_cast<TopkSmem *>(topk_smem_raw);
     // No early trigger: the next kernel on the stream (a persistent scoring
     // grid) is released at this grid's exit.
     griddep_wait();
+    // a scoring pass whose wait ran out left its block scores incomplete:
+    // every row of it is then written empty (-1 / -inf)
+    const bool pass_ok = __ldcg(&hdr->aborted) != __ldcg(&hdr->epoch);
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int64_t rows = static_cast<int64_t>(total_q) * kHeads;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kTopkRowsPerCta;
@@ -208,7 +212,8 @@ __global__ void __launch_bounds__(32 * kTopkRowsPerCta, kTopkCtasPerSm) rows_top
             }
             r = req_info(cu_q, seq_lens, total_q, seq_limit, lo);
         }
-        return (r.ok && r.c0 <= tok && tok < r.c0 + r.n) ? (r.len - r.n + (tok - r.c0)) / kPage + 1 : 0;
+        return (pass_ok && r.ok && r.c0 <= tok && tok < r.c0 + r.n) ? (r.len - r.n + (tok - r.c0)) / kPage + 1
+                                                                    : 0;
     };
 
     int64_t rw = static_cast<int64_t>(blockIdx.x) * kTopkRowsPerCta + wid;

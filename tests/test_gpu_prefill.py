@@ -41,7 +41,8 @@ def prefill_case(pairs, seed, *, ternary=False, max_model_len=None, num_pages=No
     return w, q, cu
 
 
-def run_prefill(msa, w, q_bits, cu, k=16, n_sink=1, n_window=2, block_scores=True, ws_pad=0):
+def run_prefill(msa, w, q_bits, cu, k=16, n_sink=1, n_window=2, block_scores=True, ws_pad=0,
+                ws=None):
     import torch
     total = q_bits.shape[0]
     q = torch.from_numpy(q_bits.view(np.int16)).view(torch.bfloat16).cuda()
@@ -55,8 +56,9 @@ def run_prefill(msa, w, q_bits, cu, k=16, n_sink=1, n_window=2, block_scores=Tru
     blk = None
     if block_scores:
         blk = torch.full((total, 4, stride), float("nan"), dtype=torch.float32, device="cuda")
-    n = msa.msa_indexer_prefill_workspace_bytes(total, w.max_model_len)
-    ws = torch.zeros(n + ws_pad, dtype=torch.uint8, device="cuda")
+    if ws is None:
+        n = msa.msa_indexer_prefill_workspace_bytes(total, w.max_model_len)
+        ws = torch.zeros(n + ws_pad, dtype=torch.uint8, device="cuda")
     msa.msa_indexer_prefill(q, d_cu, pool, bt, seq, k, n_sink, n_window, ids, sc, ws,
                             max_model_len=w.max_model_len, out_block_scores=blk)
     fault = msa.msa_indexer_get_error(ws)
@@ -168,6 +170,43 @@ def test_prefill_bad_page_and_bad_rows(msa, orc):
     assert fault2 & msa.MSA_FAULT_SEQ_LEN
     assert (ids2[8:] == -1).all() and np.isneginf(sc2[8:]).all()
     assert (ids2[:8, :, 0] >= 0).all()
+
+
+def test_prefill_waits_that_run_out_empty_every_row(msa, orc):
+    """The bounded-wait hook on the prefill path, made without any fault: while
+    it is set the bf16 scoring kernel loads no query row and no page (no copy
+    is ever in flight), so its first waits run out after the short poll limit.
+    The call must return and report MSA_FAULT_TIMEOUT, and its top-k must write
+    every row empty although some block scores were never written.  The same
+    workspace then matches the oracle twice (the pass count and the finish
+    counter in its header were left consistent); the E4M3 prefill is refused
+    while the hook is set."""
+    import torch
+    w, q, cu = prefill_case(MIXED, seed=262, max_model_len=8192)
+    total = q.shape[0]
+    ws = torch.zeros(msa.msa_indexer_prefill_workspace_bytes(total, w.max_model_len),
+                     dtype=torch.uint8, device="cuda")
+    msa.msa_indexer_test_withhold_pages(True)
+    try:
+        ids, sc, _, fault, _ = run_prefill(msa, w, q, cu, ws=ws)
+        codes = torch.zeros((w.num_pages, 128, 128), dtype=torch.uint8, device="cuda")
+        scales = torch.ones((w.num_pages, 128), dtype=torch.float32, device="cuda")
+        d = [torch.from_numpy(x).cuda() for x in (w.block_table, w.seq_lens, cu)]
+        qd = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).cuda()
+        out_i = torch.empty((total, 4, 16), dtype=torch.int32, device="cuda")
+        out_s = torch.empty((total, 4, 16), dtype=torch.float32, device="cuda")
+        with pytest.raises(msa.MsaError) as e:
+            msa.msa_indexer_prefill_fp8(qd, d[2], codes, scales, d[0], d[1], 16, 1, 2, out_i, out_s,
+                                        ws, max_model_len=w.max_model_len)
+        assert e.value.status == msa.MSA_ERR_UNSUPPORTED
+    finally:
+        msa.msa_indexer_test_withhold_pages(False)
+    assert fault & msa.MSA_FAULT_TIMEOUT
+    assert (ids == -1).all() and np.isneginf(sc).all()
+    for _ in range(2):
+        got = run_prefill(msa, w, q, cu, ws=ws)
+        assert got[3] == 0
+        check_prefill(orc, w, q, cu, got)
 
 
 def test_prefill_outputs_do_not_spill(msa):
