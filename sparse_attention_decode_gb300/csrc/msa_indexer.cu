@@ -62,6 +62,10 @@ struct Bf16Fmt {
 // bf16 pages for four query positions: 16 columns double each page's MMAs,
 // so four consumer warps (one per SM sub-partition, one 32 KiB stage each)
 // share the pages; measured 202 -> 175 us per call on the long-context batch.
+// One-position passes of a few pages per SM use it too (wide_pass): there
+// the pages come from L2 and the consumers' scoring, not HBM, sets the pace
+// (16 x 8700 tokens: 10.35 -> 9.73 us a call; 32 x 128K tokens, which
+// needs three stages per consumer to keep HBM busy, 155.6 -> 156.3 us).
 struct Bf16Wide4Fmt {
     static constexpr bool kFp8 = false;
     static constexpr int kConsumers = 4;
@@ -995,34 +999,87 @@ __device__ __forceinline__ void expand_row(const ExpandArgs &ex, int b, size_t r
 constexpr int kMergeThreads = 256;
 constexpr int kMergeTileKeys = 2048;  // 16 KiB of keys staged per pass
 
+// What a decode call tells its merge beyond the workspace: with the lengths
+// (batch <= kMergeThreads) each merge CTA finds its request's page range and
+// the pass's chunking itself, before the score grid has finished, instead of
+// reading them from the workspace after it.  Null seq_lens: the workspace.
+struct MergeHint {
+    const int32_t *seq_lens;
+    int seq_limit;
+    int grid;          // the score grid
+    int split_blocks;
+};
+
 template <int KMAX>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const uint8_t *ws, int batch, int k,
                                                               int cols, int slot_capacity,
                                                               int32_t *out_ids, float *out_scores,
-                                                              const ExpandArgs ex)
+                                                              const ExpandArgs ex, const MergeHint hint)
 {
     constexpr int kGroups = kMergeThreads / KMAX;
     constexpr int kTileLists = kMergeTileKeys / KMAX;
     __shared__ uint64_t tile[kMergeTileKeys];
     __shared__ uint64_t tree[kMergeThreads];
-    // the score grid's workspace writes are complete and visible after this
-    griddep_wait();
-    griddep_launch_dependents();
+    __shared__ int sums[2][kMergeThreads / 32];
 
     const int h = blockIdx.x, b = blockIdx.y;
     const int lane = threadIdx.x & 31, grp = threadIdx.x / KMAX, rank = threadIdx.x % KMAX;
     const WorkspaceHeader *hdr = reinterpret_cast<const WorkspaceHeader *>(ws);
-    const int *prefix = reinterpret_cast<const int *>(ws + prefix_offset());
     const uint64_t *slots = reinterpret_cast<const uint64_t *>(ws + slots_offset(batch));
 
-    const Partition &part = hdr->part;
-    const int p0 = prefix[b], p1 = prefix[b + 1];
+    int c_first = 0, n_lists = 0;
+    if (hint.seq_lens != nullptr) {
+        // The lengths are inputs of the call: whatever wrote them finished
+        // before the score grid got past its own wait, and only then was this
+        // grid released.  Pages before this request and in the whole batch,
+        // as the score kernel counts them.
+        int pg = 0;
+        if (threadIdx.x < batch) {
+            const int L = hint.seq_lens[threadIdx.x];
+            pg = (L < 0 || L > hint.seq_limit) ? 0 : (L + kPage - 1) / kPage;
+        }
+        const int mine = __shfl_sync(0xffffffffu, pg, b & 31);  // valid in the warp holding b
+        int before = threadIdx.x < b ? pg : 0, all = pg;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            before += __shfl_xor_sync(0xffffffffu, before, o);
+            all += __shfl_xor_sync(0xffffffffu, all, o);
+        }
+        if (lane == 0) {
+            sums[0][threadIdx.x >> 5] = before;
+            sums[1][threadIdx.x >> 5] = all;
+        }
+        if ((threadIdx.x >> 5) == (b >> 5) && lane == 0)
+            tree[0] = static_cast<uint64_t>(mine);
+        __syncthreads();
+        int p0 = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < kMergeThreads / 32; ++w) {
+            p0 += sums[0][w];
+            total += sums[1][w];
+        }
+        const int p1 = p0 + static_cast<int>(tree[0]);
+        __syncthreads();
+        const Partition part = Partition::make(total, hint.grid, hint.split_blocks);
+        if (p1 > p0 && part.unit > 0 && p1 <= part.total) {
+            c_first = part.chunk_of(p0);
+            n_lists = min(part.chunk_of(p1 - 1) - c_first + 1, slot_capacity);
+        }
+    }
+    // the score grid's workspace writes are complete and visible after this
+    griddep_wait();
+    griddep_launch_dependents();
+
     // a wait of the score pass ran out: its lists are incomplete, every row is left empty
     const bool pass_ok = hdr->aborted != hdr->epoch;
-    int c_first = 0, n_lists = 0;
-    if (pass_ok && p1 > p0 && part.unit > 0 && p1 <= part.total) {
-        c_first = part.chunk_of(p0);
-        n_lists = min(part.chunk_of(p1 - 1) - c_first + 1, slot_capacity);
+    if (hint.seq_lens == nullptr) {
+        const int *prefix = reinterpret_cast<const int *>(ws + prefix_offset());
+        const Partition &part = hdr->part;
+        const int p0 = prefix[b], p1 = prefix[b + 1];
+        if (pass_ok && p1 > p0 && part.unit > 0 && p1 <= part.total) {
+            c_first = part.chunk_of(p0);
+            n_lists = min(part.chunk_of(p1 - 1) - c_first + 1, slot_capacity);
+        }
     }
 
     uint64_t run = 0;
@@ -1057,6 +1114,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const uint8_t *ws,
         tree[threadIdx.x] = run;
         __syncthreads();
     }
+    if (!pass_ok)
+        run = 0;  // the empty key
     int id = -1;
     if (grp == 0 && rank < k) {
         float score;
@@ -1264,6 +1323,18 @@ static msa_status plan(int batch, int max_batch, int max_model_len, int k, int s
     return MSA_OK;
 }
 
+// A one-position bf16 pass whose bound is one to 64 pages per SM runs the
+// four-consumer format (Bf16Wide4Fmt).  Fewer pages than SMs leave most
+// CTAs one page or none, where the wider CTA only costs.
+constexpr int64_t kWideMaxPagesPerSm = 64;
+static bool wide_pass(int batch, int max_model_len, int dev)
+{
+    const int64_t work = static_cast<int64_t>(batch) * blocks_for(max_model_len);
+    const int sms = device_sms(dev);
+    return !g_withhold_pages.load(std::memory_order_relaxed) && sms > 0 && work >= sms &&
+           work <= kWideMaxPagesPerSm * sms;
+}
+
 template <class F, int NQ = 1>
 static msa_status score_entry(const void *q, const void *kcache_pool, const float *kscale,
                               int64_t num_pages, const int32_t *block_table, int64_t bt_stride,
@@ -1285,6 +1356,19 @@ static msa_status score_entry(const void *q, const void *kcache_pool, const floa
     if (st != MSA_OK)
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if constexpr (std::is_same<F, Bf16Fmt>::value && NQ == 1) {
+        if (wide_pass(batch, max_model_len, pl.dev)) {
+            if (kmax_for(k) == 16)
+                return launch_score<16, Bf16Wide4Fmt, 1>(q, kcache_pool, kscale, num_pages, block_table,
+                                                         bt_stride, seq_lens, batch, max_model_len, n_sink,
+                                                         n_window, out_block_scores, workspace,
+                                                         pl.slot_capacity, pl.grid, split_blocks, s, pl.dev);
+            return launch_score<32, Bf16Wide4Fmt, 1>(q, kcache_pool, kscale, num_pages, block_table,
+                                                     bt_stride, seq_lens, batch, max_model_len, n_sink,
+                                                     n_window, out_block_scores, workspace,
+                                                     pl.slot_capacity, pl.grid, split_blocks, s, pl.dev);
+        }
+    }
     if (kmax_for(k) == 16)
         return launch_score<16, F, NQ>(q, kcache_pool, kscale, num_pages, block_table, bt_stride,
                                        seq_lens, batch, max_model_len, n_sink, n_window,
@@ -1346,8 +1430,10 @@ extern "C" msa_status msa_indexer_score_fp8(const void *q, const void *kcache_fp
 
 static msa_status merge_entry(int batch, int k, int cols, int32_t *out_ids, float *out_scores,
                               const void *workspace, size_t workspace_bytes, void *stream,
-                              const ExpandArgs &ex = ExpandArgs{})
+                              const ExpandArgs &ex = ExpandArgs{}, MergeHint hint = MergeHint{})
 {
+    if (batch > kMergeThreads)
+        hint.seq_lens = nullptr;
     if (!out_ids || !out_scores || !workspace || batch < 0 || batch > MSA_MAX_BATCH)
         return MSA_ERR_INVALID_ARG;
     if (k < 1)
@@ -1372,10 +1458,29 @@ static msa_status merge_entry(int batch, int k, int cols, int32_t *out_ids, floa
                                         dim3(kMergeThreads), 0, s, attr);
     cudaError_t e = kmax == 16
                         ? cudaLaunchKernelEx(&cfg, merge_kernel<16>, ws, batch, k, cols, capacity,
-                                             out_ids, out_scores, ex)
+                                             out_ids, out_scores, ex, hint)
                         : cudaLaunchKernelEx(&cfg, merge_kernel<32>, ws, batch, k, cols, capacity,
-                                             out_ids, out_scores, ex);
+                                             out_ids, out_scores, ex, hint);
     return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
+}
+
+// The hint a decode call passes its merge: the lengths, their limit and the
+// score grid and split its score pass was launched with (as plan() sizes it).
+static MergeHint merge_hint(const int32_t *seq_lens, int batch, int64_t bt_stride, int max_model_len,
+                            int split_blocks)
+{
+    MergeHint h{nullptr, 0, 0, 0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return h;
+    const int sms = device_sms(dev);
+    if (sms <= 0)
+        return h;
+    h.seq_lens = seq_lens;
+    h.seq_limit = static_cast<int>(bt_stride * kPage < max_model_len ? bt_stride * kPage : max_model_len);
+    h.grid = score_grid(sms, batch, blocks_for(max_model_len), split_blocks);
+    h.split_blocks = split_blocks;
+    return h;
 }
 
 extern "C" msa_status msa_indexer_merge(int batch, int k, int32_t *out_ids, float *out_scores,
@@ -1401,7 +1506,8 @@ extern "C" msa_status msa_indexer_decode(const void *q, const void *kcache_pool,
                                       stream);
     if (st != MSA_OK || batch == 0)
         return st;
-    return msa_indexer_merge(batch, k, out_ids, out_scores, workspace, workspace_bytes, stream);
+    return merge_entry(batch, k, kHeads, out_ids, out_scores, workspace, workspace_bytes, stream,
+                       ExpandArgs{}, merge_hint(seq_lens, batch, bt_stride, max_model_len, split_blocks));
 }
 
 // ---------------------------------------------------------------------------
@@ -1506,7 +1612,8 @@ extern "C" msa_status msa_indexer_decode_pages(
         return st;
     const ExpandArgs ex{seq_lens, kv_block_table, kv_bt_stride, kPage / page_tokens, page_tokens,
                         out_pages, out_num_pages};
-    return merge_entry(batch, k, kHeads, out_ids, out_scores, workspace, workspace_bytes, stream, ex);
+    return merge_entry(batch, k, kHeads, out_ids, out_scores, workspace, workspace_bytes, stream, ex,
+                       merge_hint(seq_lens, batch, bt_stride, max_model_len, split_blocks));
 }
 
 extern "C" msa_status msa_indexer_decode_mq(const void *q, int q_len, const void *kcache_pool,
@@ -1542,7 +1649,8 @@ extern "C" msa_status msa_indexer_decode_mq(const void *q, int q_len, const void
     if (st != MSA_OK || batch == 0)
         return st;
     return merge_entry(batch, k, kHeads * q_len, out_ids, out_scores, workspace, workspace_bytes,
-                       stream);
+                       stream, ExpandArgs{},
+                       merge_hint(seq_lens, batch, bt_stride, max_model_len, split_blocks));
 }
 
 extern "C" msa_status msa_indexer_decode_mq_fp8(const void *q, int q_len, const void *kcache_fp8,
@@ -1580,7 +1688,8 @@ extern "C" msa_status msa_indexer_decode_mq_fp8(const void *q, int q_len, const 
     if (st != MSA_OK || batch == 0)
         return st;
     return merge_entry(batch, k, kHeads * q_len, out_ids, out_scores, workspace, workspace_bytes,
-                       stream);
+                       stream, ExpandArgs{},
+                       merge_hint(seq_lens, batch, bt_stride, max_model_len, split_blocks));
 }
 
 extern "C" msa_status msa_indexer_decode_fp8(const void *q, const void *kcache_fp8,
@@ -1601,7 +1710,8 @@ extern "C" msa_status msa_indexer_decode_fp8(const void *q, const void *kcache_f
                                           split_blocks, stream);
     if (st != MSA_OK || batch == 0)
         return st;
-    return msa_indexer_merge(batch, k, out_ids, out_scores, workspace, workspace_bytes, stream);
+    return merge_entry(batch, k, kHeads, out_ids, out_scores, workspace, workspace_bytes, stream,
+                       ExpandArgs{}, merge_hint(seq_lens, batch, bt_stride, max_model_len, split_blocks));
 }
 
 extern "C" void msa_indexer_test_withhold_pages(int on)

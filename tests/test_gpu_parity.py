@@ -94,6 +94,22 @@ def test_shape_bound_is_bitwise_invariant(lib):
     assert a[3] == 0 and b[3] == 0
 
 
+def test_four_and_two_consumer_formats_agree(lib, orc):
+    """A one-position bf16 pass of one to 64 pages per SM (decode_point: 16 x 68
+    blocks against 152 SMs) runs four consumer warps with one stage each;
+    sized for a 16x longer context (16 x 1088 blocks) the same call runs two
+    warps with three stages.  Block scores, ids and scores are bit-identical,
+    and both match the oracle."""
+    w = wl.decode_point()
+    a = parity.run_gpu(w)
+    b = parity.run_gpu(w, max_model_len=16 * w.max_model_len)
+    for x, y in zip(a[:3], b[:3]):
+        np.testing.assert_array_equal(x, y)
+    assert a[3] == 0 and b[3] == 0
+    o_scores, o_ids, _ = orc.run(w)
+    parity.check(w, o_scores, o_ids, a[0], a[1], a[2])
+
+
 def test_graph_replay_with_changed_lengths(lib, orc):
     """Capture once at one set of lengths; replay after changing lengths and tables."""
     import torch
