@@ -194,12 +194,17 @@ __device__ __forceinline__ int find_row(const int *prefix, int batch, int p)
     return lo;
 }
 
+// Pages of a request of L tokens; a length outside [0, seq_limit] is an
+// empty request.  The score kernel's prefix and a decode call's merge both
+// count pages with this rule.
+__device__ __forceinline__ int pages_for_length(int L, int seq_limit)
+{
+    return (L < 0 || L > seq_limit) ? 0 : (L + kPage - 1) / kPage;
+}
+
 __device__ __forceinline__ int pages_of_request(const ScoreParams &p, int b)
 {
-    const int L = p.seq_lens[b];
-    if (L < 0 || L > p.seq_limit)
-        return 0;
-    return (L + kPage - 1) / kPage;
+    return pages_for_length(p.seq_lens[b], p.seq_limit);
 }
 
 // a1: prefix[b] = pages of requests 0..b-1, computed by every CTA from the
@@ -1034,10 +1039,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const uint8_t *ws,
         // grid released.  Pages before this request and in the whole batch,
         // as the score kernel counts them.
         int pg = 0;
-        if (threadIdx.x < batch) {
-            const int L = hint.seq_lens[threadIdx.x];
-            pg = (L < 0 || L > hint.seq_limit) ? 0 : (L + kPage - 1) / kPage;
-        }
+        if (threadIdx.x < batch)
+            pg = pages_for_length(hint.seq_lens[threadIdx.x], hint.seq_limit);
         const int mine = __shfl_sync(0xffffffffu, pg, b & 31);  // valid in the warp holding b
         int before = threadIdx.x < b ? pg : 0, all = pg;
 #pragma unroll
@@ -1202,6 +1205,12 @@ static msa_status validate(const void *q, const void *kcache_pool, int64_t num_p
     return MSA_OK;
 }
 
+// The longest request the block table and max_model_len allow.
+static int seq_limit_for(int64_t bt_stride, int max_model_len)
+{
+    return static_cast<int>(bt_stride * kPage < max_model_len ? bt_stride * kPage : max_model_len);
+}
+
 static int score_grid(int sms, int batch, int64_t max_blocks, int split_blocks)
 {
     const int64_t work = static_cast<int64_t>(batch) * max_blocks;
@@ -1267,8 +1276,7 @@ static msa_status launch_score(const void *q, const void *kcache_pool, const flo
     p.bt_stride = bt_stride;
     p.num_pages = num_pages;
     p.batch = batch;
-    const int64_t lim = bt_stride * kPage < max_model_len ? bt_stride * kPage : max_model_len;
-    p.seq_limit = static_cast<int>(lim);
+    p.seq_limit = seq_limit_for(bt_stride, max_model_len);
     p.n_sink = n_sink;
     p.n_window = n_window;
     p.split_blocks = split_blocks;
@@ -1477,7 +1485,7 @@ static MergeHint merge_hint(const int32_t *seq_lens, int batch, int64_t bt_strid
     if (sms <= 0)
         return h;
     h.seq_lens = seq_lens;
-    h.seq_limit = static_cast<int>(bt_stride * kPage < max_model_len ? bt_stride * kPage : max_model_len);
+    h.seq_limit = seq_limit_for(bt_stride, max_model_len);
     h.grid = score_grid(sms, batch, blocks_for(max_model_len), split_blocks);
     h.split_blocks = split_blocks;
     return h;
