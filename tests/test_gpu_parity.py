@@ -216,11 +216,17 @@ def test_max_batch(lib, orc):
     _compare(orc, w)
 
 
-@pytest.mark.parametrize("case", ["decode_point", "ragged", "k32", "split1", "max_batch"])
+@pytest.mark.parametrize("case", ["decode_point", "ragged", "k32", "split1", "b256", "b200_split3",
+                                  "b257", "max_batch"])
 def test_decode_equals_its_two_stages(lib, case):
     """msa_indexer_decode and msa_indexer_score followed by msa_indexer_merge
     must give bitwise-identical ids, scores and block scores, alternating on
-    one workspace (split 1 gives the long request up to 1024 lists)."""
+    one workspace (split 1 gives the long request up to 1024 lists).  Up to
+    256 requests the decode call's merge derives each request's page range and
+    the pass's chunking from the lengths itself, while the separate merge
+    reads what the score pass left in the workspace: b256 and b200_split3
+    (a forced split) take the first way over several warps of lengths, b257
+    and max_batch the second."""
     import torch
     k, split = 16, 0
     if case in ("decode_point", "ragged"):
@@ -229,6 +235,13 @@ def test_decode_equals_its_two_stages(lib, case):
         w, k = wl.decode_point(), 32
     elif case == "split1":
         w, split = wl.ragged(), 1  # up to 1024 lists for the long request
+    elif case in ("b256", "b200_split3", "b257"):
+        B = {"b256": 256, "b200_split3": 200, "b257": 257}[case]
+        rng = np.random.default_rng(B)
+        seq = rng.integers(0, 5000, B)
+        seq[rng.random(B) < 0.05] = 0
+        w = wl.random_workload(seq, seed=B, q_scale=1 / np.sqrt(128), max_model_len=8192)
+        split = 3 if case == "b200_split3" else 0
     else:
         rng = np.random.default_rng(7)
         seq = rng.integers(0, 3000, 1500)
