@@ -997,10 +997,12 @@ __device__ __forceinline__ void expand_row(const ExpandArgs &ex, int b, size_t r
         ex.out_num[row] = total;
 }
 
-// a7: one CTA per (query column, request): column = 4 * position + head.  The request's chunk lists are staged in
-// shared memory a tile at a time (all loads in flight together), each group of
-// KMAX lanes folds every kGroups-th list of the tile into a running top-KMAX,
-// and a tree over the groups yields the request's top-KMAX for the head.
+// a7: one CTA per (query column, request): column = 4 * position + head.  The
+// request's chunk lists are staged in shared memory a tile at a time (all of a
+// thread's loads in flight together); each group of KMAX lanes merges its
+// (up to 8) lists of the tile pairwise and folds the result into a running
+// top-KMAX, and a tree over the groups, whose first level (the two groups of
+// a warp, at KMAX 16) is a shuffle, yields the request's top-KMAX.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeTileKeys = 2048;  // 16 KiB of keys staged per pass
 
@@ -1085,29 +1087,67 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const uint8_t *ws,
         }
     }
 
+    constexpr int kPer = kMergeTileKeys / kMergeThreads;  // keys a thread stages per tile
+    constexpr int kLevels = 3;                              // lists per group per tile: <= 2^kLevels
+    static_assert(kTileLists == kGroups << kLevels, "a tile holds 8 lists per group");
+    auto rev = [&](uint64_t x) { return __shfl_sync(0xffffffffu, x, lane ^ (KMAX - 1)); };
     uint64_t run = 0;
     for (int t0 = 0; t0 < n_lists; t0 += kTileLists) {
         const int nt = min(kTileLists, n_lists - t0);
-        for (int e = threadIdx.x; e < nt * KMAX; e += kMergeThreads) {
-            const int li = e / KMAX, r = e % KMAX;
-            const int slot = c_first + t0 + li + b;
-            tile[e] = slot < slot_capacity
-                          ? slots[(static_cast<size_t>(slot) * cols + h) * KMAX + r]
-                          : 0ull;
+        // all of a thread's loads in flight at once, then the stores
+        uint64_t v[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int e = threadIdx.x + i * kMergeThreads;
+            const int slot = c_first + t0 + e / KMAX + b;
+            v[i] = (e < nt * KMAX && slot < slot_capacity)
+                       ? slots[(static_cast<size_t>(slot) * cols + h) * KMAX + e % KMAX]
+                       : 0ull;
         }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+            tile[threadIdx.x + i * kMergeThreads] = v[i];
         __syncthreads();
-        for (int base = 0; base < nt; base += kGroups) {
-            const int li = base + grp;
-            const uint64_t other = li < nt ? tile[li * KMAX + (KMAX - 1 - rank)] : 0ull;
-            run = merge_top<KMAX>(run, other, lane);
+        // group grp's lists grp + kGroups m (m < 8), merged pairwise: each level's
+        // merges are independent of one another, so their latencies overlap
+        // (folding them into one running list one by one does not)
+        const int per = (nt + kGroups - 1) / kGroups;  // lists per group, uniform over the CTA
+        auto list = [&](int m, bool reversed) {
+            const int li = grp + kGroups * m;
+            return li < nt ? tile[li * KMAX + (reversed ? KMAX - 1 - rank : rank)] : 0ull;
+        };
+        uint64_t a0 = list(0, false);
+        if (per > 1) {
+            uint64_t a2 = 0, a4 = 0, a6 = 0;
+            a0 = merge_top<KMAX>(a0, list(1, true), lane);
+            if (per > 2) {
+                a2 = merge_top<KMAX>(list(2, false), list(3, true), lane);
+                if (per > 4) {
+                    a4 = merge_top<KMAX>(list(4, false), list(5, true), lane);
+                    a6 = merge_top<KMAX>(list(6, false), list(7, true), lane);
+                    a4 = merge_top<KMAX>(a4, rev(a6), lane);
+                }
+                a0 = merge_top<KMAX>(a0, rev(a2), lane);
+                if (per > 4)
+                    a0 = merge_top<KMAX>(a0, rev(a4), lane);
+            }
         }
+        run = t0 == 0 ? a0 : merge_top<KMAX>(run, rev(a0), lane);
         __syncthreads();
+    }
+    const int used = min(n_lists, kGroups);  // groups holding anything
+    int first_step = 1;
+    if constexpr (KMAX == 16) {
+        // the two groups of a warp: each half merges the other's list, read
+        // reversed straight from its lanes
+        if (used > 1)
+            run = merge_top<KMAX>(run, __shfl_sync(0xffffffffu, run, lane ^ 31), lane);
+        first_step = 2;
     }
     tree[threadIdx.x] = run;
     __syncthreads();
-    const int used = min(n_lists, kGroups);  // groups holding anything
 #pragma unroll
-    for (int step = 1; step < kGroups; step <<= 1) {
+    for (int step = first_step; step < kGroups; step <<= 1) {
         if (step >= used)
             break;  // uniform across the CTA
         const bool active = (grp % (2 * step)) == 0 && grp + step < kGroups;
