@@ -912,7 +912,10 @@ __global__ void __launch_bounds__(Pipe<F>::kThreads, 1)
         prefetch_tensormap(&p.tmap);
     // Everything above touched only this CTA's shared memory and the kernel
     // parameters; global memory is read and written only after the previous
-    // kernel on the stream has finished.
+    // kernel on the stream has finished.  The merge grid is released only
+    // after this wait: a decode call's merge reads the call's lengths before
+    // its own wait, which is safe because whatever wrote them has finished
+    // by now.
     griddep_wait();
     griddep_launch_dependents();
 
