@@ -349,6 +349,19 @@ def test_prefill_many_requests(msa, orc):
     check_prefill(orc, w, q, cu, got)
 
 
+@pytest.mark.parametrize("max_len", [139264, 139392])
+def test_prefill_rows_just_past_one_group(msa, orc, max_len):
+    """Rows just past one group of 1024 blocks (a 128K context with a few
+    thousand new tokens): a second group of 1 to 64 blocks; rows of exactly
+    1024 and 1088 blocks sit on either side.  A row stride of 1089 blocks
+    takes the plain-load path."""
+    pairs = [(32, 133000), (8, 139264), (2, 131073)]
+    w, q, cu = prefill_case(pairs, seed=310 + max_len % 11, max_model_len=max_len)
+    got = run_prefill(msa, w, q, cu)
+    assert got[3] == 0
+    check_prefill(orc, w, q, cu, got)
+
+
 @pytest.mark.parametrize("max_len,k", [(300032, 16), (300160, 16), (300032, 32)])
 def test_prefill_rows_longer_than_one_group(msa, orc, max_len, k):
     """Rows of more than 1024 blocks (contexts past 128K tokens): the per-row
