@@ -16,7 +16,7 @@
 // whole batch, in order, are cut into one equal range per pair of CTAs (the
 // page counts have a closed form), which balances the causal triangle.  The
 // kernel itself is described where it is defined; tc_prefill_fp8_kernel
-// (prefill_fp8.cuh) does the same on the E4M3 cache with one CTA per SM.
+// (prefill_fp8.cuh) does the same on the E4M3 cache, also on pairs of SMs.
 //
 // rows_topk_kernel (rows_topk.cuh): one warp per (token, head) row: pins and
 // top-k over the row's block scores.
@@ -37,15 +37,10 @@
 
 namespace msa {
 
-constexpr int kTileTokens = 64;                       // new tokens per work tile
-constexpr int kMRows = 128;                           // rows per M tile: 32 tokens x 4 heads
-constexpr int kMTiles = kTileTokens * kHeads / kMRows;  // 2
-constexpr uint32_t kTmemCols = 512;                   // the whole tensor memory
-// E4M3 kernel (one CTA per SM): accumulator buffers of both M tiles x 128 keys
-constexpr int kAccBufs = kTmemCols / (kMTiles * kPage);
-static_assert(kPage % kTileTokens == 0 && kAccBufs >= 2, "tile geometry");
-constexpr int kQTileBytes = kMRows * kDim * 2;        // 32 KiB per M tile
-constexpr uint32_t kQBytes = kMTiles * kQTileBytes;
+constexpr int kTileTokens = 64;  // new tokens per work tile
+constexpr int kMRows = 128;      // rows each CTA of a pair multiplies: 32 tokens x 4 heads
+static_assert(kTileTokens * kHeads == 2 * kMRows && kPage % kTileTokens == 0,
+              "a tile's rows are split between the two CTAs of a pair");
 
 struct TcParams {
     CUtensorMap kmap;  // pool: bf16 [num_pages*128][128] in 64x128 boxes, or E4M3
@@ -894,8 +889,9 @@ static bool make_rows_map(CUtensorMap *map, const void *base, int64_t rows)
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Clusters of two the pair kernel runs: one per two SMs, fewer if the GPU
-// cannot hold that many at once (queried once per device).
+// Clusters of two the pair kernels run: one per two SMs, fewer if the GPU
+// cannot hold that many at once (queried once per device, on the bf16
+// kernel; the E4M3 one also holds one CTA an SM).
 static int pair_clusters(int dev, int sms)
 {
     static std::atomic<int> cache[kMaxDevices];
@@ -1006,13 +1002,7 @@ static msa_status prefill_score_launch(const void *q, const int32_t *cu_seqlens_
                           : make_rows_map(&p.kmap, kcache_pool, num_pages * kPage);
     if (!maps || !make_rows_map(&p.qmap, q, static_cast<int64_t>(total_q) * kHeads))
         return MSA_ERR_CUDA;
-    if (fp8) {
-        cudaLaunchAttribute attr[1];
-        cudaLaunchConfig_t cfg = pdl_config(dim3(static_cast<unsigned>(sms)), dim3(kF8Threads), kF8SmemBytes, st,
-                                            attr);
-        return cudaLaunchKernelEx(&cfg, tc_prefill_fp8_kernel, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
-    }
-    // clusters of two CTAs, with programmatic dependent launch
+    // both kernels: clusters of two CTAs, with programmatic dependent launch
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1023,11 +1013,13 @@ static msa_status prefill_score_launch(const void *q, const int32_t *cu_seqlens_
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pair_clusters(dev, sms)));
-    cfg.blockDim = dim3(kP2Threads);
-    cfg.dynamicSmemBytes = kP2SmemBytes;
+    cfg.blockDim = dim3(fp8 ? kF8Threads : kP2Threads);
+    cfg.dynamicSmemBytes = fp8 ? kF8SmemBytes : kP2SmemBytes;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
+    if (fp8)
+        return cudaLaunchKernelEx(&cfg, tc_prefill_fp8_kernel, p) == cudaSuccess ? MSA_OK : MSA_ERR_CUDA;
     if (withhold) {
         if (cudaFuncSetAttribute(tc_prefill_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kP2SmemBytes)) != cudaSuccess)
